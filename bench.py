@@ -1,0 +1,470 @@
+"""Benchmark of the block-scaled low-precision linear layer on one GB300 (per rank).
+
+One step = one pass of the layer's hot path over one batch of the dense
+Qwen3-4B-shaped MLP projection (tokens M = 8192, hidden 2560, intermediate
+9728), forward and backward:
+    dual (row + transposed) 1x128 quantisation of X [8192, 2560] and of
+    dY [8192, 9728], dual 128x128 quantisation of W [9728, 2560], then the
+    fprop, dgrad and wgrad block-scaled FP8 GEMMs (3 x 408.02 GFLOP).
+value = GEMM FLOPs of the step / step time (TFLOPS), inputs resident in HBM.
+The same run measures, as separate sub-results, the quantise sweep on a
+BF16 [8192, 4096] tensor (GB/s per granularity), the MoE grouped MXFP8 GEMM
+(Qwen3-30B-A3B shapes) and the NVFP4 linear (Qwen2.5-32B shapes), each
+against the roofline, plus the CPU oracle on a bounded sample of the step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+For N > 1 the driver launches one rank per GPU with torchrun; every rank
+runs its own batch (weak scaling, no collective on the data path) and rank 0
+prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M3, H3, I3 = 8192, 2560, 9728
+GEMM_FLOP = 2 * M3 * H3 * I3                    # one of fprop / dgrad / wgrad
+STEP_FLOP = 3 * GEMM_FLOP
+FP8_PER_BF16 = 2.0                              # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+FP4_PER_BF16 = 6.0                              # nominal dense ratio (13.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the sub-benchmarks")
+    return ap.parse_args()
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    return p
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------- inputs
+def device_inputs(torch, seed: int, dev):
+    """Seeded synthetic BF16 operands drawn on the device (same recipe as the
+    tests' generators: N(0,1) activations with 1% outliers x50, N(0,0.02)
+    weights), so that multi-GB workloads are built in milliseconds."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def act(shape, frac, mult):
+        z = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        u = torch.rand(shape, generator=g, device=dev, dtype=torch.float32)
+        return torch.where(u < frac, z * mult, z).to(torch.bfloat16)
+
+    def wt(shape, std=0.02):
+        return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    return act, wt
+
+
+class DenseStep:
+    """Buffers and launches of one fwd+bwd step of the blockwise FP8 linear."""
+
+    def __init__(self, torch, fp, dev, seed):
+        act, wt = device_inputs(torch, seed, dev)
+        self.torch, self.fp = torch, fp
+        self.x = act((M3, H3), 0.01, 50.0)
+        self.w = wt((I3, H3))
+        self.dy = act((M3, I3), 0.01, 50.0)
+        e = lambda *s, dt=torch.uint8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        f32 = torch.float32
+        self.qx, self.sx, self.qxt, self.sxt = e(M3, H3), e(M3, H3 // 128, dt=f32), e(H3, M3), e(H3, M3 // 128, dt=f32)
+        self.qw, self.sw = e(I3, H3), e(I3 // 128, H3 // 128, dt=f32)
+        self.qwt, self.swt = e(H3, I3), e(H3 // 128, I3 // 128, dt=f32)
+        self.qdy, self.sdy, self.qdyt, self.sdyt = (e(M3, I3), e(M3, I3 // 128, dt=f32), e(I3, M3),
+                                                    e(I3, M3 // 128, dt=f32))
+        bf = torch.bfloat16
+        self.y, self.dx, self.dw = e(M3, I3, dt=bf), e(M3, H3, dt=bf), e(I3, H3, dt=bf)
+        self.ws = fp.workspace(dev)
+
+    launches_per_step = 6
+
+    def quantize(self):
+        fp = self.fp
+        fp.fp8_quantize_transposed(self.x, "1x128", True, q_t=self.qxt, scales_t=self.sxt, q=self.qx,
+                                   scales=self.sx, ws=self.ws)
+        fp.fp8_quantize_transposed(self.w, "128x128", True, q_t=self.qwt, scales_t=self.swt, q=self.qw,
+                                   scales=self.sw, ws=self.ws)
+        fp.fp8_quantize_transposed(self.dy, "1x128", True, q_t=self.qdyt, scales_t=self.sdyt, q=self.qdy,
+                                   scales=self.sdy, ws=self.ws)
+
+    def gemms(self, events=None):
+        fp = self.fp
+        ops = ((self.qx, self.sx, "1x128", self.qw, self.sw, "128x128", self.y),
+               (self.qdy, self.sdy, "1x128", self.qwt, self.swt, "128x128", self.dx),
+               (self.qdyt, self.sdyt, "1x128", self.qxt, self.sxt, "1x128", self.dw))
+        for i, (a, sa, ga, b, sb, gb, out) in enumerate(ops):
+            if events is not None:
+                events[i][0].record()
+            fp.fp8_block_gemm(a, sa, ga, b, sb, gb, out=out, ws=self.ws)
+            if events is not None:
+                events[i][1].record()
+
+    def run(self, events=None):
+        self.quantize()
+        self.gemms(events)
+
+
+def flush_l2(torch, buf):
+    buf.zero_()
+
+
+def time_fn(torch, fn, reps, flush=None, warm=3):
+    """Mean CUDA-event time (ms) of fn() on the current stream, L2 flushed before each call."""
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    return statistics.mean(ts), ts
+
+
+# ---------------------------------------------------------------- sub-benchmarks
+def quantize_sweep(torch, fp, dev, pk, flush):
+    """Quantise sweep: BF16 [8192, 4096] at every granularity, row-wise and
+    dual (row + transposed), GB/s of algorithmic bytes against HBM peak."""
+    act, _ = device_inputs(torch, 100, dev)
+    r, c = 8192, 4096
+    x = act((r, c), 0.001, 100.0)
+    e = r * c
+    out = {}
+    cases = {
+        "1x128": 2 * e + e + 4 * e // 128,
+        "128x128": 2 * e + e + 4 * (e // (128 * 128)),
+        "mxfp8": 2 * e + e + e // 32,
+        "per_tensor": 2 * 2 * e + e + 4,
+        "nvfp4": 2 * 2 * e + e // 2 + e // 16 + 4,
+    }
+    ws = fp.workspace(dev)
+    bufs = {g: fp.fp8_quantize(x, g, ws=ws) for g in cases}
+    for g, nbytes in cases.items():
+        q, s, ts = bufs[g]
+        ms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, g, q=q, scales=s, tensor_scale=ts, ws=ws), 20, flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[g] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3)}
+    for g in ("1x128", "128x128", "mxfp8"):
+        qt, st, q, s = fp.fp8_quantize_transposed(x, g, True, ws=ws)
+        sbytes = {"1x128": 4 * e // 128, "128x128": 4 * (e // 16384), "mxfp8": e // 32}[g]
+        nbytes = 2 * e + 2 * e + 2 * sbytes
+        ms, _ = time_fn(torch, lambda: fp.fp8_quantize_transposed(x, g, True, q_t=qt, scales_t=st, q=q, scales=s,
+                                                                  ws=ws), 20, flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[g + "_dual"] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3)}
+    return out
+
+
+def moe_bench(torch, fp, dev, pk, flush):
+    """MoE grouped MXFP8 GEMMs, Qwen3-30B-A3B shapes (gate+up and down)."""
+    import synth
+    tokens, experts, hidden, inter = 16384, 128, 2048, 768
+    _, offsets = synth.moe_routing(tokens, experts, 8, seed=0)
+    rows = int(offsets[-1])
+    act, wt = device_inputs(torch, 200, dev)
+    a = act((rows, hidden), 0.001, 100.0)
+    h = act((rows, inter), 0.001, 100.0)
+    wgu = wt((experts * 2 * inter, hidden))
+    wdn = wt((experts * hidden, inter))
+    ws = fp.workspace(dev)
+    qa, sa, _ = fp.fp8_quantize(a, "mxfp8", ws=ws)
+    qh, shh, _ = fp.fp8_quantize(h, "mxfp8", ws=ws)
+    qgu, sgu, _ = fp.fp8_quantize(wgu, "mxfp8", ws=ws)
+    qdn, sdn, _ = fp.fp8_quantize(wdn, "mxfp8", ws=ws)
+    off = torch.from_numpy(offsets).to(dev)
+    d_gu = torch.empty((rows, 2 * inter), dtype=torch.bfloat16, device=dev)
+    d_dn = torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev)
+    f_gu = 2 * rows * 2 * inter * hidden
+    f_dn = 2 * rows * hidden * inter
+    run_gu = lambda: fp.fp8_grouped_gemm(qa, sa, qgu.view(experts, 2 * inter, hidden),  # noqa: E731
+                                         sgu.view(experts, 2 * inter, hidden // 32), off, "mxfp8", out=d_gu, ws=ws)
+    run_dn = lambda: fp.fp8_grouped_gemm(qh, shh, qdn.view(experts, hidden, inter),  # noqa: E731
+                                         sdn.view(experts, hidden, inter // 32), off, "mxfp8", out=d_dn, ws=ws)
+    ms_gu, _ = time_fn(torch, run_gu, 10, flush)
+    ms_dn, _ = time_fn(torch, run_dn, 10, flush)
+    peak = pk["bf16_tflops"] * FP8_PER_BF16
+    t_gu, t_dn = f_gu / ms_gu / 1e9, f_dn / ms_dn / 1e9
+    return {"gate_up": {"tflops": round(t_gu, 1), "ms": round(ms_gu, 3), "frac": round(t_gu / peak, 3)},
+            "down": {"tflops": round(t_dn, 1), "ms": round(ms_dn, 3), "frac": round(t_dn / peak, 3)},
+            "peak_tflops": round(peak, 1), "peak_note": "measured bf16 burst x nominal fp8/bf16 ratio 2"}
+
+
+def nvfp4_bench(torch, fp, dev, pk, flush):
+    """NVFP4 linear, Qwen2.5-32B MLP shape X [16384,5120] x W [27648,5120]^T."""
+    m, n, k = 16384, 27648, 5120
+    act, wt = device_inputs(torch, 300, dev)
+    x = act((m, k), 0.0, 1.0)
+    w = wt((n, k))
+    ws = fp.workspace(dev)
+    qx, sx, tx = fp.fp8_quantize(x, "nvfp4", ws=ws)
+    qw, sw, tw = fp.fp8_quantize(w, "nvfp4", ws=ws)
+    d = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    run = lambda: fp.fp8_block_gemm(qx, sx, "nvfp4", qw, sw, "nvfp4", tx, tw, k=k, out=d, ws=ws)  # noqa: E731
+    ms, _ = time_fn(torch, run, 10, flush)
+    flop = 2 * m * n * k
+    t = flop / ms / 1e9
+    peak = pk["bf16_tflops"] * FP4_PER_BF16
+    qms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, "nvfp4", q=qx, scales=sx, tensor_scale=tx, ws=ws), 10, flush)
+    e = m * k
+    qgbs = (2 * 2 * e + e // 2 + e // 16) / (qms * 1e-3) / 1e9
+    return {"gemm": {"tflops": round(t, 1), "ms": round(ms, 3), "frac": round(t / peak, 3)},
+            "peak_tflops": round(peak, 1), "peak_note": "measured bf16 burst x nominal fp4/bf16 ratio 6",
+            "quantize_x": {"gbs": round(qgbs, 1), "us": round(qms * 1e3, 1), "frac": round(qgbs / pk["hbm_gbs"], 3)}}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(rows: int = 128):
+    """The oracle on a bounded slice of the step: quantise `rows` token rows of
+    X and dY and the whole weight W, run the three GEMMs for those rows
+    (fprop: rows x I, dgrad: rows x H, wgrad: I x H over `rows` tokens)."""
+    import numpy as np
+    import synth
+    from oracle import formats as OF
+    from oracle import gemm as OG
+    from oracle import quantize as OQ
+    x = OF.bf16_bits_to_f32(synth.activations((rows, H3), seed=0))
+    dy = OF.bf16_bits_to_f32(synth.activations((rows, I3), seed=2))
+    w = OF.bf16_bits_to_f32(synth.weights((I3, H3), seed=1))
+    t0 = time.perf_counter()
+    qx, sx = OQ.quantize_1x128(x)
+    qw, sw = OQ.quantize_128x128(w)
+    qdy, sdy = OQ.quantize_1x128(dy)
+    qwt, swt = OQ.transposed(OQ.quantize_128x128, w)
+    qdyt, sdyt = OQ.transposed(OQ.quantize_1x128, dy)
+    qxt, sxt = OQ.transposed(OQ.quantize_1x128, x)
+    OG.block_gemm(qx, sx, "1x128", qw, sw, "128x128")
+    OG.block_gemm(qdy, sdy, "1x128", qwt, swt, "128x128")
+    OG.block_gemm(qdyt, sdyt, "1x128", qxt, sxt, "1x128")
+    dt = time.perf_counter() - t0
+    flop = 3 * 2 * rows * H3 * I3
+    threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or (os.cpu_count() or 1)
+    return {"value": flop / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{rows} of {M3} token rows of the step (all three GEMMs, weight quantised in full); "
+                      f"FLOPs counted for the sample only"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    res = [cpu_oracle_sample() for _ in range(max(1, args.steps))]
+    v = statistics.mean(r["value"] for r in res)
+    cb = dict(res[0])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": "block-scaled FP8 GEMM TFLOPS (linear-layer fwd+bwd step)",
+            "value": v, "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args),
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args):
+    return {"workload": "dense blockwise FP8 linear fwd+bwd, Qwen3-4B MLP shape (tokens 8192, hidden 2560, "
+                        "intermediate 9728); X,dY 1x128 FP32 scales (dual row+transposed), W 128x128 FP32 scales",
+            "tokens": M3, "hidden": H3, "intermediate": I3, "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs 250 MB and step working set ~630 MB, both > 129 MB L2; sub-benchmarks flush L2 "
+                  "(512 MB write) before each timed call"}
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    from fp8_block_scaled_03_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    import fp8_block_scaled_03_gb300 as fp
+    fp.load_library()
+    pk = peaks()
+    step = DenseStep(torch, fp, dev, seed=1000 + rank)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_l2(torch, flush_buf)  # noqa: E731
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    gev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
+           for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record()
+            step.run(gev[i])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if world > 1:
+            dist.barrier()
+    ms_steps = [a.elapsed_time(b) for a, b in ev]
+    ms_total = ms_steps and ev[0][0].elapsed_time(ev[-1][1])
+    gemm_ms = [[g[j][0].elapsed_time(g[j][1]) for j in range(3)] for g in gev]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+    value = world * STEP_FLOP / (ms_per_step * 1e-3) / 1e12
+    assert fp.read_status() == 0, "a device wait timed out during the bench"
+
+    # ---- roofline of the dominant kernel (the blockwise GEMM), measured in the timed region
+    avg_gemm_ms = statistics.mean(x for row in gemm_ms for x in row)
+    achieved = GEMM_FLOP / (avg_gemm_ms * 1e-3) / 1e12
+    peak_fp8 = pk["bf16_tflops_sustained"] * FP8_PER_BF16
+    roofline = {"bound": "tensor", "kernel": "gemm_blockwise_kernel<1x128,128x128|1x128>",
+                "achieved": round(achieved, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak_fp8, 3), "traffic": None,
+                "peak_note": f"{pk['source']} bf16 sustained x nominal fp8/bf16 ratio 2 (of {pk['source']})",
+                "per_gemm_ms": [round(statistics.mean(r[j] for r in gemm_ms), 3) for j in range(3)]}
+
+    line = {"metric": "block-scaled FP8 GEMM TFLOPS (linear-layer fwd+bwd step) and quantize GB/s, % of roofline",
+            "value": round(value, 1), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "wall_s": round(wall, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accum, bf16 out)",
+            "data": "synthetic", "config": workload_config(args), "roofline": roofline,
+            "gpu_launches": step.launches_per_step * args.steps, "clocks": clk.summary()}
+
+    if rank == 0 and not args.no_extras:
+        line["quantize"] = quantize_sweep(torch, fp, dev, pk, flush)
+        line["moe_mxfp8"] = moe_bench(torch, fp, dev, pk, flush)
+        line["nvfp4"] = nvfp4_bench(torch, fp, dev, pk, flush)
+        line["e2e"] = e2e_bench(torch, fp, dev, step)
+        line["cpu_baseline"] = cpu_oracle_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_bench(torch, fp, dev, step, reps=5):
+    """Same step through the public API from pinned HOST buffers: H2D of X, W,
+    dY, the step, D2H of Y, dX, dW, all inside the timed region."""
+    hx = step.x.cpu().pin_memory()
+    hw = step.w.cpu().pin_memory()
+    hdy = step.dy.cpu().pin_memory()
+    hy = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
+    hdx = torch.empty(step.dx.shape, dtype=step.dx.dtype).pin_memory()
+    hdw = torch.empty(step.dw.shape, dtype=step.dw.dtype).pin_memory()
+
+    def once():
+        step.x.copy_(hx, non_blocking=True)
+        step.w.copy_(hw, non_blocking=True)
+        step.dy.copy_(hdy, non_blocking=True)
+        step.run()
+        hy.copy_(step.y, non_blocking=True)
+        hdx.copy_(step.dx, non_blocking=True)
+        hdw.copy_(step.dw, non_blocking=True)
+
+    once()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        once()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / reps
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hdy))
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hdw))
+    return {"value": round(STEP_FLOP / dt / 1e12, 1), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3)}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+"""Python binding of libfp8bs.so (the block-scaled low-precision linear layer).
+
+Argument marshalling only: every computation runs in the CUDA kernels
+behind the C ABI declared in include/fp8bs.h.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the shared
+library is missing or fails to load, every call raises.
+
+Entry points (same names as the C ABI):
+    fp8_quantize(x, gran)                 -> (q, scales, tensor_scale)
+    fp8_quantize_transposed(x, gran, also_rowwise=False)
+                                          -> (q_t, scales_t, q, scales)
+    fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16)
+    fp8_grouped_gemm(a, sa, b, sb, offsets, gran)                      -> d (bf16)
+
+Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfp8bs.so")
+
+GRAN = {"per_tensor": 0, "1x128": 1, "128x128": 2, "mxfp8": 3, "nvfp4": 4}
+FLAG_GIVEN_TENSOR_SCALE = 1
+STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNSUPPORTED",
+          -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE"}
+EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
+           "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
+           "fp8bs_status_string", "fp8bs_version")
+
+_lib = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({status_string(code)})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfp8bs.so and declare its signatures (no GPU needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfp8bs.so not found at {path}; build it with "
+                           "`python -m fp8_block_scaled_03_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    P, I64, I, U, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+    lib.fp8_quantize.argtypes = [P, I64, I64, I64, I, P, P, P, U, P, SZ, P]
+    lib.fp8_quantize_transposed.argtypes = [P, I64, I64, I64, I, P, P, P, P, P, U, P, SZ, P]
+    lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
+    lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
+    lib.fp8bs_workspace_size.restype = SZ
+    lib.fp8bs_workspace_size.argtypes = []
+    lib.fp8bs_read_status.argtypes = [P, P]
+    lib.fp8bs_clear_status.argtypes = [P, P]
+    lib.fp8bs_status_string.restype = ctypes.c_char_p
+    lib.fp8bs_status_string.argtypes = [I]
+    lib.fp8bs_version.argtypes = []
+    for name in ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
+                 "fp8bs_read_status", "fp8bs_clear_status", "fp8bs_version"):
+        getattr(lib, name).restype = I
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().fp8bs_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise Fp8bsError(fn, code)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_workspaces = {}
+
+
+def workspace(device=None) -> torch.Tensor:
+    """A zero-initialised workspace per device (status word + amax scratch)."""
+    dev = torch.device(device if device is not None else torch.cuda.current_device())
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    ws = _workspaces.get(dev)
+    if ws is None:
+        ws = torch.zeros(load_library().fp8bs_workspace_size(), dtype=torch.uint8, device=dev)
+        _workspaces[dev] = ws
+    return ws
+
+
+def read_status(ws: Optional[torch.Tensor] = None, stream=None) -> int:
+    ws = ws if ws is not None else workspace()
+    return load_library().fp8bs_read_status(_ptr(ws), _stream(stream))
+
+
+def clear_status(ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    ws = ws if ws is not None else workspace()
+    _check("fp8bs_clear_status", load_library().fp8bs_clear_status(_ptr(ws), _stream(stream)))
+
+
+def _gran(g) -> int:
+    return GRAN[g] if isinstance(g, str) else int(g)
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def scale_shape(gran, rows: int, cols: int):
+    """Shape and dtype of the scale tensor fp8_quantize writes for [rows, cols]."""
+    g = _gran(gran)
+    if g == 0:
+        return (1,), torch.float32
+    if g == 1:
+        return (rows, _cdiv(cols, 128)), torch.float32
+    if g == 2:
+        return (_cdiv(rows, 128), _cdiv(cols, 128)), torch.float32
+    if g == 3:
+        return (rows, _cdiv(cols, 32)), torch.uint8
+    return (rows, cols // 16), torch.uint8
+
+
+def _as_bf16_2d(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype == torch.uint16:
+        x = x.view(torch.bfloat16)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor")
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit column stride")
+    return x
+
+
+def fp8_quantize(x: torch.Tensor, gran, *, q=None, scales=None, tensor_scale=None, flags: int = 0,
+                 ws=None, stream=None):
+    """Row-wise quantisation of a BF16 matrix; returns (q, scales, tensor_scale)."""
+    x = _as_bf16_2d(x)
+    g = _gran(gran)
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty((rows, cols // 2 if g == 4 else cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        shp, dt = scale_shape(g, rows, cols)
+        scales = torch.empty(shp, dtype=dt, device=dev)
+    if g == 4 and tensor_scale is None:
+        tensor_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    rc = load_library().fp8_quantize(_ptr(x), rows, cols, x.stride(0), g, _ptr(q), _ptr(scales),
+                                     _ptr(tensor_scale), flags, _ptr(ws), ws.numel(), _stream(stream))
+    _check("fp8_quantize", rc)
+    return q, scales, tensor_scale
+
+
+def fp8_quantize_transposed(x: torch.Tensor, gran, also_rowwise: bool = False, *, q_t=None, scales_t=None,
+                            q=None, scales=None, flags: int = 0, ws=None, stream=None):
+    """Quantise X^T (and optionally X in the same pass); returns (q_t, scales_t, q, scales)."""
+    x = _as_bf16_2d(x)
+    g = _gran(gran)
+    rows, cols = x.shape
+    dev = x.device
+    if q_t is None:
+        q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    if scales_t is None:
+        shp, dt = scale_shape(g, cols, rows)
+        scales_t = torch.empty(shp, dtype=dt, device=dev)
+    if also_rowwise:
+        if q is None:
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        if scales is None:
+            shp, dt = scale_shape(g, rows, cols)
+            scales = torch.empty(shp, dtype=dt, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    rc = load_library().fp8_quantize_transposed(_ptr(x), rows, cols, x.stride(0), g, _ptr(q_t), _ptr(scales_t),
+                                                _ptr(q), _ptr(scales), None, flags, _ptr(ws), ws.numel(),
+                                                _stream(stream))
+    _check("fp8_quantize_transposed", rc)
+    return q_t, scales_t, q, scales
+
+
+def fp8_block_gemm(a, a_scales, a_gran, b, b_scales, b_gran, a_tensor_scale=None, b_tensor_scale=None, *,
+                   k: Optional[int] = None, out=None, ws=None, stream=None):
+    """D = deq(A) . deq(B)^T in BF16.  A [m, k] and B [n, k] codes (NVFP4: packed [., k/2])."""
+    ga, gb = _gran(a_gran), _gran(b_gran)
+    m, n = a.shape[0], b.shape[0]
+    if k is None:
+        k = a.shape[1] * (2 if ga == 4 else 1)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    ws = ws if ws is not None else workspace(a.device)
+    rc = load_library().fp8_block_gemm(_ptr(a), _ptr(a_scales), ga, _ptr(b), _ptr(b_scales), gb,
+                                       _ptr(a_tensor_scale), _ptr(b_tensor_scale), m, n, k, _ptr(out),
+                                       _ptr(ws), ws.numel(), _stream(stream))
+    _check("fp8_block_gemm", rc)
+    return out
+
+
+def fp8_grouped_gemm(a, a_scales, b, b_scales, offsets, gran, *, out=None, ws=None, stream=None):
+    """MoE grouped GEMM: rows offsets[e]..offsets[e+1] of A times B[e]^T; D BF16 [rows, n]."""
+    g = _gran(gran)
+    experts, n, k = b.shape
+    rows = a.shape[0]
+    if offsets.dtype != torch.int64 or not offsets.is_cuda or offsets.numel() != experts + 1:
+        raise ValueError("offsets must be a CUDA int64 tensor of experts+1 entries")
+    if out is None:
+        out = torch.empty((rows, n), dtype=torch.bfloat16, device=a.device)
+    ws = ws if ws is not None else workspace(a.device)
+    rc = load_library().fp8_grouped_gemm(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(offsets),
+                                         experts, rows, n, k, g, _ptr(out), _ptr(ws), ws.numel(),
+                                         _stream(stream))
+    _check("fp8_grouped_gemm", rc)
+    return out

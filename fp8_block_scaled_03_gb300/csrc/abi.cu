@@ -1,0 +1,220 @@
+// abi.cu -- the extern "C" entry points declared in include/fp8bs.h.
+//
+// Host-side argument checks, then a launch on the caller's stream.  Nothing
+// here allocates device memory or synchronises (except fp8bs_read_status,
+// whose job is to read the status word back).
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fp8bs.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+int sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Scale pointers: FP32 scales and UE8M0 words are read 4 bytes at a time,
+// NVFP4 block scales 16 bytes at a time.
+inline bool scales_aligned(const void* s, int gran) { return gran == 4 ? aligned16(s) : aligned4(s); }
+
+// Launchers return 0, a cudaError_t (> 0) or a negative fp8bs_status.
+inline int cuda_status(int err) {
+    if (err < 0) return err;
+    if (err != 0) {
+        (void)cudaGetLastError();
+        return FP8BS_ECUDA;
+    }
+    return FP8BS_OK;
+}
+
+// Size and granularity checks shared by both quantisers.  Returns 1 (not an
+// error) for an empty matrix, which the callers turn into a no-op before any
+// pointer is looked at (allocators may hand out NULL for empty tensors).
+int check_quant_common(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran) {
+    if (rows < 0 || cols < 0) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    if (cols % 8 != 0 || ld_x < cols || ld_x % 8 != 0) return FP8BS_EINVAL;
+    if (gran == FP8BS_NVFP4_1x16 && cols % 16 != 0) return FP8BS_EINVAL;
+    if (ceil_div(rows, 128) > 65535 || ceil_div(cols, 128) > 0x7FFFFFFF) return FP8BS_EINVAL;
+    if (rows == 0 || cols == 0) return 1;
+    if (x == nullptr) return FP8BS_EINVAL;
+    if (!aligned16(x)) return FP8BS_EALIGN;
+    return FP8BS_OK;
+}
+
+bool needs_partials(int gran, unsigned flags) {
+    return (gran == FP8BS_PER_TENSOR || gran == FP8BS_NVFP4_1x16) && !(flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
+                 void* q, void* scales, float* tensor_scale, unsigned flags,
+                 void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    int rc = check_quant_common(x, rows, cols, ld_x, gran);
+    if (rc) return rc > 0 ? FP8BS_OK : rc;
+    if (q == nullptr || scales == nullptr) return FP8BS_EINVAL;
+    if (gran == FP8BS_NVFP4_1x16 && tensor_scale == nullptr) return FP8BS_EINVAL;
+    if (!aligned16(q)) return FP8BS_EALIGN;
+    if (needs_partials(gran, flags) && (workspace == nullptr || workspace_bytes < kWorkspaceBytes))
+        return FP8BS_EWORKSPACE;
+    QuantJob j{};
+    j.x = static_cast<const uint16_t*>(x);
+    j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
+    j.q = static_cast<uint8_t*>(q); j.s = scales;
+    j.tensor_scale = tensor_scale;
+    j.given_scale = (flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE) != 0;
+    j.partials = workspace ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kPartialsOffset) : nullptr;
+    return cuda_status(launch_quantize(j, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
+                            void* q_t, void* scales_t, void* q, void* scales,
+                            float* tensor_scale, unsigned flags,
+                            void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    (void)tensor_scale;
+    if (gran == FP8BS_NVFP4_1x16) return FP8BS_EUNSUPPORTED;
+    if (rows % 16 != 0) return FP8BS_EINVAL;
+    int rc = check_quant_common(x, rows, cols, ld_x, gran);
+    if (rc) return rc > 0 ? FP8BS_OK : rc;
+    if (q_t == nullptr || scales_t == nullptr) return FP8BS_EINVAL;
+    if ((q == nullptr) != (scales == nullptr)) return FP8BS_EINVAL;
+    if (!aligned16(q_t) || (q != nullptr && !aligned16(q))) return FP8BS_EALIGN;
+    if (needs_partials(gran, flags) && (workspace == nullptr || workspace_bytes < kWorkspaceBytes))
+        return FP8BS_EWORKSPACE;
+    QuantJob j{};
+    j.x = static_cast<const uint16_t*>(x);
+    j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
+    j.qt = static_cast<uint8_t*>(q_t); j.st = scales_t;
+    j.q = static_cast<uint8_t*>(q); j.s = scales;
+    j.given_scale = (flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE) != 0;
+    j.partials = workspace ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kPartialsOffset) : nullptr;
+    return cuda_status(launch_quantize_transposed(j, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
+                   const void* b, const void* b_scales, int b_gran,
+                   const float* a_tensor_scale, const float* b_tensor_scale,
+                   int64_t m, int64_t n, int64_t k, void* d,
+                   void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
+        return FP8BS_EINVAL;
+    if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0) return FP8BS_EINVAL;
+    if (a_gran < 0 || a_gran > FP8BS_NVFP4_1x16 || b_gran < 0 || b_gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
+    if (!scales_aligned(a_scales, a_gran) || !scales_aligned(b_scales, b_gran)) return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    const bool fp32_a = a_gran <= FP8BS_BLOCK_128x128, fp32_b = b_gran <= FP8BS_BLOCK_128x128;
+    GemmJob j{};
+    j.a = a; j.sa = a_scales; j.a_gran = a_gran;
+    j.b = b; j.sb = b_scales; j.b_gran = b_gran;
+    j.a_ts = a_tensor_scale; j.b_ts = b_tensor_scale;
+    j.m = m; j.n = n; j.k = k; j.d = d;
+    j.status = static_cast<int*>(workspace);
+    j.offsets = nullptr; j.experts = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (fp32_a && fp32_b) {
+        if (k % 128 != 0) return FP8BS_EINVAL;
+        return cuda_status(launch_gemm_blockwise(j, st));
+    }
+    if (a_gran == FP8BS_MXFP8_1x32 && b_gran == FP8BS_MXFP8_1x32) {
+        if (k % 128 != 0) return FP8BS_EINVAL;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
+    if (a_gran == FP8BS_NVFP4_1x16 && b_gran == FP8BS_NVFP4_1x16) {
+        if (k % 256 != 0) return FP8BS_EINVAL;
+        if (a_tensor_scale == nullptr || b_tensor_scale == nullptr) return FP8BS_EINVAL;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
+    return FP8BS_EUNSUPPORTED;
+}
+
+int fp8_grouped_gemm(const void* a, const void* a_scales,
+                     const void* b, const void* b_scales,
+                     const int64_t* offsets, int experts, int64_t total_rows,
+                     int64_t n, int64_t k, int gran, void* d,
+                     void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr ||
+        offsets == nullptr)
+        return FP8BS_EINVAL;
+    if (experts <= 0 || experts > 1024 || total_rows < 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 128 != 0)
+        return FP8BS_EINVAL;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
+    if (!aligned4(a_scales) || !aligned4(b_scales) || (reinterpret_cast<uintptr_t>(offsets) & 7u)) return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (total_rows == 0) return FP8BS_OK;
+    GemmJob j{};
+    j.a = a; j.sa = a_scales; j.b = b; j.sb = b_scales;
+    j.m = total_rows; j.n = n; j.k = k; j.d = d;
+    j.status = static_cast<int*>(workspace);
+    j.offsets = offsets; j.experts = experts;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (gran == FP8BS_MXFP8_1x32) {
+        j.a_gran = j.b_gran = FP8BS_MXFP8_1x32;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
+    if (gran == FP8BS_TOKEN_1x128) {
+        j.a_gran = FP8BS_TOKEN_1x128; j.b_gran = FP8BS_BLOCK_128x128;
+        return cuda_status(launch_gemm_blockwise(j, st));
+    }
+    if (gran < 0 || gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    return FP8BS_EUNSUPPORTED;
+}
+
+size_t fp8bs_workspace_size(void) { return kWorkspaceBytes; }
+
+int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream) {
+    if (workspace == nullptr) return FP8BS_EINVAL;
+    int v = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status(1);
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status(1);
+    return v;
+}
+
+int fp8bs_clear_status(void* workspace, fp8bs_stream_t stream) {
+    if (workspace == nullptr) return FP8BS_EINVAL;
+    return cuda_status((int)cudaMemsetAsync(workspace, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* fp8bs_status_string(int status) {
+    switch (status) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_EINVAL: return "invalid argument (size, granularity or null pointer)";
+    case FP8BS_EALIGN: return "pointer or pitch not 16-byte aligned";
+    case FP8BS_EUNSUPPORTED: return "combination not implemented";
+    case FP8BS_ECUDA: return "CUDA runtime error or launch failure";
+    case FP8BS_ETIMEOUT: return "a bounded device wait timed out";
+    case FP8BS_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int fp8bs_version(void) { return 100; }
+
+}  // extern "C"

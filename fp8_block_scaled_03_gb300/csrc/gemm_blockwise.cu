@@ -1,0 +1,336 @@
+// gemm_blockwise.cu -- FP8 E4M3 GEMM with FP32 block scales (tcgen05 + TMA + TMEM).
+//
+//   D[m, n] = sum_kb  sa(m, kb) * sb(n, kb) * sum_{k in kb} qa[m, k] * qb[n, k]
+//
+// the block-wise ("DeepSeek-style") recipe of the "Low Precision RL" page
+// (table "Choose a precision": 128x128 blocks, FP32 scales; section
+// "2. Unified block-wise FP8") with per-token 1x128 activation scales (the
+// review's "FP8 Quantization": per-token for activations and gradients).
+// FP32 scales cannot ride on the tensor core's power-of-two block-scale
+// path, so each 128-wide K block is accumulated on its own in TMEM and the
+// epilogue warps fold it into FP32 registers with the scale product
+// ("promotion").  Two TMEM partial buffers alternate, so the MMAs of block
+// kb+1 run while block kb is being promoted.
+//
+// CTA: 384 threads (3 warpgroups), one CTA per SM (persistent), tile
+// 128 x 256, K block 128.  Launched at 168 registers per thread; the
+// producer warpgroup gives registers back (72) and the two epilogue
+// warpgroups take them (216): 128*72 + 256*216 = 384*168.
+//   warp 0      TMA producer (one lane): A 128x128 and B 256x128 boxes,
+//               128-byte swizzle, 4-stage ring.
+//   warp 1      TMEM owner + MMA issuer (one lane): 4 x tcgen05.mma
+//               kind::f8f6f4 (M128 N256 K32) per K block into partial
+//               buffer kb & 1, then tcgen05.commit to free the stage and to
+//               publish the partial.
+//   warps 2-3   idle (complete the producer warpgroup)
+//   warps 4..11 epilogue: warp w reads TMEM lanes 32*(w%4).. (one D row per
+//               thread) and columns 128*((w-4)/4).. (one 128-column half);
+//               acc += partial * sa * sb, BF16 store at the end of the tile.
+// Scale modes (template): 0 per-tensor, 1 per row (1x128), 2 per 128-row block.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+#include "tmap.h"
+
+namespace fp8bs {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(BM, BN);
+
+struct Params {
+    int64_t m, n, k;
+    const float* sa;
+    const float* sb;
+    __nv_bfloat16* d;
+    int* status;
+    const int64_t* offsets;
+    int experts;
+};
+
+struct alignas(16) Shared {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort;
+    float sbuf[8][2][128];
+    SchedShared sched;
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+
+template <int MODE>
+__device__ __forceinline__ float a_scale(const float* __restrict__ sa, int64_t row, int64_t row_end, int64_t nkb,
+                                         int64_t kb) {
+    if (MODE == 0) return __ldg(sa);
+    if (row >= row_end) return 0.0f;
+    if (MODE == 1) return __ldg(sa + row * nkb + kb);
+    return __ldg(sa + (row >> 7) * nkb + kb);
+}
+
+template <int SA_MODE, int SB_MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared* sh = reinterpret_cast<Shared*>(stages + (size_t)STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nkb = p.k / BK;
+    const int64_t n_tiles = (p.n + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&sh->full[s]), 1);
+            mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sh->tfull[b]), 1);
+            mbar_init(smem_u32(&sh->tempty[b]), 8);
+        }
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sh->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles);  // has __syncthreads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    volatile int* abort = &sh->abort;
+
+    if (warp < 4) {
+    setmaxnreg_dec<72>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+                const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&sh->full[s]);
+                    uint8_t* sa_ptr = stages + (size_t)s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d(smem_u32(sa_ptr), &tm_a, fb, (int32_t)(kb * BK), (int32_t)ti.row0);
+                    tma_load_2d(smem_u32(sa_ptr + A_BYTES), &tm_b, fb, (int32_t)(kb * BK), brow);
+                }
+            }
+            if (!ok) {  // let copies already issued land before the CTA exits
+                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                    mbar_wait(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, abort, p.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, kbg = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
+                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->tempty[b]), tph ^ 1, abort, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(stages + (size_t)s * STAGE_BYTES);
+                    const uint64_t adesc = kmajor_sw128_desc(a_addr);
+                    const uint64_t bdesc = kmajor_sw128_desc(a_addr + A_BYTES);
+                    const uint32_t d_tmem = tmem + b * BN;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk)
+                        mma_f8f6f4(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&sh->empty[s]));
+                    mma_commit(smem_u32(&sh->tfull[b]));
+                }
+            }
+            mma_commit(smem_u32(&sh->drain));
+            mbar_wait(smem_u32(&sh->drain), 0, abort, p.status);
+        }
+        __syncwarp();
+    }
+    } else {
+        setmaxnreg_inc<216>();
+        // ------------------------------------------------------------ epilogue (8 warps)
+        const int ew = warp - 4;
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int h = ew >> 2;           // 128-column half of the tile
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        float* sbuf0 = sh->sbuf[ew][0];
+        float* sbuf1 = sh->sbuf[ew][1];
+        uint32_t kbg = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const int64_t row = ti.row0 + 32 * q + lane;
+            const int64_t col0 = ti.n0 + 128 * h;
+            const float* sb_e = p.sb;
+            if (p.experts) {
+                const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
+                sb_e = p.sb + (int64_t)ti.expert * per;
+            }
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+            // scale prefetch for kb = 0
+            float fa_next = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, 0);
+            float fb_next = 0.0f;
+            float4 fbv_next = make_float4(0.f, 0.f, 0.f, 0.f);
+#define FP8BS_LOAD_B(KB)                                                                              \
+    do {                                                                                              \
+        if (SB_MODE == 0) {                                                                           \
+            fb_next = __ldg(sb_e);                                                                    \
+        } else if (SB_MODE == 2) {                                                                    \
+            fb_next = (col0 < p.n) ? __ldg(sb_e + (col0 >> 7) * nkb + (KB)) : 0.0f;                   \
+        } else {                                                                                      \
+            const int64_t c_ = col0 + 4 * lane;                                                       \
+            fbv_next.x = (c_ + 0 < p.n) ? __ldg(sb_e + (c_ + 0) * nkb + (KB)) : 0.0f;                 \
+            fbv_next.y = (c_ + 1 < p.n) ? __ldg(sb_e + (c_ + 1) * nkb + (KB)) : 0.0f;                 \
+            fbv_next.z = (c_ + 2 < p.n) ? __ldg(sb_e + (c_ + 2) * nkb + (KB)) : 0.0f;                 \
+            fbv_next.w = (c_ + 3 < p.n) ? __ldg(sb_e + (c_ + 3) * nkb + (KB)) : 0.0f;                 \
+        }                                                                                             \
+    } while (0)
+            FP8BS_LOAD_B(0);
+
+            for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
+                const float fa = fa_next;
+                const float fb = fb_next;
+                if (SB_MODE == 1) {
+                    float* buf = (kb & 1) ? sbuf1 : sbuf0;
+                    reinterpret_cast<float4*>(buf)[lane] = fbv_next;
+                }
+                if (kb + 1 < nkb) {
+                    fa_next = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, kb + 1);
+                    FP8BS_LOAD_B(kb + 1);
+                }
+                __syncwarp();
+                const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
+                const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
+                if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }   // tcgen05.ld is .sync.aligned
+                tc_fence_after();
+                const float f = fa * fb;
+                const float* buf = (kb & 1) ? sbuf1 : sbuf0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + b * BN + 128 * h + 32 * c, r);
+                    tmem_ld_wait();
+                    if (SB_MODE == 1) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 s4 = reinterpret_cast<const float4*>(buf)[(32 * c + j) >> 2];
+                            acc[32 * c + j + 0] = fmaf(__uint_as_float(r[j + 0]), fa * s4.x, acc[32 * c + j + 0]);
+                            acc[32 * c + j + 1] = fmaf(__uint_as_float(r[j + 1]), fa * s4.y, acc[32 * c + j + 1]);
+                            acc[32 * c + j + 2] = fmaf(__uint_as_float(r[j + 2]), fa * s4.z, acc[32 * c + j + 2]);
+                            acc[32 * c + j + 3] = fmaf(__uint_as_float(r[j + 3]), fa * s4.w, acc[32 * c + j + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), f, acc[32 * c + j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+            }
+#undef FP8BS_LOAD_B
+            if (!ok) break;
+            // BF16 store of this thread's row: 128 columns = 16 x 16 bytes
+            if (row < ti.row_end) {
+                __nv_bfloat16* drow = p.d + row * p.n + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 8) {
+                    if (col0 + j < p.n) {
+                        uint4 o;
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
+                        __nv_bfloat162 v1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+                        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+                        __nv_bfloat162 v3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                        o.x = *reinterpret_cast<uint32_t*>(&v0);
+                        o.y = *reinterpret_cast<uint32_t*>(&v1);
+                        o.z = *reinterpret_cast<uint32_t*>(&v2);
+                        o.w = *reinterpret_cast<uint32_t*>(&v3);
+                        *reinterpret_cast<uint4*>(drow + j) = o;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int SA, int SB>
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t st) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_blockwise_kernel<SA, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e != cudaSuccess) return (int)e;
+        attr_set[dev] = true;
+    }
+    gemm_blockwise_kernel<SA, SB><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    return (int)cudaGetLastError();
+}
+
+int mode_of(int gran) { return gran == 0 ? 0 : (gran == 1 ? 1 : 2); }
+
+}  // namespace
+
+int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
+    if (j.experts > kMaxExperts) return -3;
+    CUtensorMap ta, tb;
+    const uint64_t b_rows = (uint64_t)j.n * (uint64_t)(j.experts > 0 ? j.experts : 1);
+    if (!make_tmap_u8(&ta, j.a, (uint64_t)j.k, (uint64_t)j.m, (uint64_t)j.k, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_u8(&tb, j.b, (uint64_t)j.k, b_rows, (uint64_t)j.k, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return (int)cudaErrorInvalidValue;
+    Params p{};
+    p.m = j.m; p.n = j.n; p.k = j.k;
+    p.sa = static_cast<const float*>(j.sa);
+    p.sb = static_cast<const float*>(j.sb);
+    p.d = static_cast<__nv_bfloat16*>(j.d);
+    p.status = j.status;
+    p.offsets = j.offsets;
+    p.experts = j.experts;
+    const int sms = sm_count();
+    int grid = sms;
+    if (j.experts == 0) {
+        const int64_t tiles = ceil_div(j.m, BM) * ceil_div(j.n, BN);
+        grid = (int)std::min<int64_t>(tiles, sms);
+    }
+    const int sa = mode_of(j.a_gran), sb = mode_of(j.b_gran);
+#define FP8BS_BW_CASE(A, B) \
+    if (sa == A && sb == B) return launch_typed<A, B>(ta, tb, p, grid, st);
+    FP8BS_BW_CASE(1, 2) FP8BS_BW_CASE(1, 1) FP8BS_BW_CASE(1, 0)
+    FP8BS_BW_CASE(2, 2) FP8BS_BW_CASE(2, 1) FP8BS_BW_CASE(2, 0)
+    FP8BS_BW_CASE(0, 2) FP8BS_BW_CASE(0, 1) FP8BS_BW_CASE(0, 0)
+#undef FP8BS_BW_CASE
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,370 @@
+// gemm_mx.cu -- block-scaled GEMMs on the tensor core's own scale path:
+// MXFP8 (E4M3, UE8M0 scale per 32 K-elements) and NVFP4 (E2M1, E4M3 scale
+// per 16 K-elements, times the two FP32 tensor scales), dense and MoE
+// grouped.
+//
+// "Low Precision RL", table "Choose a precision": MXFP8 1x32 with UE8M0
+// scales and NVFP4 1x16 with two-level (E4M3 + FP32) scales, both Blackwell
+// formats; section "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend is
+// chosen separately from the dense one.  Here both are one kernel: a dense
+// GEMM is the grouped GEMM with one group.
+//
+// CTA: 384 threads, one CTA per SM (persistent), tile 128 x 256.
+//   warp 0      TMA producer: A 128 x 128 B and B 256 x 128 B boxes per stage
+//               (128 FP8 or 256 FP4 K-elements), 128-byte swizzle.
+//   warp 1      TMEM owner + MMA issuer: per stage, tcgen05.cp of the scale
+//               atoms to TMEM, then 4 block-scaled MMAs (M128 N256; K32 for
+//               MXFP8, K64 for NVFP4), accumulating the whole K range in TMEM.
+//   warp 2      scale loader: reads the row-major scale bytes of the stage's
+//               rows and writes them in the 32 x 16-byte atom layout that
+//               tcgen05.cp 32x128b.warpx4 replicates into all TMEM lane
+//               quarters (row r0 + 32*r1 at byte r0*16 + r1*4).
+//   warp 3      idle
+//   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
+//               128 columns per thread) to BF16 registers, release TMEM, store.
+// TMEM: columns 0..255 accumulator, 256.. scale factors per stage.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+#include "tmap.h"
+
+namespace fp8bs {
+namespace {
+
+constexpr int BM = 128, BN = 256, BKB = 128;  // BKB: K bytes per stage and row
+constexpr int A_BYTES = BM * BKB, B_BYTES = BN * BKB;
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+
+enum { kMx = 0, kNv = 1 };
+
+template <int KIND> struct Cfg;
+template <> struct Cfg<kMx> {
+    static constexpr int STAGES = 4;
+    static constexpr int K_PER_STAGE = 128;           // elements
+    static constexpr int A_ATOMS = 1, B_ATOMS = 2;    // 512-byte scale atoms per stage
+    static constexpr int SF_BYTES_PER_ROW = 4;        // scale bytes per row per stage
+};
+template <> struct Cfg<kNv> {
+    static constexpr int STAGES = 3;
+    static constexpr int K_PER_STAGE = 256;
+    static constexpr int A_ATOMS = 4, B_ATOMS = 8;
+    static constexpr int SF_BYTES_PER_ROW = 16;
+};
+
+struct Params {
+    int64_t m, n, k;
+    const uint8_t* sa;   // row-major scale bytes [m, k / vec]
+    const uint8_t* sb;   // [experts * n, k / vec]
+    const float* a_ts;   // NVFP4 tensor scales
+    const float* b_ts;
+    __nv_bfloat16* d;
+    int* status;
+    const int64_t* offsets;
+    int experts;
+};
+
+template <int STAGES>
+struct alignas(16) Shared {
+    uint64_t full[STAGES], empty[STAGES], tfull, tempty, drain;
+    uint32_t tmem_base;
+    int abort;
+    SchedShared sched;
+};
+
+// Stage = A tile | B tile | scale atoms, rounded up to 1024 bytes so that
+// every tile starts on a 128-byte-swizzle atom boundary.
+template <int KIND>
+constexpr size_t stage_bytes() {
+    return ((size_t)A_BYTES + B_BYTES + 512u * (Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS) + 1023) & ~size_t(1023);
+}
+template <int KIND>
+constexpr size_t smem_bytes() {
+    return 1024 + Cfg<KIND>::STAGES * stage_bytes<KIND>() + sizeof(Shared<Cfg<KIND>::STAGES>);
+}
+
+// Scale words of one stage for one lane: A rows r0 + 32*r1 (r1 < 4) and B rows
+// r0 + 32*r1 (r1 < 8); MXFP8 one 32-bit word per row, NVFP4 four.
+template <int KIND>
+struct ScaleRegs {
+    static constexpr int W = Cfg<KIND>::SF_BYTES_PER_ROW / 4;
+    uint32_t a[4][W];
+    uint32_t b[8][W];
+};
+
+template <int KIND>
+__device__ __forceinline__ void load_scales(ScaleRegs<KIND>& r, const Params& p, const TileInfo& ti, int64_t kb,
+                                            int lane, int64_t sf_pitch) {
+    constexpr int W = ScaleRegs<KIND>::W;
+    const int64_t koff = kb * Cfg<KIND>::SF_BYTES_PER_ROW;
+#pragma unroll
+    for (int r1 = 0; r1 < 4; ++r1) {
+        const int64_t row = ti.row0 + lane + 32 * r1;
+        const bool ok = row < p.m;
+        const uint8_t* src = p.sa + row * sf_pitch + koff;
+        if (W == 1) {
+            r.a[r1][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
+        } else {
+            const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+            r.a[r1][0] = v.x; r.a[r1][1 % W] = v.y; r.a[r1][2 % W] = v.z; r.a[r1][3 % W] = v.w;
+        }
+    }
+    const int64_t brow0 = (int64_t)ti.expert * p.n + ti.n0;
+#pragma unroll
+    for (int r1 = 0; r1 < 8; ++r1) {
+        const int64_t n = ti.n0 + lane + 32 * r1;
+        const bool ok = n < p.n;
+        const uint8_t* src = p.sb + (brow0 + lane + 32 * r1) * sf_pitch + koff;
+        if (W == 1) {
+            r.b[r1][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
+        } else {
+            const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+            r.b[r1][0] = v.x; r.b[r1][1 % W] = v.y; r.b[r1][2 % W] = v.z; r.b[r1][3 % W] = v.w;
+        }
+    }
+}
+
+// Write one stage's scales into the tcgen05.cp atom layout.  Atom j of A
+// holds the j-th scale word of every row (MXFP8: j = 0 only); B atoms are
+// ordered (j, 128-row chunk).
+template <int KIND>
+__device__ __forceinline__ void store_scales(const ScaleRegs<KIND>& r, uint8_t* sf, int lane) {
+    constexpr int W = ScaleRegs<KIND>::W;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        *reinterpret_cast<uint4*>(sf + j * 512 + lane * 16) = make_uint4(r.a[0][j], r.a[1][j], r.a[2][j], r.a[3][j]);
+    }
+    uint8_t* sfb = sf + Cfg<KIND>::A_ATOMS * 512;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            *reinterpret_cast<uint4*>(sfb + (j * 2 + c) * 512 + lane * 16) =
+                make_uint4(r.b[4 * c + 0][j], r.b[4 * c + 1][j], r.b[4 * c + 2][j], r.b[4 * c + 3][j]);
+        }
+    }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
+    constexpr int STAGES = Cfg<KIND>::STAGES;
+    constexpr size_t SB = stage_bytes<KIND>();
+    constexpr uint32_t SF_COLS = 4 * (Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS);  // TMEM columns per stage
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared<STAGES>* sh = reinterpret_cast<Shared<STAGES>*>(stages + STAGES * SB);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nkb = p.k / Cfg<KIND>::K_PER_STAGE;
+    const int64_t n_tiles = (p.n + BN - 1) / BN;
+    const int64_t sf_pitch = p.k / (KIND == kMx ? 32 : 16);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&sh->full[s]), 2);   // TMA bytes + scale loader
+            mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        mbar_init(smem_u32(&sh->tfull), 1);
+        mbar_init(smem_u32(&sh->tempty), 8);
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sh->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    volatile int* abort = &sh->abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+                const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&sh->full[s]);
+                    uint8_t* st = stages + s * SB;
+                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+                    tma_load_2d(smem_u32(st), &tm_a, fb, (int32_t)(kb * BKB), (int32_t)ti.row0);
+                    tma_load_2d(smem_u32(st + A_BYTES), &tm_b, fb, (int32_t)(kb * BKB), brow);
+                }
+            }
+            if (!ok) {
+                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                    mbar_wait(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, abort, p.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+                if (!mbar_wait(smem_u32(&sh->tempty), (tcount & 1) ^ 1, abort, p.status)) { ok = false; break; }
+                tc_fence_after();
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    uint8_t* st = stages + s * SB;
+                    const uint32_t a_addr = smem_u32(st);
+                    const uint64_t adesc = kmajor_sw128_desc(a_addr);
+                    const uint64_t bdesc = kmajor_sw128_desc(a_addr + A_BYTES);
+                    const uint32_t sf_addr = a_addr + A_BYTES + B_BYTES;
+                    const uint32_t sfa = tmem + 256 + s * SF_COLS;
+                    const uint32_t sfb = sfa + 4 * Cfg<KIND>::A_ATOMS;
+#pragma unroll
+                    for (int j = 0; j < Cfg<KIND>::A_ATOMS; ++j)
+                        tmem_cp_32x128b_x4(sfa + 4 * j, smem_desc(sf_addr + 512 * j, 0, 128, 0));
+#pragma unroll
+                    for (int j = 0; j < Cfg<KIND>::B_ATOMS; ++j)
+                        tmem_cp_32x128b_x4(sfb + 4 * j, smem_desc(sf_addr + 512 * (Cfg<KIND>::A_ATOMS + j), 0, 128, 0));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (KIND == kMx) {
+                            const uint32_t idesc = idesc_block_scaled(BM, BN, 0, 0, 1, kk, kk);
+                            mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa, sfb, acc);
+                        } else {
+                            const uint32_t idesc = idesc_block_scaled(BM, BN, 1, 1, 0, 0, 0);
+                            mma_nvf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 8 * kk, acc);
+                        }
+                    }
+                    mma_commit(smem_u32(&sh->empty[s]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&sh->tfull));
+            }
+            mma_commit(smem_u32(&sh->drain));
+            mbar_wait(smem_u32(&sh->drain), 0, abort, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale loader
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            ScaleRegs<KIND> cur, nxt;
+            load_scales<KIND>(cur, p, ti, 0, lane, sf_pitch);
+            for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
+                if (kb + 1 < nkb) load_scales<KIND>(nxt, p, ti, kb + 1, lane, sf_pitch);
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                store_scales<KIND>(cur, stages + s * SB + A_BYTES + B_BYTES, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
+                cur = nxt;
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue (8 warps)
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        float g = 1.0f;
+        if (KIND == kNv) g = __ldg(p.a_ts) * __ldg(p.b_ts);
+        uint32_t tcount = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const bool got = mbar_wait(smem_u32(&sh->tfull), tcount & 1, abort, p.status);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
+            tc_fence_after();
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + 128 * h + 32 * c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * g, __uint_as_float(r[2 * j + 1]) * g);
+                    packed[16 * c + j] = *reinterpret_cast<uint32_t*>(&v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
+            const int64_t row = ti.row0 + 32 * q + lane;
+            const int64_t col0 = ti.n0 + 128 * h;
+            if (row < ti.row_end) {
+                __nv_bfloat16* drow = p.d + row * p.n + col0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (col0 + 8 * j < p.n)
+                        *reinterpret_cast<uint4*>(drow + 8 * j) =
+                            make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int KIND>
+int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t st) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem_bytes<KIND>());
+        if (e != cudaSuccess) return (int)e;
+        attr_set[dev] = true;
+    }
+    gemm_mx_kernel<KIND><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
+    if (j.experts > kMaxExperts) return -3;
+    const bool nv = j.a_gran == 4;
+    const uint64_t kbytes = nv ? (uint64_t)j.k / 2 : (uint64_t)j.k;
+    const uint64_t b_rows = (uint64_t)j.n * (uint64_t)(j.experts > 0 ? j.experts : 1);
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8(&ta, j.a, kbytes, (uint64_t)j.m, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_u8(&tb, j.b, kbytes, b_rows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return (int)cudaErrorInvalidValue;
+    Params p{};
+    p.m = j.m; p.n = j.n; p.k = j.k;
+    p.sa = static_cast<const uint8_t*>(j.sa);
+    p.sb = static_cast<const uint8_t*>(j.sb);
+    p.a_ts = j.a_ts; p.b_ts = j.b_ts;
+    p.d = static_cast<__nv_bfloat16*>(j.d);
+    p.status = j.status;
+    p.offsets = j.offsets;
+    p.experts = j.experts;
+    const int sms = sm_count();
+    int grid = sms;
+    if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);
+    return nv ? launch_kind<kNv>(ta, tb, p, grid, st) : launch_kind<kMx>(ta, tb, p, grid, st);
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,47 @@
+// internal.h -- launchers behind the C ABI (host side, not exported).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+// Workspace layout: [0, 4) sticky status word; [256, ...) amax partials.
+constexpr size_t kWorkspaceBytes = 16384;
+constexpr size_t kPartialsOffset = 256;
+constexpr int kMaxPartials = (int)((kWorkspaceBytes - kPartialsOffset) / 4);
+
+int sm_count();  // of the current device, cached per device
+
+// ---- quantisers (quant.cu); return a cudaError_t as int
+struct QuantJob {
+    const uint16_t* x;  // BF16 bits
+    int64_t rows, cols, ldx;
+    int gran;
+    uint8_t* q;         // row-wise codes (may be null in transposed mode)
+    void* s;            // row-wise scales
+    uint8_t* qt;        // transposed codes (transposed mode)
+    void* st;           // transposed scales
+    float* tensor_scale;
+    bool given_scale;
+    uint32_t* partials; // amax partials (per-tensor / NVFP4)
+};
+int launch_quantize(const QuantJob& j, cudaStream_t s);
+int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
+
+// ---- GEMMs (gemm_blockwise.cu, gemm_mx.cu)
+struct GemmJob {
+    const void* a; const void* sa; int a_gran;
+    const void* b; const void* sb; int b_gran;
+    const float* a_ts; const float* b_ts;
+    int64_t m, n, k;
+    void* d;
+    int* status;
+    // grouped
+    const int64_t* offsets; int experts;  // experts == 0 -> dense
+};
+int launch_gemm_blockwise(const GemmJob& j, cudaStream_t s);
+int launch_gemm_mx(const GemmJob& j, cudaStream_t s);
+
+}  // namespace fp8bs

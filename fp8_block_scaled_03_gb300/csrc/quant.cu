@@ -1,0 +1,464 @@
+// quant.cu -- fused amax / scale / cast quantisers (BF16 -> E4M3 / E2M1).
+//
+// Steps 1 and 2 of "FP8 Quantization" (Unified FP8 review): S = max|X| / V_max
+// over the group, Q(x) = round(x / S), at the granularities of the
+// "Choose a precision" table of the "Low Precision RL" page.  All of them
+// are HBM-bound streaming kernels: every BF16 element is read once (twice
+// for the per-tensor / NVFP4 tensor amax), every code written once.
+//
+// Row-wise kernels: one warp task is one row segment of 1024 columns; a lane
+// owns 4 x 8 consecutive BF16 (four 16-byte loads in flight per lane).  A
+// 1x128 group is 16 lanes, a 1x32 group 4 lanes, a 1x16 group 2 lanes, so
+// every group amax is a handful of xor-shuffles; no shared memory.
+// 128x128 and transposed kernels: one CTA per 128x128 tile, the tile held
+// in registers (16 rows x 4 columns per thread), per-column partial amaxes
+// combined through shared memory.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+enum { kGranPT = 0, kGranTok = 1, kGranBlk = 2, kGranMx = 3, kGranNv = 4 };
+
+constexpr int kSeg = 1024;       // columns per row-wise warp task
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t absmax_v4(const uint4& v) {
+    return max(max(bf16x2_absmax_bits(v.x), bf16x2_absmax_bits(v.y)),
+               max(bf16x2_absmax_bits(v.z), bf16x2_absmax_bits(v.w)));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Eight elements x / S -> eight E4M3 bytes.
+__device__ __forceinline__ uint2 cast8_div(const float* f, float s) {
+    uint2 o;
+    o.x = e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+    o.y = e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    return o;
+}
+
+// Eight elements x * 2^-e (exact power-of-two division) -> eight E4M3 bytes.
+__device__ __forceinline__ uint2 cast8_mul(const float* f, float m) {
+    uint2 o;
+    o.x = e4m3x4(__fmul_rn(f[0], m), __fmul_rn(f[1], m), __fmul_rn(f[2], m), __fmul_rn(f[3], m));
+    o.y = e4m3x4(__fmul_rn(f[4], m), __fmul_rn(f[5], m), __fmul_rn(f[6], m), __fmul_rn(f[7], m));
+    return o;
+}
+
+// Block-wide max of a u32; every thread gets the result.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v) {
+    __shared__ uint32_t red[32];
+    v = warp_max_u32(v, 32);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    uint32_t r = 0;
+    const int nw = (blockDim.x + 31) >> 5;
+    for (int i = 0; i < nw; ++i) r = max(r, red[i]);
+    return r;
+}
+
+// Tensor amax (BF16 bits) from the per-CTA partials of amax_partials_kernel.
+__device__ __forceinline__ float tensor_amax(const uint32_t* __restrict__ partials, int nparts) {
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) m = max(m, partials[i]);
+    return amax_bits_to_f32(block_max_u32(m));
+}
+
+// ---------------------------------------------------------------- pass 1: amax partials
+__global__ void __launch_bounds__(kThreads)
+amax_partials_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                     uint32_t* __restrict__ partials) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t segs = ceil_div(cols, kSeg);
+    const int64_t total = rows * segs;
+    uint32_t m = 0;
+    for (int64_t t = gw; t < total; t += nw) {
+        const int64_t r = t / segs;
+        const int64_t cb = (t - r * segs) * kSeg;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = cb + j * 256 + lane * 8;
+            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = max(m, absmax_v4(v[j]));
+    }
+    m = block_max_u32(m);
+    if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// ---------------------------------------------------------------- row-wise 1x128 / 1x32 / per-tensor
+template <int GRAN>
+__global__ void __launch_bounds__(kThreads)
+quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                  uint8_t* __restrict__ q, void* __restrict__ sout,
+                  const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
+    const int lane = threadIdx.x & 31;
+    float s_uniform = 1.0f;
+    if constexpr (GRAN == kGranPT) {
+        if (given != nullptr) {
+            s_uniform = *given;
+        } else {
+            s_uniform = fp32_scale_from_amax(tensor_amax(partials, nparts));
+            if (blockIdx.x == 0 && threadIdx.x == 0) static_cast<float*>(sout)[0] = s_uniform;
+        }
+    }
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t segs = ceil_div(cols, kSeg);
+    const int64_t total = rows * segs;
+    const int64_t ng = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
+    for (int64_t t = gw; t < total; t += nw) {
+        const int64_t r = t / segs;
+        const int64_t cb = (t - r * segs) * kSeg;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = cb + j * 256 + lane * 8;
+            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = cb + j * 256 + lane * 8;
+            const bool ok = c < cols;
+            float f[8];
+            unpack8(v[j], f);
+            uint2 o;
+            if constexpr (GRAN == kGranTok) {
+                const uint32_t m = warp_max_u32(absmax_v4(v[j]), 16);
+                const float s = fp32_scale_from_amax(amax_bits_to_f32(m));
+                o = cast8_div(f, s);
+                if (ok && (lane & 15) == 0) static_cast<float*>(sout)[r * ng + (c >> 7)] = s;
+            } else if constexpr (GRAN == kGranMx) {
+                const uint32_t m = warp_max_u32(absmax_v4(v[j]), 4);
+                const int e = mx_exponent_from_amax_bits(m << 16);
+                o = cast8_mul(f, exp2_neg(e));
+                if (ok && (lane & 3) == 0) static_cast<uint8_t*>(sout)[r * ng + (c >> 5)] = (uint8_t)(e + 127);
+            } else {
+                o = cast8_div(f, s_uniform);
+            }
+            if (ok) *reinterpret_cast<uint2*>(q + r * cols + c) = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- NVFP4 1x16 (row-wise)
+__global__ void __launch_bounds__(kThreads)
+quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                   uint8_t* __restrict__ q, uint8_t* __restrict__ sb, float* __restrict__ tensor_scale,
+                   const uint32_t* __restrict__ partials, int nparts, bool given) {
+    const int lane = threadIdx.x & 31;
+    float s_g;
+    if (given) {
+        s_g = *tensor_scale;
+    } else {
+        const float amax = tensor_amax(partials, nparts);
+        s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kNvfp4GlobalDiv);
+        if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_g;
+    }
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t segs = ceil_div(cols, kSeg);
+    const int64_t total = rows * segs;
+    const int64_t nb = cols >> 4;
+    for (int64_t t = gw; t < total; t += nw) {
+        const int64_t r = t / segs;
+        const int64_t cb = (t - r * segs) * kSeg;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = cb + j * 256 + lane * 8;
+            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = cb + j * 256 + lane * 8;
+            const bool ok = c < cols;
+            const uint32_t m = warp_max_u32(absmax_v4(v[j]), 2);
+            const float amax_b = amax_bits_to_f32(m);
+            const uint32_t code = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, kE2M1Max), s_g));
+            const float big_s = __fmul_rn(e4m3_value(code), s_g);
+            float f[8];
+            unpack8(v[j], f);
+            uint32_t packed = 0;
+            if (big_s != 0.0f) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __fdiv_rn(f[i], big_s);
+                packed = e2m1x8(f);
+            }
+            if (ok) {
+                *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
+                if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- 128x128 (row-wise)
+__global__ void __launch_bounds__(kThreads)
+quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                   uint8_t* __restrict__ q, float* __restrict__ s) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int64_t c = c0 + (lane & 15) * 8;
+    const bool cok = c < cols;
+    uint4 v[8];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + 16 * w + 2 * i + (lane >> 4);
+        v[i] = (cok && r < rows) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, absmax_v4(v[i]));
+    const float sc = fp32_scale_from_amax(amax_bits_to_f32(block_max_u32(m)));
+    if (threadIdx.x == 0) s[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = sc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + 16 * w + 2 * i + (lane >> 4);
+        if (cok && r < rows) {
+            float f[8];
+            unpack8(v[i], f);
+            *reinterpret_cast<uint2*>(q + r * cols + c) = cast8_div(f, sc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- transposed (+ optional row-wise)
+// CTA tile: 128 rows x 128 columns of X; warp w owns rows 16w..16w+15, lane l
+// owns columns 4l..4l+3.  Codes of X^T go out as 16-byte runs (16 rows of one
+// column); the optional row-wise codes as 4-byte runs.
+template <int GRAN, bool DUAL>
+__global__ void __launch_bounds__(kThreads)
+quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                    uint8_t* __restrict__ qt, void* __restrict__ st,
+                    uint8_t* __restrict__ q, void* __restrict__ s,
+                    const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
+    __shared__ uint32_t red[8][128];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rt = blockIdx.y, ct = blockIdx.x;
+    const int64_t r0 = rt * 128, c0 = ct * 128;
+    const int64_t cc = c0 + lane * 4;
+    const bool cok = cc < cols;
+    const int64_t rw = r0 + 16 * w;          // first row of this warp
+    const bool wok = rw < rows;              // rows % 16 == 0: 16 rows all valid or all not
+
+    float s_uniform = 1.0f;
+    if constexpr (GRAN == kGranPT) {
+        if (given != nullptr) {
+            s_uniform = *given;
+        } else {
+            s_uniform = fp32_scale_from_amax(tensor_amax(partials, nparts));
+            if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+                static_cast<float*>(st)[0] = s_uniform;
+                if (DUAL) static_cast<float*>(s)[0] = s_uniform;
+            }
+        }
+    }
+
+    uint2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = (cok && wok) ? ldg_v2(x + (rw + i) * ldx + cc) : make_uint2(0, 0);
+
+    uint32_t cm[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        cm[0] = max(cm[0], v[i].x & 0x7FFFu);
+        cm[1] = max(cm[1], (v[i].x >> 16) & 0x7FFFu);
+        cm[2] = max(cm[2], v[i].y & 0x7FFFu);
+        cm[3] = max(cm[3], (v[i].y >> 16) & 0x7FFFu);
+    }
+
+    float col_s[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // divisor (FP32 grans) or multiplier (MX)
+    int col_e[4] = {0, 0, 0, 0};
+    float s_blk = 1.0f;
+    if constexpr (GRAN == kGranTok || GRAN == kGranMx) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[w][lane * 4 + j] = cm[j];
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t m = 0;
+            if constexpr (GRAN == kGranTok) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = max(m, red[k][lane * 4 + j]);
+                col_s[j] = fp32_scale_from_amax(amax_bits_to_f32(m));
+            } else {
+                const int g = w & ~1;
+                m = max(red[g][lane * 4 + j], red[g + 1][lane * 4 + j]);
+                col_e[j] = mx_exponent_from_amax_bits(m << 16);
+                col_s[j] = exp2_neg(col_e[j]);
+            }
+        }
+    } else if constexpr (GRAN == kGranBlk) {
+        s_blk = fp32_scale_from_amax(amax_bits_to_f32(block_max_u32(max(max(cm[0], cm[1]), max(cm[2], cm[3])))));
+    }
+
+    // ---- transposed codes: column cc + j, rows rw .. rw+15
+    if (cok && wok) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t word = (j < 2) ? v[i].x : v[i].y;
+                f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+            }
+            float d = (GRAN == kGranPT) ? s_uniform : (GRAN == kGranBlk ? s_blk : col_s[j]);
+            uint4 o;
+            if constexpr (GRAN == kGranMx) {
+                o.x = e4m3x4(__fmul_rn(f[0], d), __fmul_rn(f[1], d), __fmul_rn(f[2], d), __fmul_rn(f[3], d));
+                o.y = e4m3x4(__fmul_rn(f[4], d), __fmul_rn(f[5], d), __fmul_rn(f[6], d), __fmul_rn(f[7], d));
+                o.z = e4m3x4(__fmul_rn(f[8], d), __fmul_rn(f[9], d), __fmul_rn(f[10], d), __fmul_rn(f[11], d));
+                o.w = e4m3x4(__fmul_rn(f[12], d), __fmul_rn(f[13], d), __fmul_rn(f[14], d), __fmul_rn(f[15], d));
+            } else {
+                o.x = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
+                o.y = e4m3x4(__fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
+                o.z = e4m3x4(__fdiv_rn(f[8], d), __fdiv_rn(f[9], d), __fdiv_rn(f[10], d), __fdiv_rn(f[11], d));
+                o.w = e4m3x4(__fdiv_rn(f[12], d), __fdiv_rn(f[13], d), __fdiv_rn(f[14], d), __fdiv_rn(f[15], d));
+            }
+            *reinterpret_cast<uint4*>(qt + (cc + j) * rows + rw) = o;
+        }
+    }
+    // ---- scales of X^T ([cols, *] grid)
+    if constexpr (GRAN == kGranTok) {
+        if (w == 0 && cok) {
+            const int64_t nrb = ceil_div(rows, 128);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) static_cast<float*>(st)[(cc + j) * nrb + rt] = col_s[j];
+        }
+    } else if constexpr (GRAN == kGranMx) {
+        if ((w & 1) == 0 && cok && wok) {
+            const int64_t nrb = ceil_div(rows, 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) static_cast<uint8_t*>(st)[(cc + j) * nrb + (rw >> 5)] = (uint8_t)(col_e[j] + 127);
+        }
+    } else if constexpr (GRAN == kGranBlk) {
+        if (threadIdx.x == 0) static_cast<float*>(st)[ct * gridDim.y + rt] = s_blk;
+    }
+
+    // ---- row-wise codes of X from the same registers
+    if constexpr (DUAL) {
+        const int64_t ncb = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float f[4] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y)};
+            const uint32_t m4 = max(bf16x2_absmax_bits(v[i].x), bf16x2_absmax_bits(v[i].y));
+            uint32_t o;
+            if constexpr (GRAN == kGranTok) {
+                const float sr = fp32_scale_from_amax(amax_bits_to_f32(warp_max_u32(m4, 32)));
+                o = e4m3x4(__fdiv_rn(f[0], sr), __fdiv_rn(f[1], sr), __fdiv_rn(f[2], sr), __fdiv_rn(f[3], sr));
+                if (lane == 0 && wok) static_cast<float*>(s)[(rw + i) * ncb + ct] = sr;
+            } else if constexpr (GRAN == kGranMx) {
+                const int e = mx_exponent_from_amax_bits(warp_max_u32(m4, 8) << 16);
+                const float mm = exp2_neg(e);
+                o = e4m3x4(__fmul_rn(f[0], mm), __fmul_rn(f[1], mm), __fmul_rn(f[2], mm), __fmul_rn(f[3], mm));
+                if ((lane & 7) == 0 && cok && wok) static_cast<uint8_t*>(s)[(rw + i) * ncb + (cc >> 5)] = (uint8_t)(e + 127);
+            } else {
+                const float d = (GRAN == kGranPT) ? s_uniform : s_blk;
+                o = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
+            }
+            if (cok && wok) *reinterpret_cast<uint32_t*>(q + (rw + i) * cols + cc) = o;
+        }
+        if constexpr (GRAN == kGranBlk) {
+            if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = s_blk;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+static int rowwise_blocks(int64_t rows, int64_t cols, int cap) {
+    const int64_t tasks = rows * ceil_div(cols, kSeg);
+    const int64_t want = ceil_div(tasks, kThreads / 32);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
+}
+
+static int launch_amax(const QuantJob& j, cudaStream_t st, int* nparts) {
+    const int n = rowwise_blocks(j.rows, j.cols, std::min(kMaxPartials, sm_count() * 4));
+    amax_partials_kernel<<<n, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.partials);
+    *nparts = n;
+    return (int)cudaGetLastError();
+}
+
+int launch_quantize(const QuantJob& j, cudaStream_t st) {
+    const int cap = sm_count() * 8;
+    const int nb = rowwise_blocks(j.rows, j.cols, cap);
+    int nparts = 0;
+    switch (j.gran) {
+    case kGranTok:
+        quant_rows_kernel<kGranTok><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0, nullptr);
+        break;
+    case kGranMx:
+        quant_rows_kernel<kGranMx><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0, nullptr);
+        break;
+    case kGranPT: {
+        if (!j.given_scale) {
+            const int e = launch_amax(j, st, &nparts);
+            if (e) return e;
+        }
+        quant_rows_kernel<kGranPT><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, j.partials, nparts,
+                                                             j.given_scale ? static_cast<const float*>(j.s) : nullptr);
+        break;
+    }
+    case kGranBlk: {
+        dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
+        quant_block_kernel<<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, static_cast<float*>(j.s));
+        break;
+    }
+    case kGranNv: {
+        if (!j.given_scale) {
+            const int e = launch_amax(j, st, &nparts);
+            if (e) return e;
+        }
+        quant_nvfp4_kernel<<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, static_cast<uint8_t*>(j.s),
+                                                    j.tensor_scale, j.partials, nparts, j.given_scale);
+        break;
+    }
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+    return (int)cudaGetLastError();
+}
+
+template <int GRAN>
+static void launch_tile(const QuantJob& j, cudaStream_t st, int nparts, const float* given) {
+    dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
+    if (j.q != nullptr)
+        quant_tile_t_kernel<GRAN, true><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q, j.s,
+                                                                   j.partials, nparts, given);
+    else
+        quant_tile_t_kernel<GRAN, false><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, nullptr,
+                                                                    nullptr, j.partials, nparts, given);
+}
+
+int launch_quantize_transposed(const QuantJob& j, cudaStream_t st) {
+    int nparts = 0;
+    switch (j.gran) {
+    case kGranTok: launch_tile<kGranTok>(j, st, 0, nullptr); break;
+    case kGranMx: launch_tile<kGranMx>(j, st, 0, nullptr); break;
+    case kGranBlk: launch_tile<kGranBlk>(j, st, 0, nullptr); break;
+    case kGranPT: {
+        if (!j.given_scale) {
+            const int e = launch_amax(j, st, &nparts);
+            if (e) return e;
+        }
+        launch_tile<kGranPT>(j, st, nparts, j.given_scale ? static_cast<const float*>(j.st) : nullptr);
+        break;
+    }
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+    return (int)cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,202 @@
+/*
+ * fp8bs.h -- C ABI of the block-scaled low-precision linear layer (sm_103a).
+ *
+ * What is computed (page title, section):
+ *   "Unified FP8: Beyond Mixed Precision, Achieving Stable Accelerated MoE RL
+ *    Training", section "FP8 Quantization":
+ *      Step 1  S = max|X| / V_max  over the tensor or one block,
+ *      Step 2  Q(x) = round(x / S),
+ *   at per-tensor, per-token and per-block granularity, FP32 scales
+ *   (section "FP8 Scale Selection"), E4M3 codes (section "FP8 Format").
+ *   "Low Precision RL", table "Choose a precision": block-wise FP8 128x128
+ *   with FP32 scales, MXFP8 1x32 with UE8M0 scales, NVFP4 E2M1 1x16 with an
+ *   E4M3 block scale and an outer FP32 scale; sections "3. Unified MXFP8
+ *   (Blackwell)" (MXFP8 also for weight-gradient and data-gradient GEMMs)
+ *   and "4. NVFP4 (Blackwell)".
+ *
+ * Arithmetic contract (bit-exact against the CPU oracle):
+ *   amax is exact; FP32 scales are IEEE float32 S = amax / 448 (S = 1 when
+ *   amax = 0); codes are the saturating round-to-nearest-even E4M3 cast of
+ *   the IEEE float32 quotient x / S.  MXFP8: S = 2^e with e the smallest
+ *   integer such that 448 * 2^e >= amax, clamped to [-127, 127], stored as
+ *   the UE8M0 byte e + 127 (amax = 0 gives byte 0).  NVFP4: S_g = amax_T /
+ *   2688 (1 when amax_T = 0), block byte s_b = E4M3((amax_b / 6) / S_g),
+ *   S_b = E4M3value(s_b) * S_g in float32, codes E2M1(x / S_b), all-zero
+ *   codes for a block whose s_b is 0.  Inputs must be finite BF16.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates or frees memory, never synchronises, and
+ *     enqueues all work on `stream` (a cudaStream_t; NULL = legacy stream).
+ *   - Matrices are row-major.  `ld_x` is the row pitch of the BF16 input in
+ *     elements.  Outputs are densely packed (pitch = their column count).
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns a negative fp8bs_status and enqueues nothing.
+ *   - `workspace` is a caller-owned device buffer of at least
+ *     FP8BS_WORKSPACE_BYTES bytes, zero-filled once by the caller before its
+ *     first use.  Its first 4 bytes are a sticky device status word that
+ *     kernels set (never clear) when a bounded wait gives up; read it with
+ *     fp8bs_read_status and clear it with fp8bs_clear_status.  The rest is
+ *     scratch for the per-tensor / NVFP4 amax reduction.  Calls that share a
+ *     workspace must be ordered on the GPU (same stream or events).
+ *   - Launch failures return FP8BS_ECUDA (cudaGetLastError is consumed).
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8bs_stream_t;   /* identical to cudaStream_t */
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_EINVAL = -1,        /* bad size, granularity, or NULL pointer */
+    FP8BS_EALIGN = -2,        /* pointer or pitch not 16-byte aligned */
+    FP8BS_EUNSUPPORTED = -3,  /* valid request this library does not implement */
+    FP8BS_ECUDA = -4,         /* a CUDA runtime call or launch failed */
+    FP8BS_ETIMEOUT = -5,      /* (status word) a bounded device wait gave up */
+    FP8BS_EWORKSPACE = -6     /* workspace NULL or smaller than required */
+} fp8bs_status;
+
+typedef enum {
+    FP8BS_PER_TENSOR = 0,     /* one float32 scale for the tensor */
+    FP8BS_TOKEN_1x128 = 1,    /* float32 scale per row and 128 columns */
+    FP8BS_BLOCK_128x128 = 2,  /* float32 scale per 128x128 tile */
+    FP8BS_MXFP8_1x32 = 3,     /* UE8M0 byte per row and 32 columns */
+    FP8BS_NVFP4_1x16 = 4      /* E4M3 byte per row and 16 columns + float32 S_g */
+} fp8bs_gran;
+
+#define FP8BS_WORKSPACE_BYTES ((size_t)16384)
+
+/* flags for fp8_quantize / fp8_quantize_transposed */
+#define FP8BS_FLAG_GIVEN_TENSOR_SCALE 1u  /* PER_TENSOR / NVFP4: *tensor_scale is
+                                             an input (S, resp. S_g); skip the amax pass */
+
+/*
+ * fp8_quantize -- row-wise quantisation of a BF16 matrix x [rows, cols].
+ *
+ * Steps 1-2 of "FP8 Quantization" (review) at granularity `gran`.
+ * Requirements: cols % 8 == 0 (cols % 16 == 0 for NVFP4), ld_x >= cols,
+ * ld_x % 8 == 0, x 16-byte aligned, q 16-byte aligned.  rows or cols == 0
+ * is a no-op (pointers are then not examined and may be NULL).  A last
+ * group that runs past cols (or past rows for 128x128) is ragged: its amax
+ * covers only the elements that exist.
+ *
+ *   gran             q (uint8)             scales
+ *   PER_TENSOR       E4M3 [rows, cols]     float32 [1]
+ *   TOKEN_1x128      E4M3 [rows, cols]     float32 [rows, ceil(cols/128)]
+ *   BLOCK_128x128    E4M3 [rows, cols]     float32 [ceil(rows/128), ceil(cols/128)]
+ *   MXFP8_1x32       E4M3 [rows, cols]     uint8 UE8M0 [rows, ceil(cols/32)]
+ *   NVFP4_1x16       E2M1 [rows, cols/2]   uint8 E4M3 [rows, cols/16]
+ *                    (element 2j in the low nibble of byte j)
+ *
+ * tensor_scale: NVFP4 only, device float32[1], receives S_g (or supplies it
+ * with FP8BS_FLAG_GIVEN_TENSOR_SCALE).  PER_TENSOR with that flag reads S
+ * from scales[0].  Otherwise may be NULL.
+ * workspace: required for PER_TENSOR and NVFP4 (amax partials); may be
+ * NULL for the other granularities.
+ */
+int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
+                 void* q, void* scales, float* tensor_scale, unsigned flags,
+                 void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8_quantize_transposed -- quantise X^T [cols, rows] from the same BF16
+ * source, and optionally X itself in the same pass over memory.
+ *
+ * Used by the backward GEMMs ("Low Precision RL", "3. Unified MXFP8
+ * (Blackwell)": low-precision weight-gradient and data-gradient GEMMs),
+ * which contract over the other axis of X.  The result is exactly
+ * fp8_quantize applied to the transposed BF16 matrix (never a re-rounding
+ * of already-quantised codes).  For BLOCK_128x128 the codes are the
+ * transpose of the row-wise codes and the scales the transposed scale grid.
+ *
+ * gran: PER_TENSOR, TOKEN_1x128, BLOCK_128x128 or MXFP8_1x32 (NVFP4 returns
+ * FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
+ *   q_t      uint8 [cols, rows]           codes of X^T
+ *   scales_t layout of the table above for a [cols, rows] matrix
+ *   q, scales  optional (both NULL or both set): the row-wise result of
+ *            fp8_quantize(x, gran), produced from the same read of x.
+ */
+int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
+                            void* q_t, void* scales_t, void* q, void* scales,
+                            float* tensor_scale, unsigned flags,
+                            void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8_block_gemm -- D[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], D in BF16.
+ *
+ * The matching low-precision GEMM of "Low Precision RL" ("Unified training
+ * recipe"), on operands quantised as above, with FP32 accumulation on the
+ * tensor cores.  A is [m, k], B is [n, k]; both K-major (row-major with k
+ * contiguous); D is row-major [m, n] BF16 (round-to-nearest-even).
+ *
+ *   (a_gran, b_gran)                          scale handling
+ *   {PER_TENSOR,TOKEN_1x128,BLOCK_128x128}^2  FP32 scales applied per
+ *       128-wide K block to the FP32 partial sums (k % 128 == 0)
+ *   (MXFP8_1x32, MXFP8_1x32)                  UE8M0 scales applied by the
+ *       tensor core per 32-wide K block (k % 128 == 0)
+ *   (NVFP4_1x16, NVFP4_1x16)                  E4M3 block scales applied by
+ *       the tensor core per 16-wide K block, times *a_tensor_scale *
+ *       *b_tensor_scale (k % 256 == 0); a, b are packed E2M1 [m|n, k/2]
+ * Other pairs return FP8BS_EUNSUPPORTED.  Scale layouts are those written
+ * by fp8_quantize for the operand's own [rows, k] shape.  m, n > 0,
+ * n % 8 == 0; a, b, d 16-byte aligned.  a_tensor_scale / b_tensor_scale:
+ * device float32[1], NVFP4 only (else ignored, may be NULL).
+ * workspace: required (status word for the bounded pipeline waits).
+ */
+int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
+                   const void* b, const void* b_scales, int b_gran,
+                   const float* a_tensor_scale, const float* b_tensor_scale,
+                   int64_t m, int64_t n, int64_t k, void* d,
+                   void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8_grouped_gemm -- MoE grouped (per-expert) GEMM.
+ *
+ * Rows offsets[e] .. offsets[e+1]-1 of A (expert-contiguous routed tokens)
+ * are multiplied by expert e's weight B[e] ([n, k]):
+ *   D[r, j] = sum_k deq(A)[r, k] * deq(B[e])[j, k]   for offsets[e] <= r < offsets[e+1]
+ * ("Low Precision RL", "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend
+ * chosen separately from the dense one).  offsets: DEVICE int64 [experts+1],
+ * non-decreasing, offsets[0] == 0, offsets[experts] == total_rows (not
+ * checked on the host; the host never reads it).  Experts with no rows
+ * cost nothing.  gran: MXFP8_1x32 (k % 128 == 0) or TOKEN_1x128 for A with
+ * BLOCK_128x128 for B (k % 128 == 0, FP32 scales).  a: [total_rows, k],
+ * a_scales as fp8_quantize for [total_rows, k]; b: [experts, n, k] codes,
+ * b_scales: per-expert scale grids stacked along the expert axis.
+ * D: BF16 [total_rows, n].  n % 8 == 0.  workspace required.
+ */
+int fp8_grouped_gemm(const void* a, const void* a_scales,
+                     const void* b, const void* b_scales,
+                     const int64_t* offsets, int experts, int64_t total_rows,
+                     int64_t n, int64_t k, int gran, void* d,
+                     void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/* Bytes of workspace every entry point accepts (FP8BS_WORKSPACE_BYTES). */
+size_t fp8bs_workspace_size(void);
+
+/* Synchronises `stream`, then returns the sticky device status word of
+ * `workspace` (FP8BS_OK, or FP8BS_ETIMEOUT if a bounded wait gave up), or
+ * FP8BS_ECUDA if the copy failed. */
+int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream);
+
+/* Enqueues a reset of the status word to FP8BS_OK on `stream`. */
+int fp8bs_clear_status(void* workspace, fp8bs_stream_t stream);
+
+/* Static English text for a status code. */
+const char* fp8bs_status_string(int status);
+
+/* ABI version: 100 * major + minor. */
+int fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

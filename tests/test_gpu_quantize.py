@@ -1,0 +1,178 @@
+"""GPU quantisers vs the CPU oracle: codes and scales must match bit for bit.
+
+Cases: the tiny blockwise-linear operands, the full 8192x4096 quantise
+sweep (every granularity, row-wise, transposed and dual outputs), ragged
+groups and tiles, strided input rows, empty input, all-zero and extreme
+magnitude tensors, and a sweep of every BF16 bit pattern.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import formats as OF
+from oracle import quantize as OQ
+from tests._util import np_f32, np_u8, to_dev_bf16, to_f32
+
+pytestmark = pytest.mark.gpu
+
+fp = pytest.importorskip("fp8_block_scaled_03_gb300")
+
+ROW_ORACLE = {
+    "per_tensor": OQ.quantize_per_tensor,
+    "1x128": OQ.quantize_1x128,
+    "128x128": OQ.quantize_128x128,
+    "mxfp8": OQ.quantize_mxfp8,
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from fp8_block_scaled_03_gb300 import build
+    build.build()
+    fp.load_library()
+    assert torch.cuda.is_available()
+
+
+def check_rowwise(bits, gran, x_dev=None):
+    x = to_f32(bits)
+    xd = x_dev if x_dev is not None else to_dev_bf16(bits)
+    q, s, ts = fp.fp8_quantize(xd, gran)
+    torch.cuda.synchronize()
+    if gran == "nvfp4":
+        pq, sb, sg = OQ.quantize_nvfp4(x)
+        assert np.array_equal(np_u8(q), pq)
+        assert np.array_equal(np_u8(s), sb)
+        assert np_f32(ts)[0] == sg
+        return
+    rq, rs = ROW_ORACLE[gran](x)
+    assert np.array_equal(np_u8(q), rq), f"{gran}: {(np_u8(q) != rq).sum()} codes differ"
+    if gran == "mxfp8":
+        assert np.array_equal(np_u8(s), rs)
+    else:
+        assert np.array_equal(np_f32(s).reshape(np.shape(rs)), np.asarray(rs, dtype=np.float32))
+
+
+def check_transposed(bits, gran, dual):
+    x = to_f32(bits)
+    xd = to_dev_bf16(bits)
+    qt, st, q, s = fp.fp8_quantize_transposed(xd, gran, also_rowwise=dual)
+    torch.cuda.synchronize()
+    rq, rs = OQ.transposed(ROW_ORACLE[gran], x)
+    assert np.array_equal(np_u8(qt), rq), f"{gran}^T: {(np_u8(qt) != rq).sum()} codes differ"
+    if gran == "mxfp8":
+        assert np.array_equal(np_u8(st), rs)
+    else:
+        assert np.array_equal(np_f32(st).reshape(np.shape(rs)), np.asarray(rs, dtype=np.float32))
+    if dual:
+        rq2, rs2 = ROW_ORACLE[gran](x)
+        assert np.array_equal(np_u8(q), rq2)
+        if gran == "mxfp8":
+            assert np.array_equal(np_u8(s), rs2)
+        else:
+            assert np.array_equal(np_f32(s).reshape(np.shape(rs2)), np.asarray(rs2, dtype=np.float32))
+
+
+GRANS = ["per_tensor", "1x128", "128x128", "mxfp8"]
+
+
+# -------------------------------------------------------------- tiny blockwise linear operands
+def test_tiny_linear_operands():
+    x = synth.activations((128, 256), seed=0, outlier_frac=0.01, outlier_mult=50.0)
+    w = synth.weights((256, 256), seed=1, std=0.02)
+    check_rowwise(x, "1x128")
+    check_rowwise(w, "128x128")
+
+
+# -------------------------------------------------------------- full-size quantise sweep
+@pytest.fixture(scope="module")
+def sweep_bits():
+    return synth.activations((8192, 4096), seed=0, outlier_frac=0.001, outlier_mult=100.0)
+
+
+@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+def test_sweep_rowwise(sweep_bits, gran):
+    check_rowwise(sweep_bits, gran)
+
+
+@pytest.mark.parametrize("gran", GRANS)
+def test_sweep_transposed_dual(sweep_bits, gran):
+    check_transposed(sweep_bits, gran, dual=True)
+
+
+# -------------------------------------------------------------- shapes and edge cases
+@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+@pytest.mark.parametrize("shape", [(1, 16), (3, 200), (130, 264), (257, 1032), (64, 4096)])
+def test_ragged_rowwise(gran, shape):
+    if gran == "nvfp4" and shape[1] % 16:
+        pytest.skip("NVFP4 needs cols % 16")
+    bits = synth.activations(shape, seed=sum(shape), outlier_frac=0.02, outlier_mult=80.0)
+    check_rowwise(bits, gran)
+
+
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("dual", [False, True])
+@pytest.mark.parametrize("shape", [(16, 8), (144, 200), (272, 392), (128, 128)])
+def test_ragged_transposed(gran, dual, shape):
+    bits = synth.activations(shape, seed=3 * sum(shape), outlier_frac=0.02, outlier_mult=80.0)
+    check_transposed(bits, gran, dual)
+
+
+@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+def test_strided_rows(gran):
+    bits = synth.activations((96, 384), seed=5)
+    big = torch.zeros((96, 512), dtype=torch.bfloat16, device="cuda")
+    big[:, :384] = to_dev_bf16(bits)
+    check_rowwise(bits, gran, x_dev=big[:, :384])
+
+
+@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+def test_zero_and_extreme_tensors(gran):
+    zeros = np.zeros((64, 256), dtype=np.uint16)
+    zeros[3, 7] = 0x8000                                   # a negative zero
+    check_rowwise(zeros, gran)
+    g = np.random.Generator(np.random.PCG64(9))
+    extreme = np.where(g.random((64, 256)) < 0.5,
+                       synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(3e37)),
+                       synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(1e-38)))
+    check_rowwise(extreme.astype(np.uint16), gran)
+    tiny = synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(1e-39))
+    check_rowwise(tiny, gran)
+
+
+def test_every_bf16_pattern():
+    """All 65536 BF16 bit patterns except inf/NaN, in several group contexts."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = allbits[(allbits & 0x7F80) != 0x7F80]
+    g = np.random.Generator(np.random.PCG64(10))
+    perm = finite[g.permutation(finite.size)]
+    n = (perm.size // 512) * 512
+    bits = perm[:n].reshape(-1, 512)
+    for gran in GRANS + ["nvfp4"]:
+        check_rowwise(bits, gran)
+    # every pattern with |x| <= 448 under a scale of exactly 1 (amax 448 in every group)
+    small = finite[(finite & 0x7FFF) <= 0x43E0]
+    small = small[g.permutation(small.size)]
+    fixed = small[: (small.size // 512) * 512].reshape(-1, 512).copy()
+    fixed[:, ::32] = 0x43E0                                 # 448.0
+    for gran in ("1x128", "mxfp8"):
+        check_rowwise(fixed, gran)
+
+
+def test_empty_is_noop():
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    q, s, _ = fp.fp8_quantize(x, "1x128")
+    assert q.shape == (0, 128)
+
+
+def test_given_tensor_scale():
+    bits = synth.activations((64, 256), seed=12)
+    x = to_f32(bits)
+    xd = to_dev_bf16(bits)
+    s_in = torch.tensor([0.125], dtype=torch.float32, device="cuda")
+    q, s, _ = fp.fp8_quantize(xd, "per_tensor", scales=s_in.clone(), flags=fp.FLAG_GIVEN_TENSOR_SCALE)
+    assert np.array_equal(np_u8(q), OQ.cast_e4m3(x, np.float32(0.125)))
+    sg = torch.tensor([np.float32(0.01)], dtype=torch.float32, device="cuda")
+    pq, sb, _ = fp.fp8_quantize(xd, "nvfp4", tensor_scale=sg, flags=fp.FLAG_GIVEN_TENSOR_SCALE)
+    rq, rsb, _ = OQ.quantize_nvfp4(x, s_g=np.float32(0.01))
+    assert np.array_equal(np_u8(pq), rq) and np.array_equal(np_u8(sb), rsb)
