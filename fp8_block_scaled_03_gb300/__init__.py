@@ -31,7 +31,7 @@ STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNS
           -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE"}
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
-           "fp8bs_status_string", "fp8bs_version")
+           "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm")
 
 _lib = None
 
@@ -56,6 +56,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_quantize_transposed.argtypes = [P, I64, I64, I64, I, P, P, P, P, P, U, P, SZ, P]
     lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
     lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
+    lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
     lib.fp8bs_read_status.argtypes = [P, P]
@@ -64,7 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8bs_status_string.argtypes = [I]
     lib.fp8bs_version.argtypes = []
     for name in ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
-                 "fp8bs_read_status", "fp8bs_clear_status", "fp8bs_version"):
+                 "fp8bs_read_status", "fp8bs_clear_status", "fp8bs_version", "fp8bs_test_stalled_gemm"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -226,3 +227,17 @@ def fp8_grouped_gemm(a, a_scales, b, b_scales, offsets, gran, *, out=None, ws=No
                                          _stream(stream))
     _check("fp8_grouped_gemm", rc)
     return out
+
+
+def test_stalled_gemm(a, a_scales, b, b_scales, wait_limit_ns: int, *, out=None, ws=None, stream=None) -> int:
+    """Run the MXFP8 GEMM with its producer withholding stage 0 (test hook for the
+    bounded waits); returns the launch status.  The timeout shows up in the
+    workspace status word (read_status)."""
+    m, k = a.shape
+    n = b.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    ws = ws if ws is not None else workspace(a.device)
+    return load_library().fp8bs_test_stalled_gemm(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), m, n, k,
+                                                  _ptr(out), int(wait_limit_ns), _ptr(ws), ws.numel(),
+                                                  _stream(stream))

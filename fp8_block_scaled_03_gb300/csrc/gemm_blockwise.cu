@@ -52,6 +52,8 @@ struct Params {
     int* status;
     const int64_t* offsets;
     int experts;
+    uint64_t wait_ns;     // bound of every pipeline wait
+    int stall_stage0;     // test hook: the producer withholds stage 0
 };
 
 struct alignas(16) Shared {
@@ -124,7 +126,8 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
+                    if (p.stall_stage0 && it == 0) continue;   // test hook: never fill stage 0
                     const uint32_t fb = smem_u32(&sh->full[s]);
                     uint8_t* sa_ptr = stages + (size_t)s * STAGE_BYTES;
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -132,10 +135,11 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     tma_load_2d(smem_u32(sa_ptr + A_BYTES), &tm_b, fb, (int32_t)(kb * BK), brow);
                 }
             }
-            if (!ok) {  // let copies already issued land before the CTA exits
-                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    mbar_wait(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, abort, p.status);
-            }
+            // Copies issued to the last STAGES stages must have landed before
+            // the CTA exits (on the normal path they already have).
+            for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                if (!(p.stall_stage0 && j == 0))
+                    mbar_wait_drain(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -147,8 +151,8 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
-                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status)) { ok = false; break; }
-                    if (!mbar_wait(smem_u32(&sh->tempty[b]), tph ^ 1, abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status, p.wait_ns)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->tempty[b]), tph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(stages + (size_t)s * STAGE_BYTES);
                     const uint64_t adesc = kmajor_sw128_desc(a_addr);
@@ -317,6 +321,8 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
     p.status = j.status;
     p.offsets = j.offsets;
     p.experts = j.experts;
+    p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
+    p.stall_stage0 = j.stall_stage0;
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) {

@@ -65,6 +65,8 @@ struct Params {
     int* status;
     const int64_t* offsets;
     int experts;
+    uint64_t wait_ns;     // bound of every pipeline wait
+    int stall_stage0;     // test hook: the producer withholds stage 0
 };
 
 template <int STAGES>
@@ -199,7 +201,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
+                    if (p.stall_stage0 && it == 0) continue;   // test hook: never fill stage 0
                     const uint32_t fb = smem_u32(&sh->full[s]);
                     uint8_t* st = stages + s * SB;
                     mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
@@ -207,10 +210,11 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     tma_load_2d(smem_u32(st + A_BYTES), &tm_b, fb, (int32_t)(kb * BKB), brow);
                 }
             }
-            if (!ok) {
-                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    mbar_wait(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, abort, p.status);
-            }
+            // Copies issued to the last STAGES stages must have landed before
+            // the CTA exits (on the normal path they already have).
+            for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                if (!(p.stall_stage0 && j == 0))
+                    mbar_wait_drain(smem_u32(&sh->full[j % STAGES]), (j / STAGES) & 1, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -219,11 +223,11 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
-                if (!mbar_wait(smem_u32(&sh->tempty), (tcount & 1) ^ 1, abort, p.status)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&sh->tempty), (tcount & 1) ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status, p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     uint8_t* st = stages + s * SB;
                     const uint32_t a_addr = smem_u32(st);
@@ -269,7 +273,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                 if (kb + 1 < nkb) load_scales<KIND>(nxt, p, ti, kb + 1, lane, sf_pitch);
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                 store_scales<KIND>(cur, stages + s * SB + A_BYTES + B_BYTES, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -361,6 +365,8 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     p.status = j.status;
     p.offsets = j.offsets;
     p.experts = j.experts;
+    p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
+    p.stall_stage0 = j.stall_stage0;
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);

@@ -40,6 +40,8 @@ struct GemmJob {
     int* status;
     // grouped
     const int64_t* offsets; int experts;  // experts == 0 -> dense
+    uint64_t wait_ns = 0;                 // 0 -> default bound (1 s)
+    int stall_stage0 = 0;                 // test hook (fp8bs_test_stalled_gemm)
 };
 int launch_gemm_blockwise(const GemmJob& j, cudaStream_t s);
 int launch_gemm_mx(const GemmJob& j, cudaStream_t s);

@@ -58,22 +58,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Gives up after
-// kWaitLimitNs, or as soon as another role of the CTA has given up
+// `limit_ns`, or as soon as another role of the CTA has given up
 // (*abort != 0); on giving up it sets *abort, records FP8BS_ETIMEOUT in the
 // sticky status word, and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 atomicExch(status, kStatusTimeout);
                 return false;
             }
         }
+    }
+}
+
+// Teardown wait for asynchronous work this CTA itself started (TMA copies,
+// MMAs): bounded by time only, deliberately deaf to the abort flag, so that
+// an aborting CTA does not leave copies landing in shared memory it no
+// longer owns.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && globaltimer() - t0 > limit_ns) return false;
     }
 }
 

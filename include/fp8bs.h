@@ -178,6 +178,22 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
                      int64_t n, int64_t k, int gran, void* d,
                      void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
 
+/*
+ * fp8bs_test_stalled_gemm -- test hook for the bounded pipeline waits.
+ *
+ * Runs the MXFP8 fp8_block_gemm (same arguments and requirements) with its
+ * TMA producer withholding the first pipeline stage, so the MMA issuer waits
+ * on a barrier that nothing will complete.  Every wait is bounded by
+ * wait_limit_ns (1 .. 2e9): the kernel gives up, writes FP8BS_ETIMEOUT to
+ * the workspace status word, lets its own copies in flight land, frees its
+ * tensor memory and returns; the CUDA context stays usable.  No counterpart
+ * on the pages: it exists to test failure detection without a GPU fault.
+ * The contents of d are unspecified afterwards.
+ */
+int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, const void* b_scales,
+                            int64_t m, int64_t n, int64_t k, void* d, uint64_t wait_limit_ns,
+                            void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
 /* Bytes of workspace every entry point accepts (FP8BS_WORKSPACE_BYTES). */
 size_t fp8bs_workspace_size(void);
 

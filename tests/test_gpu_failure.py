@@ -1,0 +1,37 @@
+"""Failure detection without a GPU fault: a GEMM whose producer withholds a
+pipeline stage must give up after its bounded wait, report FP8BS_ETIMEOUT in
+the workspace status word, and leave the context usable."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import gemm as OG
+from oracle import quantize as OQ
+from tests._util import assert_gemm_close, bf16_to_f64, to_dev_bf16, to_f32
+
+pytestmark = pytest.mark.gpu
+fp = pytest.importorskip("fp8_block_scaled_03_gb300")
+
+
+def test_stalled_pipeline_times_out_and_recovers():
+    from fp8_block_scaled_03_gb300 import build
+    build.build()
+    fp.load_library()
+    ws = torch.zeros(fp.load_library().fp8bs_workspace_size(), dtype=torch.uint8, device="cuda")
+    ab = synth.activations((256, 512), seed=1)
+    bb = synth.weights((256, 512), seed=2)
+    qa, sa, _ = fp.fp8_quantize(to_dev_bf16(ab), "mxfp8", ws=ws)
+    qb, sb, _ = fp.fp8_quantize(to_dev_bf16(bb), "mxfp8", ws=ws)
+    assert fp.read_status(ws) == 0
+    rc = fp.test_stalled_gemm(qa, sa, qb, sb, 50_000_000, ws=ws)   # 50 ms bound
+    assert rc == 0
+    assert fp.read_status(ws) == -5                                 # FP8BS_ETIMEOUT
+    fp.clear_status(ws)
+    assert fp.read_status(ws) == 0
+    # the context is still usable and the kernel still correct
+    d = fp.fp8_block_gemm(qa, sa, "mxfp8", qb, sb, "mxfp8", ws=ws)
+    ca, ea = OQ.quantize_mxfp8(to_f32(ab))
+    cb, eb = OQ.quantize_mxfp8(to_f32(bb))
+    assert_gemm_close(bf16_to_f64(d), OG.gemm_bf16(OG.dequant_mxfp8(ca, ea), OG.dequant_mxfp8(cb, eb)))
+    assert fp.read_status(ws) == 0
