@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the sub-benchmarks")
+    ap.add_argument("--kernel", default=None,
+                    choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
+                             "moe_gate_up", "nvfp4"],
+                    help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
 
@@ -176,6 +180,15 @@ class DenseStep:
     def run(self, events=None):
         self.quantize()
         self.gemms(events)
+
+
+def max_over_ranks(torch, dist, value: float, device) -> float:
+    """Largest value over all ranks (the job takes as long as its slowest rank)."""
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def flush_l2(torch, buf):
@@ -368,6 +381,9 @@ def main():
         dist.barrier()
     import fp8_block_scaled_03_gb300 as fp
     fp.load_library()
+    if args.kernel is not None:
+        single_kernel(args, torch, fp, dev)
+        return
     pk = peaks()
     step = DenseStep(torch, fp, dev, seed=1000 + rank)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -397,10 +413,7 @@ def main():
     ms_steps = [a.elapsed_time(b) for a, b in ev]
     ms_total = ms_steps and ev[0][0].elapsed_time(ev[-1][1])
     gemm_ms = [[g[j][0].elapsed_time(g[j][1]) for j in range(3)] for g in gev]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(torch, dist if world > 1 else None, ms_total, dev)
     ms_per_step = ms_total / args.steps
     value = world * STEP_FLOP / (ms_per_step * 1e-3) / 1e12
     assert fp.read_status() == 0, "a device wait timed out during the bench"
@@ -432,6 +445,62 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def single_kernel(args, torch, fp, dev):
+    """One piece of the path, W warm-up + K timed calls, inputs sized as in the
+    step (used for ncu captures of a single kernel)."""
+    act, wt = device_inputs(torch, 7, dev)
+    ws = fp.workspace(dev)
+    name = args.kernel
+    if name in ("fprop", "dgrad", "wgrad"):
+        m, n, k = {"fprop": (M3, I3, H3), "dgrad": (M3, H3, I3), "wgrad": (I3, H3, M3)}[name]
+        a = act((m, k), 0.01, 50.0)
+        b = act((n, k), 0.01, 50.0) if name == "wgrad" else wt((n, k))
+        gb = "1x128" if name == "wgrad" else "128x128"
+        qa, sa, _ = fp.fp8_quantize(a, "1x128", ws=ws)
+        qb, sb, _ = fp.fp8_quantize(b, gb, ws=ws)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp.fp8_block_gemm(qa, sa, "1x128", qb, sb, gb, out=out, ws=ws)  # noqa: E731
+        work = 2 * m * n * k
+    elif name.startswith("quant"):
+        x = act((8192, 4096), 0.001, 100.0)
+        if name == "quant_dual_1x128":
+            bufs = fp.fp8_quantize_transposed(x, "1x128", True, ws=ws)
+            fn = lambda: fp.fp8_quantize_transposed(x, "1x128", True, q_t=bufs[0], scales_t=bufs[1],  # noqa: E731
+                                                    q=bufs[2], scales=bufs[3], ws=ws)
+        else:
+            g = "1x128" if name == "quant_1x128" else "mxfp8"
+            q, s_, _ = fp.fp8_quantize(x, g, ws=ws)
+            fn = lambda: fp.fp8_quantize(x, g, q=q, scales=s_, ws=ws)  # noqa: E731
+        work = 0
+    elif name == "moe_gate_up":
+        import synth
+        _, offsets = synth.moe_routing(16384, 128, 8, seed=0)
+        rows = int(offsets[-1])
+        qa, sa, _ = fp.fp8_quantize(act((rows, 2048), 0.001, 100.0), "mxfp8", ws=ws)
+        qb, sb, _ = fp.fp8_quantize(wt((128 * 1536, 2048)), "mxfp8", ws=ws)
+        off = torch.from_numpy(offsets).to(dev)
+        out = torch.empty((rows, 1536), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp.fp8_grouped_gemm(qa, sa, qb.view(128, 1536, 2048), sb.view(128, 1536, 64), off,  # noqa: E731
+                                         "mxfp8", out=out, ws=ws)
+        work = 2 * rows * 1536 * 2048
+    else:  # nvfp4
+        m, n, k = 16384, 27648, 5120
+        qx, sx, tx = fp.fp8_quantize(act((m, k), 0.0, 1.0), "nvfp4", ws=ws)
+        qw, sw, tw = fp.fp8_quantize(wt((n, k)), "nvfp4", ws=ws)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp.fp8_block_gemm(qx, sx, "nvfp4", qw, sw, "nvfp4", tx, tw, k=k, out=out, ws=ws)  # noqa: E731
+        work = 2 * m * n * k
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ms, _ = time_fn(torch, fn, max(1, args.steps), None, warm=0)
+    res = {"kernel": name, "ms": round(ms, 4)}
+    if work:
+        res["tflops"] = round(work / ms / 1e9, 1)
+    assert fp.read_status() == 0
+    print(json.dumps(res), flush=True)
 
 
 def e2e_bench(torch, fp, dev, step, reps=5):

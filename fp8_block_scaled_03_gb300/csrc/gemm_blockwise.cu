@@ -190,9 +190,9 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
                 sb_e = p.sb + (int64_t)ti.expert * per;
             }
-            float acc[128];
+            uint64_t acc[64];   // FP32 pairs: columns (2j, 2j+1) of this thread's 128-column half
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j) acc[j] = 0ull;
 
             // scale prefetch for kb = 0
             float fa_next = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, 0);
@@ -230,30 +230,47 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
                 if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }   // tcgen05.ld is .sync.aligned
                 tc_fence_after();
-                const float f = fa * fb;
-                const float* buf = (kb & 1) ? sbuf1 : sbuf0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + b * BN + 128 * h + 32 * c, r);
-                    tmem_ld_wait();
+                const uint64_t f2 = f2_pack(fa * fb, fa * fb);
+                const uint64_t fa2 = f2_pack(fa, fa);
+                const float4* buf4 = reinterpret_cast<const float4*>((kb & 1) ? sbuf1 : sbuf0);
+                const uint32_t taddr = tmem + lane_base + b * BN + 128 * h;
+                // Promote one 16-column chunk held in r: acc += partial * scale.
+                auto promote = [&](const uint32_t* r, int c) {
                     if (SB_MODE == 1) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 s4 = reinterpret_cast<const float4*>(buf)[(32 * c + j) >> 2];
-                            acc[32 * c + j + 0] = fmaf(__uint_as_float(r[j + 0]), fa * s4.x, acc[32 * c + j + 0]);
-                            acc[32 * c + j + 1] = fmaf(__uint_as_float(r[j + 1]), fa * s4.y, acc[32 * c + j + 1]);
-                            acc[32 * c + j + 2] = fmaf(__uint_as_float(r[j + 2]), fa * s4.z, acc[32 * c + j + 2]);
-                            acc[32 * c + j + 3] = fmaf(__uint_as_float(r[j + 3]), fa * s4.w, acc[32 * c + j + 3]);
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 s4 = buf4[(16 * c + j) >> 2];
+                            f2_fma(acc[(16 * c + j) / 2], f2_pack_bits(r[j], r[j + 1]), f2_mul(fa2, f2_pack(s4.x, s4.y)));
+                            f2_fma(acc[(16 * c + j) / 2 + 1], f2_pack_bits(r[j + 2], r[j + 3]),
+                                   f2_mul(fa2, f2_pack(s4.z, s4.w)));
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), f, acc[32 * c + j]);
+                        for (int j = 0; j < 8; ++j) f2_fma(acc[8 * c + j], f2_pack_bits(r[2 * j], r[2 * j + 1]), f2);
+                    }
+                };
+                // Two 16-register staging buffers: the TMEM load of chunk c+1 is
+                // in flight while chunk c is promoted.
+                uint32_t ra[16], rb[16];
+                tmem_ld_32x32b_x16(taddr, ra);
+                tmem_ld_wait16(ra);
+#pragma unroll
+                for (int c = 0; c < 8; c += 2) {
+                    tmem_ld_32x32b_x16(taddr + 16 * (c + 1), rb);
+                    promote(ra, c);
+                    tmem_ld_wait16(rb);
+                    if (c + 2 < 8) {
+                        tmem_ld_32x32b_x16(taddr + 16 * (c + 2), ra);
+                        promote(rb, c + 1);
+                        tmem_ld_wait16(ra);
+                    } else {
+                        // every read of this partial buffer is complete: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+                        promote(rb, c + 1);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
             }
 #undef FP8BS_LOAD_B
             if (!ok) break;
@@ -264,10 +281,15 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 for (int j = 0; j < 128; j += 8) {
                     if (col0 + j < p.n) {
                         uint4 o;
-                        __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
-                        __nv_bfloat162 v1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
-                        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
-                        __nv_bfloat162 v3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                        float a0, a1, a2, a3, a4, a5, a6, a7;
+                        f2_unpack(acc[j / 2 + 0], a0, a1);
+                        f2_unpack(acc[j / 2 + 1], a2, a3);
+                        f2_unpack(acc[j / 2 + 2], a4, a5);
+                        f2_unpack(acc[j / 2 + 3], a6, a7);
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(a0, a1);
+                        __nv_bfloat162 v1 = __floats2bfloat162_rn(a2, a3);
+                        __nv_bfloat162 v2 = __floats2bfloat162_rn(a4, a5);
+                        __nv_bfloat162 v3 = __floats2bfloat162_rn(a6, a7);
                         o.x = *reinterpret_cast<uint32_t*>(&v0);
                         o.y = *reinterpret_cast<uint32_t*>(&v1);
                         o.z = *reinterpret_cast<uint32_t*>(&v2);
