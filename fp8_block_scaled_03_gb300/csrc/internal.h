@@ -29,6 +29,8 @@ struct QuantJob {
 };
 int launch_quantize(const QuantJob& j, cudaStream_t s);
 int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
+int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                       float* scale, uint32_t* partials, int nparts, cudaStream_t s);
 
 // ---- GEMMs (gemm_blockwise.cu, gemm_mx.cu)
 struct GemmJob {

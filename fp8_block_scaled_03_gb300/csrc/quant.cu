@@ -462,3 +462,20 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t st) {
 }
 
 }  // namespace fp8bs
+
+namespace fp8bs {
+
+// Per-tensor quantisation with the amax partials in scratch the caller
+// names: pass 1 runs exactly `nparts` CTAs, each writing one partial, and
+// pass 2 reduces those `nparts` partials, so no slot needs clearing first.
+int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                       float* scale, uint32_t* partials, int nparts, cudaStream_t st) {
+    amax_partials_kernel<<<nparts, kThreads, 0, st>>>(x, rows, cols, ldx, partials);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    const int nb = rowwise_blocks(rows, cols, sm_count() * 8);
+    quant_rows_kernel<kGranPT><<<nb, kThreads, 0, st>>>(x, rows, cols, ldx, q, scale, partials, nparts, nullptr);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -194,6 +194,39 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
                             int64_t m, int64_t n, int64_t k, void* d, uint64_t wait_limit_ns,
                             void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
 
+/*
+ * fp8_quantize_per_tensor_noalloc -- fp8_quantize(gran = PER_TENSOR) for
+ * callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is an interface variant, not a different computation.
+ *
+ * The per-tensor scale needs the amax of the whole tensor before any code is
+ * written, and the usual entry point keeps the partial maxima of that
+ * reduction in a caller-provided workspace.  Callers that only receive the
+ * input and output buffers (a framework allocator owns all device memory, a
+ * plugin interface passes tensors but no scratch, a real-time caller forbids
+ * allocation while running) use this entry point instead: the partials live
+ * in a fixed array inside the library (FP8BS_NOALLOC_MAX_PARTIALS 32-bit
+ * words, 16 KB, held on every GPU that loads the library until exit).  It
+ * never calls an allocating routine.
+ *
+ *   x      BF16 [rows, cols], pitch ld_x (as fp8_quantize)
+ *   q      E4M3 codes [rows, cols], written
+ *   scale  device float32[1], receives S = amax / 448 (1 for an all-zero tensor)
+ * Results are identical to fp8_quantize(x, ..., FP8BS_PER_TENSOR, q, scale, ...).
+ *
+ * Limit: rows * ceil(cols / 1024) <= 64 * FP8BS_NOALLOC_MAX_PARTIALS
+ * (262144; e.g. 268,435,456 elements when cols is a multiple of 1024);
+ * larger inputs return FP8BS_EINVAL and launch nothing.  Other checks and
+ * codes as fp8_quantize.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call uses the same array: calls that
+ * overlap on the GPU (different streams without ordering) race and give
+ * wrong scales.
+ */
+#define FP8BS_NOALLOC_MAX_PARTIALS 4096
+int fp8_quantize_per_tensor_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                                    float* scale, fp8bs_stream_t stream);
+
 /* Bytes of workspace every entry point accepts (FP8BS_WORKSPACE_BYTES). */
 size_t fp8bs_workspace_size(void);
 
