@@ -135,16 +135,21 @@ def device_inputs(torch, seed: int, dev):
 
 
 class DenseStep:
-    """Buffers and launches of one fwd+bwd step of the blockwise FP8 linear."""
+    """Buffers and launches of one fwd+bwd step of the blockwise FP8 linear.
 
-    def __init__(self, torch, fp, dev, seed):
+    recipe "fp32": 1x128 / 128x128 FP32 scales, promoted in the GEMM epilogue;
+    recipe "pow2": the same blocks with power-of-two (UE8M0) scales applied by
+    the tensor core's block-scale path."""
+
+    def __init__(self, torch, fp, dev, seed, recipe="fp32"):
+        self.g_tok, self.g_blk = ("1x128", "128x128") if recipe == "fp32" else ("1x128_pow2", "128x128_pow2")
         act, wt = device_inputs(torch, seed, dev)
         self.torch, self.fp = torch, fp
         self.x = act((M3, H3), 0.01, 50.0)
         self.w = wt((I3, H3))
         self.dy = act((M3, I3), 0.01, 50.0)
         e = lambda *s, dt=torch.uint8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
-        f32 = torch.float32
+        f32 = torch.float32 if recipe == "fp32" else torch.uint8
         self.qx, self.sx, self.qxt, self.sxt = e(M3, H3), e(M3, H3 // 128, dt=f32), e(H3, M3), e(H3, M3 // 128, dt=f32)
         self.qw, self.sw = e(I3, H3), e(I3 // 128, H3 // 128, dt=f32)
         self.qwt, self.swt = e(H3, I3), e(H3 // 128, I3 // 128, dt=f32)
@@ -158,18 +163,19 @@ class DenseStep:
 
     def quantize(self):
         fp = self.fp
-        fp.fp8_quantize_transposed(self.x, "1x128", True, q_t=self.qxt, scales_t=self.sxt, q=self.qx,
+        fp.fp8_quantize_transposed(self.x, self.g_tok, True, q_t=self.qxt, scales_t=self.sxt, q=self.qx,
                                    scales=self.sx, ws=self.ws)
-        fp.fp8_quantize_transposed(self.w, "128x128", True, q_t=self.qwt, scales_t=self.swt, q=self.qw,
+        fp.fp8_quantize_transposed(self.w, self.g_blk, True, q_t=self.qwt, scales_t=self.swt, q=self.qw,
                                    scales=self.sw, ws=self.ws)
-        fp.fp8_quantize_transposed(self.dy, "1x128", True, q_t=self.qdyt, scales_t=self.sdyt, q=self.qdy,
+        fp.fp8_quantize_transposed(self.dy, self.g_tok, True, q_t=self.qdyt, scales_t=self.sdyt, q=self.qdy,
                                    scales=self.sdy, ws=self.ws)
 
     def gemms(self, events=None):
         fp = self.fp
-        ops = ((self.qx, self.sx, "1x128", self.qw, self.sw, "128x128", self.y),
-               (self.qdy, self.sdy, "1x128", self.qwt, self.swt, "128x128", self.dx),
-               (self.qdyt, self.sdyt, "1x128", self.qxt, self.sxt, "1x128", self.dw))
+        t, b = self.g_tok, self.g_blk
+        ops = ((self.qx, self.sx, t, self.qw, self.sw, b, self.y),
+               (self.qdy, self.sdy, t, self.qwt, self.swt, b, self.dx),
+               (self.qdyt, self.sdyt, t, self.qxt, self.sxt, t, self.dw))
         for i, (a, sa, ga, b, sb, gb, out) in enumerate(ops):
             if events is not None:
                 events[i][0].record()
@@ -436,6 +442,7 @@ def main():
             "gpu_launches": step.launches_per_step * args.steps, "clocks": clk.summary()}
 
     if rank == 0 and not args.no_extras:
+        line["dense_pow2"] = pow2_step_bench(torch, fp, dev, args, pk)
         line["quantize"] = quantize_sweep(torch, fp, dev, pk, flush)
         line["moe_mxfp8"] = moe_bench(torch, fp, dev, pk, flush)
         line["nvfp4"] = nvfp4_bench(torch, fp, dev, pk, flush)
@@ -501,6 +508,34 @@ def single_kernel(args, torch, fp, dev):
         res["tflops"] = round(work / ms / 1e9, 1)
     assert fp.read_status() == 0
     print(json.dumps(res), flush=True)
+
+
+def pow2_step_bench(torch, fp, dev, args, pk):
+    """The same fwd+bwd step with power-of-two block scales (tensor-core
+    block-scale path instead of FP32 promotion)."""
+    step = DenseStep(torch, fp, dev, seed=2000, recipe="pow2")
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    gev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, args.steps)
+    gms = [0.0, 0.0, 0.0]
+    s0.record()
+    for _ in range(n):
+        step.run(gev)
+        torch.cuda.synchronize()
+        for j in range(3):
+            gms[j] += gev[j][0].elapsed_time(gev[j][1])
+    s1.record()
+    s1.synchronize()
+    per_step = s0.elapsed_time(s1) / n
+    peak = pk["bf16_tflops_sustained"] * FP8_PER_BF16
+    avg = statistics.mean(g / n for g in gms)
+    t = GEMM_FLOP / avg / 1e9
+    return {"tflops_step": round(STEP_FLOP / per_step / 1e9, 1), "ms_per_step": round(per_step, 4),
+            "gemm_tflops": round(t, 1), "gemm_frac": round(t / peak, 3),
+            "per_gemm_ms": [round(g / n, 3) for g in gms]}
 
 
 def e2e_bench(torch, fp, dev, step, reps=5):

@@ -12,7 +12,8 @@ Entry points (same names as the C ABI):
     fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16)
     fp8_grouped_gemm(a, sa, b, sb, offsets, gran)                      -> d (bf16)
 
-Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4".
+Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4", and the
+block-wise recipe with power-of-two scales "1x128_pow2", "128x128_pow2".
 """
 from __future__ import annotations
 
@@ -25,7 +26,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfp8bs.so")
 
-GRAN = {"per_tensor": 0, "1x128": 1, "128x128": 2, "mxfp8": 3, "nvfp4": 4}
+GRAN = {"per_tensor": 0, "1x128": 1, "128x128": 2, "mxfp8": 3, "nvfp4": 4, "1x128_pow2": 5, "128x128_pow2": 6}
 FLAG_GIVEN_TENSOR_SCALE = 1
 STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNSUPPORTED",
           -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE"}
@@ -135,6 +136,10 @@ def scale_shape(gran, rows: int, cols: int):
         return (_cdiv(rows, 128), _cdiv(cols, 128)), torch.float32
     if g == 3:
         return (rows, _cdiv(cols, 32)), torch.uint8
+    if g == 5:
+        return (rows, _cdiv(cols, 128)), torch.uint8
+    if g == 6:
+        return (_cdiv(rows, 128), _cdiv(cols, 128)), torch.uint8
     return (rows, cols // 16), torch.uint8
 
 

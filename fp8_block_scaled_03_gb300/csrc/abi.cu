@@ -38,7 +38,12 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 // Scale pointers: FP32 scales and UE8M0 words are read 4 bytes at a time,
 // NVFP4 block scales 16 bytes at a time.
-inline bool scales_aligned(const void* s, int gran) { return gran == 4 ? aligned16(s) : aligned4(s); }
+inline bool scales_aligned(const void* s, int gran) {
+    if (gran == FP8BS_NVFP4_1x16) return aligned16(s);
+    if (gran == FP8BS_TOKEN_1x128_POW2 || gran == FP8BS_BLOCK_128x128_POW2) return true;   // read bytewise
+    return aligned4(s);
+}
+inline bool is_pow2_block(int gran) { return gran == FP8BS_TOKEN_1x128_POW2 || gran == FP8BS_BLOCK_128x128_POW2; }
 
 // Launchers return 0, a cudaError_t (> 0) or a negative fp8bs_status.
 inline int cuda_status(int err) {
@@ -55,7 +60,7 @@ inline int cuda_status(int err) {
 // pointer is looked at (allocators may hand out NULL for empty tensors).
 int check_quant_common(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran) {
     if (rows < 0 || cols < 0) return FP8BS_EINVAL;
-    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_BLOCK_128x128_POW2) return FP8BS_EINVAL;
     if (cols % 8 != 0 || ld_x < cols || ld_x % 8 != 0) return FP8BS_EINVAL;
     if (gran == FP8BS_NVFP4_1x16 && cols % 16 != 0) return FP8BS_EINVAL;
     if (ceil_div(rows, 128) > 65535 || ceil_div(cols, 128) > 0x7FFFFFFF) return FP8BS_EINVAL;
@@ -125,7 +130,8 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0) return FP8BS_EINVAL;
-    if (a_gran < 0 || a_gran > FP8BS_NVFP4_1x16 || b_gran < 0 || b_gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    if (a_gran < 0 || a_gran > FP8BS_BLOCK_128x128_POW2 || b_gran < 0 || b_gran > FP8BS_BLOCK_128x128_POW2)
+        return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
     if (!scales_aligned(a_scales, a_gran) || !scales_aligned(b_scales, b_gran)) return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
@@ -143,6 +149,10 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
         return cuda_status(launch_gemm_blockwise(j, st));
     }
     if (a_gran == FP8BS_MXFP8_1x32 && b_gran == FP8BS_MXFP8_1x32) {
+        if (k % 128 != 0) return FP8BS_EINVAL;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
+    if (is_pow2_block(a_gran) && is_pow2_block(b_gran)) {
         if (k % 128 != 0) return FP8BS_EINVAL;
         return cuda_status(launch_gemm_mx(j, st));
     }
@@ -182,7 +192,11 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
         j.a_gran = FP8BS_TOKEN_1x128; j.b_gran = FP8BS_BLOCK_128x128;
         return cuda_status(launch_gemm_blockwise(j, st));
     }
-    if (gran < 0 || gran > FP8BS_NVFP4_1x16) return FP8BS_EINVAL;
+    if (gran == FP8BS_TOKEN_1x128_POW2) {
+        j.a_gran = FP8BS_TOKEN_1x128_POW2; j.b_gran = FP8BS_BLOCK_128x128_POW2;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
+    if (gran < 0 || gran > FP8BS_BLOCK_128x128_POW2) return FP8BS_EINVAL;
     return FP8BS_EUNSUPPORTED;
 }
 

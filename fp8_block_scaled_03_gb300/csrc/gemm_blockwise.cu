@@ -194,37 +194,48 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0ull;
 
-            // scale prefetch for kb = 0
-            float fa_next = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, 0);
-            float fb_next = 0.0f;
-            float4 fbv_next = make_float4(0.f, 0.f, 0.f, 0.f);
-#define FP8BS_LOAD_B(KB)                                                                              \
+            // Scales run PD K blocks ahead of their use in a register ring, so
+            // the L2 latency of these small scattered loads stays off the
+            // per-K-block critical path.
+            constexpr int PD = 4;
+            float fa_r[PD], fb_r[PD];
+            float4 fv_r[PD];
+#define FP8BS_LOAD_SCALES(D, KB)                                                                      \
     do {                                                                                              \
+        fa_r[D] = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, (KB));                                 \
         if (SB_MODE == 0) {                                                                           \
-            fb_next = __ldg(sb_e);                                                                    \
+            fb_r[D] = __ldg(sb_e);                                                                    \
         } else if (SB_MODE == 2) {                                                                    \
-            fb_next = (col0 < p.n) ? __ldg(sb_e + (col0 >> 7) * nkb + (KB)) : 0.0f;                   \
+            fb_r[D] = (col0 < p.n) ? __ldg(sb_e + (col0 >> 7) * nkb + (KB)) : 0.0f;                   \
         } else {                                                                                      \
             const int64_t c_ = col0 + 4 * lane;                                                       \
-            fbv_next.x = (c_ + 0 < p.n) ? __ldg(sb_e + (c_ + 0) * nkb + (KB)) : 0.0f;                 \
-            fbv_next.y = (c_ + 1 < p.n) ? __ldg(sb_e + (c_ + 1) * nkb + (KB)) : 0.0f;                 \
-            fbv_next.z = (c_ + 2 < p.n) ? __ldg(sb_e + (c_ + 2) * nkb + (KB)) : 0.0f;                 \
-            fbv_next.w = (c_ + 3 < p.n) ? __ldg(sb_e + (c_ + 3) * nkb + (KB)) : 0.0f;                 \
+            fv_r[D].x = (c_ + 0 < p.n) ? __ldg(sb_e + (c_ + 0) * nkb + (KB)) : 0.0f;                  \
+            fv_r[D].y = (c_ + 1 < p.n) ? __ldg(sb_e + (c_ + 1) * nkb + (KB)) : 0.0f;                  \
+            fv_r[D].z = (c_ + 2 < p.n) ? __ldg(sb_e + (c_ + 2) * nkb + (KB)) : 0.0f;                  \
+            fv_r[D].w = (c_ + 3 < p.n) ? __ldg(sb_e + (c_ + 3) * nkb + (KB)) : 0.0f;                  \
         }                                                                                             \
     } while (0)
-            FP8BS_LOAD_B(0);
+#pragma unroll
+            for (int d = 0; d < PD; ++d) {
+                fa_r[d] = fb_r[d] = 0.0f;
+                fv_r[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (d < nkb) FP8BS_LOAD_SCALES(d, d);
+            }
 
             for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
-                const float fa = fa_next;
-                const float fb = fb_next;
+                const float fa = fa_r[0];
+                const float fb = fb_r[0];
                 if (SB_MODE == 1) {
                     float* buf = (kb & 1) ? sbuf1 : sbuf0;
-                    reinterpret_cast<float4*>(buf)[lane] = fbv_next;
+                    reinterpret_cast<float4*>(buf)[lane] = fv_r[0];
                 }
-                if (kb + 1 < nkb) {
-                    fa_next = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, kb + 1);
-                    FP8BS_LOAD_B(kb + 1);
+#pragma unroll
+                for (int d = 0; d + 1 < PD; ++d) {
+                    fa_r[d] = fa_r[d + 1];
+                    fb_r[d] = fb_r[d + 1];
+                    fv_r[d] = fv_r[d + 1];
                 }
+                if (kb + PD < nkb) FP8BS_LOAD_SCALES(PD - 1, kb + PD);
                 __syncwarp();
                 const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
                 const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
@@ -272,7 +283,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     }
                 }
             }
-#undef FP8BS_LOAD_B
+#undef FP8BS_LOAD_SCALES
             if (!ok) break;
             // BF16 store of this thread's row: 128 columns = 16 x 16 bytes
             if (row < ti.row_end) {

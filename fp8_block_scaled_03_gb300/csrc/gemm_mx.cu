@@ -5,7 +5,9 @@
 //
 // "Low Precision RL", table "Choose a precision": MXFP8 1x32 with UE8M0
 // scales and NVFP4 1x16 with two-level (E4M3 + FP32) scales, both Blackwell
-// formats; section "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend is
+// formats; section "2. Unified block-wise FP8": on Blackwell the block-wise
+// recipe runs on this path with power-of-two scales (one UE8M0 byte per
+// 128-wide K block, replicated over its four 32-wide sub-blocks); section "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend is
 // chosen separately from the dense one.  Here both are one kernel: a dense
 // GEMM is the grouped GEMM with one group.
 //
@@ -39,7 +41,7 @@ constexpr int A_BYTES = BM * BKB, B_BYTES = BN * BKB;
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 
-enum { kMx = 0, kNv = 1 };
+enum { kMx = 0, kNv = 1, kP2 = 2 };   // MXFP8, NVFP4, block-wise with power-of-two scales
 
 template <int KIND> struct Cfg;
 template <> struct Cfg<kMx> {
@@ -47,6 +49,12 @@ template <> struct Cfg<kMx> {
     static constexpr int K_PER_STAGE = 128;           // elements
     static constexpr int A_ATOMS = 1, B_ATOMS = 2;    // 512-byte scale atoms per stage
     static constexpr int SF_BYTES_PER_ROW = 4;        // scale bytes per row per stage
+};
+template <> struct Cfg<kP2> {                     // one UE8M0 byte per 128-wide K block,
+    static constexpr int STAGES = 4;              // replicated over its four 32-wide sub-blocks
+    static constexpr int K_PER_STAGE = 128;
+    static constexpr int A_ATOMS = 1, B_ATOMS = 2;
+    static constexpr int SF_BYTES_PER_ROW = 4;
 };
 template <> struct Cfg<kNv> {
     static constexpr int STAGES = 3;
@@ -97,10 +105,28 @@ struct ScaleRegs {
     uint32_t b[8][W];
 };
 
-template <int KIND>
+template <int KIND, int SA, int SB>
 __device__ __forceinline__ void load_scales(ScaleRegs<KIND>& r, const Params& p, const TileInfo& ti, int64_t kb,
                                             int lane, int64_t sf_pitch) {
     constexpr int W = ScaleRegs<KIND>::W;
+    if constexpr (KIND == kP2) {
+        // SA / SB: 1 = one byte per row, 2 = one byte per 128-row block (rows of
+        // the operand's own scale grid; B grids stacked per expert).
+#pragma unroll
+        for (int r1 = 0; r1 < 4; ++r1) {
+            const int64_t row = ti.row0 + lane + 32 * r1;
+            const int64_t idx = (SA == 1 ? row : (row >> 7)) * sf_pitch + kb;
+            r.a[r1][0] = row < p.m ? (uint32_t)__ldg(p.sa + idx) * 0x01010101u : 0u;
+        }
+        const int64_t nb_e = (p.n + 127) / 128;
+#pragma unroll
+        for (int r1 = 0; r1 < 8; ++r1) {
+            const int64_t n = ti.n0 + lane + 32 * r1;
+            const int64_t srow = (SB == 1) ? (int64_t)ti.expert * p.n + n : (int64_t)ti.expert * nb_e + (n >> 7);
+            r.b[r1][0] = n < p.n ? (uint32_t)__ldg(p.sb + srow * sf_pitch + kb) * 0x01010101u : 0u;
+        }
+        return;
+    }
     const int64_t koff = kb * Cfg<KIND>::SF_BYTES_PER_ROW;
 #pragma unroll
     for (int r1 = 0; r1 < 4; ++r1) {
@@ -150,20 +176,20 @@ __device__ __forceinline__ void store_scales(const ScaleRegs<KIND>& r, uint8_t* 
     }
 }
 
-template <int KIND>
+template <int KIND, int SA, int SB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
     constexpr int STAGES = Cfg<KIND>::STAGES;
-    constexpr size_t SB = stage_bytes<KIND>();
+    constexpr size_t STAGE_B = stage_bytes<KIND>();
     constexpr uint32_t SF_COLS = 4 * (Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS);  // TMEM columns per stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared<STAGES>* sh = reinterpret_cast<Shared<STAGES>*>(stages + STAGES * SB);
+    Shared<STAGES>* sh = reinterpret_cast<Shared<STAGES>*>(stages + STAGES * STAGE_B);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = p.k / Cfg<KIND>::K_PER_STAGE;
     const int64_t n_tiles = (p.n + BN - 1) / BN;
-    const int64_t sf_pitch = p.k / (KIND == kMx ? 32 : 16);
+    const int64_t sf_pitch = p.k / (KIND == kMx ? 32 : (KIND == kNv ? 16 : 128));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -204,7 +230,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                     if (p.stall_stage0 && it == 0) continue;   // test hook: never fill stage 0
                     const uint32_t fb = smem_u32(&sh->full[s]);
-                    uint8_t* st = stages + s * SB;
+                    uint8_t* st = stages + s * STAGE_B;
                     mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
                     tma_load_2d(smem_u32(st), &tm_a, fb, (int32_t)(kb * BKB), (int32_t)ti.row0);
                     tma_load_2d(smem_u32(st + A_BYTES), &tm_b, fb, (int32_t)(kb * BKB), brow);
@@ -229,7 +255,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort, p.status, p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
-                    uint8_t* st = stages + s * SB;
+                    uint8_t* st = stages + s * STAGE_B;
                     const uint32_t a_addr = smem_u32(st);
                     const uint64_t adesc = kmajor_sw128_desc(a_addr);
                     const uint64_t bdesc = kmajor_sw128_desc(a_addr + A_BYTES);
@@ -245,7 +271,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (KIND == kMx) {
+                        if constexpr (KIND != kNv) {
                             const uint32_t idesc = idesc_block_scaled(BM, BN, 0, 0, 1, kk, kk);
                             mma_mxf8(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa, sfb, acc);
                         } else {
@@ -264,21 +290,52 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale loader
+        // A load cursor runs SF_PD stages ahead of the store cursor; the
+        // loaded words wait in a register ring (slot = stage mod SF_PD, the
+        // loop unrolled so every slot index is a constant), which keeps the
+        // L2 latency of the scale loads off the per-stage path.
+        constexpr int SF_PD = (KIND == kNv) ? 2 : 4;   // NVFP4 stages carry 4x the scale words
+        ScaleRegs<KIND> ring[SF_PD];
+        int64_t lt = blockIdx.x, lkb = 0;                 // load cursor
+        TileInfo lti{};
+        if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+#pragma unroll
+        for (int d = 0; d < SF_PD; ++d) {
+            if (lt < total) {
+                load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
+                if (++lkb == nkb) {
+                    lkb = 0;
+                    lt += gridDim.x;
+                    if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+                }
+            }
+        }
+        int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
-            ScaleRegs<KIND> cur, nxt;
-            load_scales<KIND>(cur, p, ti, 0, lane, sf_pitch);
-            for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
-                if (kb + 1 < nkb) load_scales<KIND>(nxt, p, ti, kb + 1, lane, sf_pitch);
+        while (st_t < total && ok) {
+#pragma unroll
+            for (int d = 0; d < SF_PD; ++d) {
+                if (st_t >= total || !ok) break;
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                 if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
-                store_scales<KIND>(cur, stages + s * SB + A_BYTES + B_BYTES, lane);
+                store_scales<KIND>(ring[d], stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
-                cur = nxt;
+                ++it;
+                if (lt < total) {
+                    load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
+                    if (++lkb == nkb) {
+                        lkb = 0;
+                        lt += gridDim.x;
+                        if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+                    }
+                }
+                if (++st_kb == nkb) {
+                    st_kb = 0;
+                    st_t += gridDim.x;
+                }
             }
         }
     } else if (warp >= 4) {
@@ -330,18 +387,18 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 }
 
-template <int KIND>
+template <int KIND, int SA = 0, int SB = 0>
 int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t st) {
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<KIND, SA, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem_bytes<KIND>());
         if (e != cudaSuccess) return (int)e;
         attr_set[dev] = true;
     }
-    gemm_mx_kernel<KIND><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, p);
+    gemm_mx_kernel<KIND, SA, SB><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, p);
     return (int)cudaGetLastError();
 }
 
@@ -370,7 +427,14 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);
-    return nv ? launch_kind<kNv>(ta, tb, p, grid, st) : launch_kind<kMx>(ta, tb, p, grid, st);
+    if (nv) return launch_kind<kNv>(ta, tb, p, grid, st);
+    if (j.a_gran == 3) return launch_kind<kMx>(ta, tb, p, grid, st);
+    // power-of-two block-wise: 5 = one byte per row and 128 K, 6 = per 128x128 block
+    const int sa = j.a_gran == 5 ? 1 : 2, sb = j.b_gran == 5 ? 1 : 2;
+    if (sa == 1 && sb == 2) return launch_kind<kP2, 1, 2>(ta, tb, p, grid, st);
+    if (sa == 1 && sb == 1) return launch_kind<kP2, 1, 1>(ta, tb, p, grid, st);
+    if (sa == 2 && sb == 2) return launch_kind<kP2, 2, 2>(ta, tb, p, grid, st);
+    return launch_kind<kP2, 2, 1>(ta, tb, p, grid, st);
 }
 
 }  // namespace fp8bs

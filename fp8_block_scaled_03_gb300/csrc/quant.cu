@@ -18,7 +18,11 @@
 
 namespace fp8bs {
 
-enum { kGranPT = 0, kGranTok = 1, kGranBlk = 2, kGranMx = 3, kGranNv = 4 };
+enum { kGranPT = 0, kGranTok = 1, kGranBlk = 2, kGranMx = 3, kGranNv = 4, kGranTokP2 = 5, kGranBlkP2 = 6 };
+
+// Granularities whose scale is a power of two (UE8M0 byte): the division by
+// the scale is an exact multiplication by 2^-e.
+template <int G> constexpr bool kPow2 = (G == kGranMx || G == kGranTokP2 || G == kGranBlkP2);
 
 constexpr int kSeg = 1024;       // columns per row-wise warp task
 constexpr int kThreads = 256;
@@ -143,6 +147,11 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
                 const int e = mx_exponent_from_amax_bits(m << 16);
                 o = cast8_mul(f, exp2_neg(e));
                 if (ok && (lane & 3) == 0) static_cast<uint8_t*>(sout)[r * ng + (c >> 5)] = (uint8_t)(e + 127);
+            } else if constexpr (GRAN == kGranTokP2) {
+                const uint32_t m = warp_max_u32(absmax_v4(v[j]), 16);
+                const int e = mx_exponent_from_amax_bits(m << 16);
+                o = cast8_mul(f, exp2_neg(e));
+                if (ok && (lane & 15) == 0) static_cast<uint8_t*>(sout)[r * ng + (c >> 7)] = (uint8_t)(e + 127);
             } else {
                 o = cast8_div(f, s_uniform);
             }
@@ -204,9 +213,10 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
 }
 
 // ---------------------------------------------------------------- 128x128 (row-wise)
+template <bool P2>
 __global__ void __launch_bounds__(kThreads)
 quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-                   uint8_t* __restrict__ q, float* __restrict__ s) {
+                   uint8_t* __restrict__ q, void* __restrict__ s) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
     const int64_t c = c0 + (lane & 15) * 8;
@@ -220,37 +230,53 @@ quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) m = max(m, absmax_v4(v[i]));
-    const float sc = fp32_scale_from_amax(amax_bits_to_f32(block_max_u32(m)));
-    if (threadIdx.x == 0) s[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = sc;
+    const uint32_t bm = block_max_u32(m);
+    float sc = 1.0f;
+    if constexpr (P2) {
+        const int e = mx_exponent_from_amax_bits(bm << 16);
+        sc = exp2_neg(e);
+        if (threadIdx.x == 0) static_cast<uint8_t*>(s)[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = (uint8_t)(e + 127);
+    } else {
+        sc = fp32_scale_from_amax(amax_bits_to_f32(bm));
+        if (threadIdx.x == 0) static_cast<float*>(s)[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = sc;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t r = r0 + 16 * w + 2 * i + (lane >> 4);
         if (cok && r < rows) {
             float f[8];
             unpack8(v[i], f);
-            *reinterpret_cast<uint2*>(q + r * cols + c) = cast8_div(f, sc);
+            *reinterpret_cast<uint2*>(q + r * cols + c) = P2 ? cast8_mul(f, sc) : cast8_div(f, sc);
         }
     }
 }
 
 // ---------------------------------------------------------------- transposed (+ optional row-wise)
-// CTA tile: 128 rows x 128 columns of X; warp w owns rows 16w..16w+15, lane l
-// owns columns 4l..4l+3.  Codes of X^T go out as 16-byte runs (16 rows of one
-// column); the optional row-wise codes as 4-byte runs.
+// CTA tile: 128 rows x 128 columns of X, 512 threads.  Warp w owns rows
+// 8w..8w+7, lane l owns columns 4l..4l+3 (8-byte loads, 256 bytes per warp
+// and row).  Column amaxes are combined through shared memory.  The codes
+// of X^T are staged in shared memory as a [column][row] byte tile (row pitch
+// 136 bytes, so the 8-byte stores of one warp spread over all banks) and
+// leave as whole 128-byte rows of X^T; the optional row-wise codes of X
+// leave straight from registers as 4-byte runs (128 bytes per warp and row).
+constexpr int kTileThreads = 512;
+constexpr int kTPitch = 136;
+
 template <int GRAN, bool DUAL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kTileThreads, 2)
 quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                     uint8_t* __restrict__ qt, void* __restrict__ st,
                     uint8_t* __restrict__ q, void* __restrict__ s,
                     const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
-    __shared__ uint32_t red[8][128];
+    __shared__ uint32_t red[16][128];
+    __shared__ __align__(16) uint8_t tq[128 * kTPitch];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t rt = blockIdx.y, ct = blockIdx.x;
     const int64_t r0 = rt * 128, c0 = ct * 128;
     const int64_t cc = c0 + lane * 4;
     const bool cok = cc < cols;
-    const int64_t rw = r0 + 16 * w;          // first row of this warp
-    const bool wok = rw < rows;              // rows % 16 == 0: 16 rows all valid or all not
+    const int64_t rw = r0 + 8 * w;           // first row of this warp
+    const bool wok = rw < rows;              // rows % 16 == 0: 8 rows all valid or all not
 
     float s_uniform = 1.0f;
     if constexpr (GRAN == kGranPT) {
@@ -265,69 +291,90 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
         }
     }
 
-    uint2 v[16];
+    uint2 v[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 8; ++i)
         v[i] = (cok && wok) ? ldg_v2(x + (rw + i) * ldx + cc) : make_uint2(0, 0);
 
     uint32_t cm[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
         cm[0] = max(cm[0], v[i].x & 0x7FFFu);
         cm[1] = max(cm[1], (v[i].x >> 16) & 0x7FFFu);
         cm[2] = max(cm[2], v[i].y & 0x7FFFu);
         cm[3] = max(cm[3], (v[i].y >> 16) & 0x7FFFu);
     }
 
-    float col_s[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // divisor (FP32 grans) or multiplier (MX)
+    float col_s[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // divisor (FP32 grans) or multiplier (power-of-two grans)
     int col_e[4] = {0, 0, 0, 0};
     float s_blk = 1.0f;
-    if constexpr (GRAN == kGranTok || GRAN == kGranMx) {
+    int e_blk = 0;
+    if constexpr (GRAN == kGranTok || GRAN == kGranMx || GRAN == kGranTokP2) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) red[w][lane * 4 + j] = cm[j];
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t m = 0;
-            if constexpr (GRAN == kGranTok) {
+            if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m = max(m, red[k][lane * 4 + j]);
-                col_s[j] = fp32_scale_from_amax(amax_bits_to_f32(m));
+                for (int k = 0; k < 16; ++k) m = max(m, red[k][lane * 4 + j]);
+                if constexpr (GRAN == kGranTok) {
+                    col_s[j] = fp32_scale_from_amax(amax_bits_to_f32(m));
+                } else {
+                    col_e[j] = mx_exponent_from_amax_bits(m << 16);
+                    col_s[j] = exp2_neg(col_e[j]);
+                }
             } else {
-                const int g = w & ~1;
-                m = max(red[g][lane * 4 + j], red[g + 1][lane * 4 + j]);
+                const int g = w & ~3;            // 32 rows = 4 warps
+#pragma unroll
+                for (int k = 0; k < 4; ++k) m = max(m, red[g + k][lane * 4 + j]);
                 col_e[j] = mx_exponent_from_amax_bits(m << 16);
                 col_s[j] = exp2_neg(col_e[j]);
             }
         }
-    } else if constexpr (GRAN == kGranBlk) {
-        s_blk = fp32_scale_from_amax(amax_bits_to_f32(block_max_u32(max(max(cm[0], cm[1]), max(cm[2], cm[3])))));
+    } else if constexpr (GRAN == kGranBlk || GRAN == kGranBlkP2) {
+        const uint32_t bm = block_max_u32(max(max(cm[0], cm[1]), max(cm[2], cm[3])));
+        if constexpr (GRAN == kGranBlk) {
+            s_blk = fp32_scale_from_amax(amax_bits_to_f32(bm));
+        } else {
+            e_blk = mx_exponent_from_amax_bits(bm << 16);
+            s_blk = exp2_neg(e_blk);
+        }
     }
 
-    // ---- transposed codes: column cc + j, rows rw .. rw+15
-    if (cok && wok) {
+    // ---- transposed codes: column cc + j, rows rw .. rw+7 -> shared tile
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float f[16];
+    for (int j = 0; j < 4; ++j) {
+        float f[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t word = (j < 2) ? v[i].x : v[i].y;
-                f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
-            }
-            float d = (GRAN == kGranPT) ? s_uniform : (GRAN == kGranBlk ? s_blk : col_s[j]);
-            uint4 o;
-            if constexpr (GRAN == kGranMx) {
-                o.x = e4m3x4(__fmul_rn(f[0], d), __fmul_rn(f[1], d), __fmul_rn(f[2], d), __fmul_rn(f[3], d));
-                o.y = e4m3x4(__fmul_rn(f[4], d), __fmul_rn(f[5], d), __fmul_rn(f[6], d), __fmul_rn(f[7], d));
-                o.z = e4m3x4(__fmul_rn(f[8], d), __fmul_rn(f[9], d), __fmul_rn(f[10], d), __fmul_rn(f[11], d));
-                o.w = e4m3x4(__fmul_rn(f[12], d), __fmul_rn(f[13], d), __fmul_rn(f[14], d), __fmul_rn(f[15], d));
-            } else {
-                o.x = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
-                o.y = e4m3x4(__fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
-                o.z = e4m3x4(__fdiv_rn(f[8], d), __fdiv_rn(f[9], d), __fdiv_rn(f[10], d), __fdiv_rn(f[11], d));
-                o.w = e4m3x4(__fdiv_rn(f[12], d), __fdiv_rn(f[13], d), __fdiv_rn(f[14], d), __fdiv_rn(f[15], d));
-            }
-            *reinterpret_cast<uint4*>(qt + (cc + j) * rows + rw) = o;
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t word = (j < 2) ? v[i].x : v[i].y;
+            f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+        }
+        const float d = (GRAN == kGranPT) ? s_uniform : ((GRAN == kGranBlk || GRAN == kGranBlkP2) ? s_blk : col_s[j]);
+        uint2 o;
+        if constexpr (kPow2<GRAN>) {
+            o.x = e4m3x4(__fmul_rn(f[0], d), __fmul_rn(f[1], d), __fmul_rn(f[2], d), __fmul_rn(f[3], d));
+            o.y = e4m3x4(__fmul_rn(f[4], d), __fmul_rn(f[5], d), __fmul_rn(f[6], d), __fmul_rn(f[7], d));
+        } else {
+            o.x = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
+            o.y = e4m3x4(__fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
+        }
+        *reinterpret_cast<uint2*>(tq + (lane * 4 + j) * kTPitch + 8 * w) = o;
+    }
+    __syncthreads();
+    // ---- whole rows of X^T: 128 columns x 128 bytes, 16 bytes per thread and pass
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int t = threadIdx.x + pass * kTileThreads;
+        const int qc = t >> 3, k = t & 7;    // column of X (row of X^T), 16-byte chunk
+        const int64_t c = c0 + qc;
+        if (c < cols && r0 + 16 * k < rows) {
+            const uint8_t* src = tq + qc * kTPitch + 16 * k;
+            const uint2 lo = *reinterpret_cast<const uint2*>(src);
+            const uint2 hi = *reinterpret_cast<const uint2*>(src + 8);
+            *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) = make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
     }
     // ---- scales of X^T ([cols, *] grid)
@@ -338,20 +385,28 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
             for (int j = 0; j < 4; ++j) static_cast<float*>(st)[(cc + j) * nrb + rt] = col_s[j];
         }
     } else if constexpr (GRAN == kGranMx) {
-        if ((w & 1) == 0 && cok && wok) {
+        if ((w & 3) == 0 && cok && wok) {
             const int64_t nrb = ceil_div(rows, 32);
 #pragma unroll
             for (int j = 0; j < 4; ++j) static_cast<uint8_t*>(st)[(cc + j) * nrb + (rw >> 5)] = (uint8_t)(col_e[j] + 127);
         }
+    } else if constexpr (GRAN == kGranTokP2) {
+        if (w == 0 && cok) {
+            const int64_t nrb = ceil_div(rows, 128);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) static_cast<uint8_t*>(st)[(cc + j) * nrb + rt] = (uint8_t)(col_e[j] + 127);
+        }
     } else if constexpr (GRAN == kGranBlk) {
         if (threadIdx.x == 0) static_cast<float*>(st)[ct * gridDim.y + rt] = s_blk;
+    } else if constexpr (GRAN == kGranBlkP2) {
+        if (threadIdx.x == 0) static_cast<uint8_t*>(st)[ct * gridDim.y + rt] = (uint8_t)(e_blk + 127);
     }
 
     // ---- row-wise codes of X from the same registers
     if constexpr (DUAL) {
         const int64_t ncb = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             float f[4] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y)};
             const uint32_t m4 = max(bf16x2_absmax_bits(v[i].x), bf16x2_absmax_bits(v[i].y));
             uint32_t o;
@@ -364,6 +419,13 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
                 const float mm = exp2_neg(e);
                 o = e4m3x4(__fmul_rn(f[0], mm), __fmul_rn(f[1], mm), __fmul_rn(f[2], mm), __fmul_rn(f[3], mm));
                 if ((lane & 7) == 0 && cok && wok) static_cast<uint8_t*>(s)[(rw + i) * ncb + (cc >> 5)] = (uint8_t)(e + 127);
+            } else if constexpr (GRAN == kGranTokP2) {
+                const int e = mx_exponent_from_amax_bits(warp_max_u32(m4, 32) << 16);
+                const float mm = exp2_neg(e);
+                o = e4m3x4(__fmul_rn(f[0], mm), __fmul_rn(f[1], mm), __fmul_rn(f[2], mm), __fmul_rn(f[3], mm));
+                if (lane == 0 && wok) static_cast<uint8_t*>(s)[(rw + i) * ncb + ct] = (uint8_t)(e + 127);
+            } else if constexpr (GRAN == kGranBlkP2) {
+                o = e4m3x4(__fmul_rn(f[0], s_blk), __fmul_rn(f[1], s_blk), __fmul_rn(f[2], s_blk), __fmul_rn(f[3], s_blk));
             } else {
                 const float d = (GRAN == kGranPT) ? s_uniform : s_blk;
                 o = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
@@ -372,6 +434,8 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
         }
         if constexpr (GRAN == kGranBlk) {
             if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = s_blk;
+        } else if constexpr (GRAN == kGranBlkP2) {
+            if (threadIdx.x == 0) static_cast<uint8_t*>(s)[rt * gridDim.x + ct] = (uint8_t)(e_blk + 127);
         }
     }
 }
@@ -410,11 +474,18 @@ int launch_quantize(const QuantJob& j, cudaStream_t st) {
                                                              j.given_scale ? static_cast<const float*>(j.s) : nullptr);
         break;
     }
-    case kGranBlk: {
+    case kGranBlk:
+    case kGranBlkP2: {
         dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
-        quant_block_kernel<<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, static_cast<float*>(j.s));
+        if (j.gran == kGranBlk)
+            quant_block_kernel<false><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s);
+        else
+            quant_block_kernel<true><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s);
         break;
     }
+    case kGranTokP2:
+        quant_rows_kernel<kGranTokP2><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0, nullptr);
+        break;
     case kGranNv: {
         if (!j.given_scale) {
             const int e = launch_amax(j, st, &nparts);
@@ -434,10 +505,10 @@ template <int GRAN>
 static void launch_tile(const QuantJob& j, cudaStream_t st, int nparts, const float* given) {
     dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
     if (j.q != nullptr)
-        quant_tile_t_kernel<GRAN, true><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q, j.s,
+        quant_tile_t_kernel<GRAN, true><<<grid, kTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q, j.s,
                                                                    j.partials, nparts, given);
     else
-        quant_tile_t_kernel<GRAN, false><<<grid, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, nullptr,
+        quant_tile_t_kernel<GRAN, false><<<grid, kTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, nullptr,
                                                                     nullptr, j.partials, nparts, given);
 }
 
@@ -447,6 +518,8 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t st) {
     case kGranTok: launch_tile<kGranTok>(j, st, 0, nullptr); break;
     case kGranMx: launch_tile<kGranMx>(j, st, 0, nullptr); break;
     case kGranBlk: launch_tile<kGranBlk>(j, st, 0, nullptr); break;
+    case kGranTokP2: launch_tile<kGranTokP2>(j, st, 0, nullptr); break;
+    case kGranBlkP2: launch_tile<kGranBlkP2>(j, st, 0, nullptr); break;
     case kGranPT: {
         if (!j.given_scale) {
             const int e = launch_amax(j, st, &nparts);

@@ -68,7 +68,9 @@ typedef enum {
     FP8BS_TOKEN_1x128 = 1,    /* float32 scale per row and 128 columns */
     FP8BS_BLOCK_128x128 = 2,  /* float32 scale per 128x128 tile */
     FP8BS_MXFP8_1x32 = 3,     /* UE8M0 byte per row and 32 columns */
-    FP8BS_NVFP4_1x16 = 4      /* E4M3 byte per row and 16 columns + float32 S_g */
+    FP8BS_NVFP4_1x16 = 4,     /* E4M3 byte per row and 16 columns + float32 S_g */
+    FP8BS_TOKEN_1x128_POW2 = 5,   /* UE8M0 byte per row and 128 columns */
+    FP8BS_BLOCK_128x128_POW2 = 6  /* UE8M0 byte per 128x128 tile */
 } fp8bs_gran;
 
 #define FP8BS_WORKSPACE_BYTES ((size_t)16384)
@@ -94,6 +96,13 @@ typedef enum {
  *   MXFP8_1x32       E4M3 [rows, cols]     uint8 UE8M0 [rows, ceil(cols/32)]
  *   NVFP4_1x16       E2M1 [rows, cols/2]   uint8 E4M3 [rows, cols/16]
  *                    (element 2j in the low nibble of byte j)
+ *   TOKEN_1x128_POW2 E4M3 [rows, cols]     uint8 UE8M0 [rows, ceil(cols/128)]
+ *   BLOCK_128x128_POW2 E4M3 [rows, cols]   uint8 UE8M0 [ceil(rows/128), ceil(cols/128)]
+ *
+ * The two _POW2 granularities are the block-wise recipe with power-of-two
+ * scales ("Low Precision RL", section "2. Unified block-wise FP8": on
+ * Blackwell the block-wise recipe runs through MXFP8 and needs power-of-two
+ * scales): the MXFP8 scale rule applied to 1x128 groups or 128x128 tiles.
  *
  * tensor_scale: NVFP4 only, device float32[1], receives S_g (or supplies it
  * with FP8BS_FLAG_GIVEN_TENSOR_SCALE).  PER_TENSOR with that flag reads S
@@ -116,8 +125,8 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gr
  * of already-quantised codes).  For BLOCK_128x128 the codes are the
  * transpose of the row-wise codes and the scales the transposed scale grid.
  *
- * gran: PER_TENSOR, TOKEN_1x128, BLOCK_128x128 or MXFP8_1x32 (NVFP4 returns
- * FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
+ * gran: PER_TENSOR, TOKEN_1x128, BLOCK_128x128, MXFP8_1x32 or the two
+ * _POW2 granularities (NVFP4 returns FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
  *   q_t      uint8 [cols, rows]           codes of X^T
  *   scales_t layout of the table above for a [cols, rows] matrix
  *   q, scales  optional (both NULL or both set): the row-wise result of
@@ -141,6 +150,9 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
  *       128-wide K block to the FP32 partial sums (k % 128 == 0)
  *   (MXFP8_1x32, MXFP8_1x32)                  UE8M0 scales applied by the
  *       tensor core per 32-wide K block (k % 128 == 0)
+ *   {TOKEN_1x128_POW2,BLOCK_128x128_POW2}^2   UE8M0 scales of 128-wide K
+ *       blocks, each applied by the tensor core to its four 32-wide sub-blocks
+ *       (k % 128 == 0)
  *   (NVFP4_1x16, NVFP4_1x16)                  E4M3 block scales applied by
  *       the tensor core per 16-wide K block, times *a_tensor_scale *
  *       *b_tensor_scale (k % 256 == 0); a, b are packed E2M1 [m|n, k/2]
@@ -166,8 +178,9 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
  * chosen separately from the dense one).  offsets: DEVICE int64 [experts+1],
  * non-decreasing, offsets[0] == 0, offsets[experts] == total_rows (not
  * checked on the host; the host never reads it).  Experts with no rows
- * cost nothing.  gran: MXFP8_1x32 (k % 128 == 0) or TOKEN_1x128 for A with
- * BLOCK_128x128 for B (k % 128 == 0, FP32 scales).  a: [total_rows, k],
+ * cost nothing.  gran: MXFP8_1x32 (k % 128 == 0), TOKEN_1x128 for A with
+ * BLOCK_128x128 for B (k % 128 == 0, FP32 scales), or TOKEN_1x128_POW2 for A
+ * with BLOCK_128x128_POW2 for B (k % 128 == 0).  a: [total_rows, k],
  * a_scales as fp8_quantize for [total_rows, k]; b: [experts, n, k] codes,
  * b_scales: per-expert scale grids stacked along the expert axis.
  * D: BF16 [total_rows, n].  n % 8 == 0.  workspace required.

@@ -49,6 +49,16 @@ def dequant_mxfp8(codes, e8, group: int = 32):
     return e4m3_decode(codes) * _expand(ue8m0_decode(e8), r, c, 1, group)
 
 
+def dequant_1x128_pow2(codes, e8, group: int = 128):
+    r, c = codes.shape
+    return e4m3_decode(codes) * _expand(ue8m0_decode(e8), r, c, 1, group)
+
+
+def dequant_128x128_pow2(codes, e8, block: int = 128):
+    r, c = codes.shape
+    return e4m3_decode(codes) * _expand(ue8m0_decode(e8), r, c, block, block)
+
+
 def dequant_nvfp4(packed, sb, s_g, group: int = 16):
     """value = E2M1(code) * E4M3(block scale) * S_g, all exact in float64."""
     q = unpack_e2m1(packed)
@@ -61,7 +71,20 @@ DEQUANT = {
     "1x128": dequant_1x128,
     "128x128": dequant_128x128,
     "mxfp8": dequant_mxfp8,
+    "1x128_pow2": dequant_1x128_pow2,
+    "128x128_pow2": dequant_128x128_pow2,
 }
+
+
+def dequantize_bf16(codes, scales, gran, s_g=None):
+    """BF16 dequantisation of quantised operands (the "dequantized backward"
+    of "Low Precision RL", "Advanced: dequantized backward": the BF16 backward
+    GEMMs consume BF16 dequantisations of the low-precision forward operands).
+    Reading: the exact dequantised value, rounded once to BF16 (nearest even).
+    Returns float64 values that are exactly BF16."""
+    if gran == "nvfp4":
+        return round_to_bf16(dequant_nvfp4(codes, scales, s_g))
+    return round_to_bf16(DEQUANT[gran](codes, scales))
 
 
 def gemm_f64(a64: np.ndarray, b64: np.ndarray) -> np.ndarray:

@@ -123,6 +123,33 @@ def quantize_mxfp8(x: np.ndarray, group: int = 32):
     return codes, (e + 127).astype(np.uint8)
 
 
+def quantize_1x128_pow2(x: np.ndarray, group: int = 128):
+    """Block-wise recipe with power-of-two scales: 1x128 groups, the MXFP8
+    scale rule (smallest 2^e with 448 * 2^e >= amax) applied per group.  The
+    "Low Precision RL" page (section "2. Unified block-wise FP8") notes that on
+    Blackwell TransformerEngine runs the block-wise recipe through MXFP8 with
+    power-of-two scales.  Returns (codes, UE8M0 codes [R, ceil(C/128)])."""
+    x = np.asarray(x, dtype=F32)
+    e = mxfp8_exponent(_group_amax_1d(x, group))
+    s = np.ldexp(np.float64(1.0), e).astype(F32)
+    codes = cast_e4m3(x, _expand_cols(s, group, x.shape[1]))
+    return codes, (e + 127).astype(np.uint8)
+
+
+def quantize_128x128_pow2(x: np.ndarray, block: int = 128):
+    """128x128 blocks with power-of-two scales (see quantize_1x128_pow2).
+    Returns (codes, UE8M0 codes [ceil(R/128), ceil(C/128)])."""
+    x = np.asarray(x, dtype=F32)
+    r, c = x.shape
+    nr, nc = _ceil_div(r, block), _ceil_div(c, block)
+    pad = np.zeros((nr * block, nc * block), dtype=F32)
+    pad[:r, :c] = np.abs(x)
+    e = mxfp8_exponent(pad.reshape(nr, block, nc, block).max(axis=(1, 3)))
+    s = np.ldexp(np.float64(1.0), e).astype(F32)
+    s_full = np.repeat(np.repeat(s, block, axis=0), block, axis=1)[:r, :c]
+    return cast_e4m3(x, s_full), (e + 127).astype(np.uint8)
+
+
 NVFP4_GLOBAL_DIV = F32(E4M3_MAX * E2M1_MAX)   # 448 * 6 = 2688
 
 

@@ -256,3 +256,81 @@ def test_nvfp4_full_size_sampled():
     b64 = nv_deq(wf[cols], s_g=sg_w)
     got = bf16_to_f64(d[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
     assert_gemm_close(got, OG.gemm_bf16(a64, b64))
+
+
+# ------------------------------------------------------------------ block-wise with power-of-two scales
+P2_Q = {"1x128_pow2": OQ.quantize_1x128_pow2, "128x128_pow2": OQ.quantize_128x128_pow2}
+
+
+def p2_deq(x_f32, gran):
+    c, e = P2_Q[gran](x_f32)
+    return OG.DEQUANT[gran](c, e)
+
+
+@pytest.mark.parametrize("a_gran,b_gran", [("1x128_pow2", "128x128_pow2"), ("1x128_pow2", "1x128_pow2"),
+                                           ("128x128_pow2", "128x128_pow2"), ("128x128_pow2", "1x128_pow2")])
+@pytest.mark.parametrize("m,n,k", [(300, 520, 384), (128, 256, 128), (1, 8, 256), (1000, 1536, 2048)])
+def test_pow2_blockwise(a_gran, b_gran, m, n, k):
+    ab = synth.activations((m, k), seed=m + k + 9, outlier_frac=0.01, outlier_mult=50.0)
+    bb = synth.weights((n, k), seed=n + k + 10, std=0.02)
+    d = gpu_block_gemm(ab, a_gran, bb, b_gran)
+    ref = OG.gemm_bf16(p2_deq(to_f32(ab), a_gran), p2_deq(to_f32(bb), b_gran))
+    assert_gemm_close(bf16_to_f64(d), ref)
+    assert fp.read_status() == 0
+
+
+@pytest.mark.parametrize("counts", [[0, 1, 127, 129, 0, 3, 256, 64], [300], [128] * 12])
+def test_pow2_grouped_ragged(counts):
+    n, k = 264, 384
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    rows, e = int(offsets[-1]), len(counts)
+    ab = synth.activations((rows, k), seed=rows + 1, outlier_frac=0.01, outlier_mult=50.0)
+    bb = synth.weights((e * n, k), seed=rows + 2)
+    qa, sa, _ = fp.fp8_quantize(to_dev_bf16(ab), "1x128_pow2")
+    qbs, sbs = [], []
+    for i in range(e):   # per-expert 128x128 grids, stacked along the expert axis
+        q_, s_, _ = fp.fp8_quantize(to_dev_bf16(bb[i * n:(i + 1) * n]), "128x128_pow2")
+        qbs.append(q_); sbs.append(s_)
+    qb, sb = torch.stack(qbs), torch.stack(sbs)
+    d = fp.fp8_grouped_gemm(qa, sa, qb, sb, torch.from_numpy(offsets).cuda(), "1x128_pow2")
+    got = bf16_to_f64(d)
+    a64 = p2_deq(to_f32(ab), "1x128_pow2")
+    for i in range(e):
+        lo, hi = offsets[i], offsets[i + 1]
+        if hi > lo:
+            ref = OG.gemm_bf16(a64[lo:hi], p2_deq(to_f32(bb[i * n:(i + 1) * n]), "128x128_pow2"))
+            assert_gemm_close(got[lo:hi], ref)
+    assert fp.read_status() == 0
+
+
+def test_pow2_dense_linear_sampled(dense_inputs):
+    """The full-size fwd+bwd step on the power-of-two path, sampled outputs."""
+    x, w, dy = dense_inputs
+    xd, wd, dyd = to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy)
+    qxt, sxt, qx, sx = fp.fp8_quantize_transposed(xd, "1x128_pow2", also_rowwise=True)
+    qwt, swt, qw, sw = fp.fp8_quantize_transposed(wd, "128x128_pow2", also_rowwise=True)
+    qdyt, sdyt, qdy, sdy = fp.fp8_quantize_transposed(dyd, "1x128_pow2", also_rowwise=True)
+    y = fp.fp8_block_gemm(qx, sx, "1x128_pow2", qw, sw, "128x128_pow2")
+    dx = fp.fp8_block_gemm(qdy, sdy, "1x128_pow2", qwt, swt, "128x128_pow2")
+    dw = fp.fp8_block_gemm(qdyt, sdyt, "1x128_pow2", qxt, sxt, "1x128_pow2")
+    torch.cuda.synchronize()
+    assert fp.read_status() == 0
+    xf, wf, dyf = to_f32(x), to_f32(w), to_f32(dy)
+    rows, blocks = sampled(M3, I3, 20)
+    a64 = p2_deq(xf[rows], "1x128_pow2")
+    for nb in blocks:
+        b64 = p2_deq(wf[nb * 128:(nb + 1) * 128], "128x128_pow2")
+        assert_gemm_close(bf16_to_f64(y[torch.from_numpy(rows).cuda(), nb * 128:(nb + 1) * 128]),
+                          OG.gemm_bf16(a64, b64))
+    rows, blocks = sampled(M3, H3, 21)
+    a64 = p2_deq(dyf[rows], "1x128_pow2")
+    for nb in blocks:
+        b64 = p2_deq(np.ascontiguousarray(wf[:, nb * 128:(nb + 1) * 128].T), "128x128_pow2")
+        assert_gemm_close(bf16_to_f64(dx[torch.from_numpy(rows).cuda(), nb * 128:(nb + 1) * 128]),
+                          OG.gemm_bf16(a64, b64))
+    rows, blocks = sampled(I3, H3, 22)
+    a64 = p2_deq(np.ascontiguousarray(dyf[:, rows].T), "1x128_pow2")
+    for nb in blocks:
+        b64 = p2_deq(np.ascontiguousarray(xf[:, nb * 128:(nb + 1) * 128].T), "1x128_pow2")
+        assert_gemm_close(bf16_to_f64(dw[torch.from_numpy(rows).cuda(), nb * 128:(nb + 1) * 128]),
+                          OG.gemm_bf16(a64, b64))

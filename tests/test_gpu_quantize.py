@@ -23,7 +23,10 @@ ROW_ORACLE = {
     "1x128": OQ.quantize_1x128,
     "128x128": OQ.quantize_128x128,
     "mxfp8": OQ.quantize_mxfp8,
+    "1x128_pow2": OQ.quantize_1x128_pow2,
+    "128x128_pow2": OQ.quantize_128x128_pow2,
 }
+BYTE_SCALES = ("mxfp8", "1x128_pow2", "128x128_pow2")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,7 +50,7 @@ def check_rowwise(bits, gran, x_dev=None):
         return
     rq, rs = ROW_ORACLE[gran](x)
     assert np.array_equal(np_u8(q), rq), f"{gran}: {(np_u8(q) != rq).sum()} codes differ"
-    if gran == "mxfp8":
+    if gran in BYTE_SCALES:
         assert np.array_equal(np_u8(s), rs)
     else:
         assert np.array_equal(np_f32(s).reshape(np.shape(rs)), np.asarray(rs, dtype=np.float32))
@@ -60,20 +63,20 @@ def check_transposed(bits, gran, dual):
     torch.cuda.synchronize()
     rq, rs = OQ.transposed(ROW_ORACLE[gran], x)
     assert np.array_equal(np_u8(qt), rq), f"{gran}^T: {(np_u8(qt) != rq).sum()} codes differ"
-    if gran == "mxfp8":
+    if gran in BYTE_SCALES:
         assert np.array_equal(np_u8(st), rs)
     else:
         assert np.array_equal(np_f32(st).reshape(np.shape(rs)), np.asarray(rs, dtype=np.float32))
     if dual:
         rq2, rs2 = ROW_ORACLE[gran](x)
         assert np.array_equal(np_u8(q), rq2)
-        if gran == "mxfp8":
+        if gran in BYTE_SCALES:
             assert np.array_equal(np_u8(s), rs2)
         else:
             assert np.array_equal(np_f32(s).reshape(np.shape(rs2)), np.asarray(rs2, dtype=np.float32))
 
 
-GRANS = ["per_tensor", "1x128", "128x128", "mxfp8"]
+GRANS = ["per_tensor", "1x128", "128x128", "mxfp8", "1x128_pow2", "128x128_pow2"]
 
 
 # -------------------------------------------------------------- tiny blockwise linear operands

@@ -135,3 +135,57 @@ def test_transposed_operands_track_bf16_products():
     for got, want in ((dgrad, dy.astype(np.float64) @ w), (wgrad, dy.astype(np.float64).T @ x)):
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
         assert rel < 0.05, rel
+
+
+def rational_bf16(q):
+    """Round a Fraction to the nearest BF16 value (ties to even), exactly."""
+    from fractions import Fraction
+    if q == 0:
+        return 0.0
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 7)          # 8 significant bits
+    n, r = divmod(a, quantum)
+    n = int(n)
+    if r * 2 > quantum or (r * 2 == quantum and n % 2 == 1):
+        n += 1
+    return sign * float(n * quantum)
+
+
+def test_dequantize_bf16_single_rounding():
+    """Each dequantised value is the exact code x scale rounded once to BF16,
+    checked with rational arithmetic; the sample includes values where a
+    float32 intermediate would round twice and land elsewhere."""
+    from fractions import Fraction
+    g = np.random.Generator(np.random.PCG64(41))
+    codes = np.arange(0, 0x7F, dtype=np.uint8)[None, :]
+    double_rounding_cases = 0
+    # random scales, plus scales built so that code * S lands just above a
+    # BF16 rounding tie by less than half a float32 ulp
+    scales = [np.float32(g.uniform(0.5, 2.0)) * np.float32(2.0 ** g.integers(-20, 20)) for _ in range(200)]
+    for c in (1.125, 1.375, 1.625, 1.875, 3.5, 7.0):
+        for d_ in (2.0 ** -26, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -27):
+            scales.append(np.float32((1 + 2.0 ** -8 + d_) / c))
+    for s in scales:
+        d = G.dequantize_bf16(codes, np.array(s, dtype=np.float32), "per_tensor")
+        for c, v in zip(codes[0], d[0]):
+            exact = Fraction(float(F.E4M3_TABLE[c])) * Fraction(float(s))
+            assert v == rational_bf16(exact)
+            via_f32 = F.round_to_bf16(np.float64(np.float32(F.E4M3_TABLE[c]) * s))
+            double_rounding_cases += int(via_f32 != v)
+    assert double_rounding_cases > 0
+    # NVFP4 values: E2M1 x E4M3 x S_g, each rounded once
+    x = F.bf16_bits_to_f32(synth.activations((2, 64), seed=40))
+    p, sb, sg = Q.quantize_nvfp4(x)
+    d = G.dequantize_bf16(p, sb, "nvfp4", s_g=sg)
+    q = F.unpack_e2m1(p)
+    for i in range(2):
+        for j in range(64):
+            exact = (Fraction(float(F.E2M1_TABLE[q[i, j]])) * Fraction(float(F.E4M3_TABLE[sb[i, j // 16]]))
+                     * Fraction(float(sg)))
+            assert d[i, j] == rational_bf16(exact)

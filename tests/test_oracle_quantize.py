@@ -263,3 +263,46 @@ def test_transposed_is_quantize_of_transpose(act):
     c, s = Q.transposed(Q.quantize_1x128, act)
     c2, s2 = Q.quantize_1x128(np.ascontiguousarray(act.T))
     assert np.array_equal(c, c2) and np.array_equal(s, s2) and c.shape == (512, 256)
+
+
+# ---------------------------------------------------------------- power-of-two block-wise
+def test_pow2_1x128_matches_loops_and_mxfp8(tiny):
+    c, e8 = Q.quantize_1x128_pow2(tiny)
+    r, cc = tiny.shape
+    for i in range(r):
+        for bj in range((cc + 127) // 128):
+            blk = tiny[i, bj * 128: bj * 128 + 128]
+            amax = max(abs(float(v)) for v in blk)
+            e = -127
+            while 448.0 * 2.0 ** e < amax:
+                e += 1
+            assert int(e8[i, bj]) == e + 127
+            for j, v in enumerate(blk):
+                assert int(c[i, bj * 128 + j]) == int(F.e4m3_encode(F32(v) / F32(2.0 ** e)))
+    # the 1x128 exponent is the largest of its four 1x32 MXFP8 exponents
+    _, e32 = Q.quantize_mxfp8(tiny)
+    for i in range(r):
+        for bj in range((cc + 127) // 128):
+            assert int(e8[i, bj]) == int(e32[i, 4 * bj: 4 * bj + 4].max())
+
+
+def test_pow2_128x128_matches_loops():
+    x = F.bf16_bits_to_f32(synth.activations((130, 260), seed=15))
+    c, e8 = Q.quantize_128x128_pow2(x)
+    assert e8.shape == (2, 3)
+    for bi in range(2):
+        for bj in range(3):
+            blk = x[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            e = int(Q.mxfp8_exponent(np.abs(blk).max()))
+            assert int(e8[bi, bj]) == e + 127
+            want = F.e4m3_encode(blk / np.float32(2.0 ** e))
+            assert np.array_equal(c[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128], want)
+    ct, et = Q.transposed(Q.quantize_128x128_pow2, x)
+    assert np.array_equal(ct, c.T) and np.array_equal(et, e8.T)
+
+
+def test_pow2_amax_element_range_and_no_saturation(act):
+    c, e8 = Q.quantize_1x128_pow2(act)
+    dec = np.abs(F.e4m3_decode(c)).reshape(256, 4, 128)
+    top = dec.max(axis=2)
+    assert np.all((top >= 224) & (top <= 448))
