@@ -60,10 +60,14 @@ def dequant_128x128_pow2(codes, e8, block: int = 128):
 
 
 def dequant_nvfp4(packed, sb, s_g, group: int = 16):
-    """value = E2M1(code) * E4M3(block scale) * S_g, all exact in float64."""
+    """value = E2M1(code) * E4M3(block scale) * S_g, all exact in float64.
+    S_g is one outer scale, or one per row ([R]) for per-token scaling."""
     q = unpack_e2m1(packed)
     r, c = q.shape
-    return e2m1_decode(q) * _expand(e4m3_decode(sb), r, c, 1, group) * np.float64(s_g)
+    g = np.asarray(s_g, dtype=np.float64)
+    if g.ndim == 1:
+        g = g.reshape(r, 1)
+    return e2m1_decode(q) * _expand(e4m3_decode(sb), r, c, 1, group) * g
 
 
 DEQUANT = {

@@ -33,7 +33,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import E2M1_MAX, E4M3_MAX, e2m1_encode, e4m3_decode, e4m3_encode, pack_e2m1
+from .formats import E2M1_MAX, E4M3_MAX, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode, pack_e2m1
 
 F32 = np.float32
 
@@ -151,17 +151,71 @@ def quantize_128x128_pow2(x: np.ndarray, block: int = 128):
 
 
 NVFP4_GLOBAL_DIV = F32(E4M3_MAX * E2M1_MAX)   # 448 * 6 = 2688
+# Four-over-six keeps the largest block scale at 256 (not 448) for the map-to-6
+# choice, so the map-to-4 choice of the same block (1.5x larger, 384) still fits
+# E4M3: S_g = amax / (256 * 6).
+NVFP4_GLOBAL_DIV_4OVER6 = F32(256.0 * E2M1_MAX)   # 1536
 
 
-def nvfp4_tensor_scale(x: np.ndarray):
-    """Outer FP32 scale S_g = amax_T / (448 * 6); S_g = 1 for an all-zero tensor."""
+def _outer_scale(amax, four_over_six: bool):
+    """S_g = amax / (V_max(E4M3) * 6) in float32; 1 where amax == 0."""
+    div = NVFP4_GLOBAL_DIV_4OVER6 if four_over_six else NVFP4_GLOBAL_DIV
+    amax = np.asarray(amax, dtype=F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = (amax / div).astype(F32)
+    return np.where(amax == 0, F32(1.0), s).astype(F32)
+
+
+def nvfp4_tensor_scale(x: np.ndarray, four_over_six: bool = False):
+    """Outer FP32 scale of the whole tensor: S_g = amax_T / (448 * 6)
+    (amax_T / (256 * 6) with four-over-six); S_g = 1 for an all-zero tensor."""
     x = np.asarray(x, dtype=F32)
     amax = np.abs(x).max() if x.size else F32(0)
-    amax = F32(amax)
-    return F32(1.0) if amax == 0 else F32(amax / NVFP4_GLOBAL_DIV)
+    return F32(_outer_scale(F32(amax), four_over_six))
 
 
-def quantize_nvfp4(x: np.ndarray, group: int = 16, s_g=None):
+def nvfp4_row_scales(x: np.ndarray, four_over_six: bool = False) -> np.ndarray:
+    """Per-token outer scales ("4. NVFP4 (Blackwell)": activation scaling is
+    computed per token): S_g[r] = amax(row r) / (448 * 6), or / (256 * 6) with
+    four-over-six; 1 for an all-zero row.  Shape [R], float32."""
+    x = np.asarray(x, dtype=F32)
+    amax = np.abs(x).max(axis=1) if x.shape[1] else np.zeros(x.shape[0], dtype=F32)
+    return _outer_scale(amax, four_over_six)
+
+
+def _nvfp4_candidate(x, amax_b, s_col, v_map, group):
+    """Block scales and codes when the block amax is mapped to the E2M1
+    magnitude v_map (6 = the format's maximum, or 4)."""
+    c = x.shape[1]
+    sb = e4m3_encode((amax_b / F32(v_map)) / s_col)
+    big_s = (e4m3_decode(sb).astype(F32) * s_col).astype(F32)
+    big_s_full = _expand_cols(big_s, group, c)
+    zero = big_s_full == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = x / np.where(zero, F32(1.0), big_s_full)
+    q = np.where(zero, np.uint8(0), e2m1_encode(t)).astype(np.uint8)
+    return sb, q, big_s_full
+
+
+def nvfp4_block_sq_error(x, q, big_s_full, group: int = 16):
+    """Squared quantisation error of each 16-element block, in float32:
+    y = E2M1(q) * S_b, d = x - y, and d*d summed over elements 0..7 and 8..15
+    of the block in order, the two half sums then added (each operation one
+    IEEE float32 rounding; the summation order is fixed so that the choice it
+    decides is reproducible).  Returns [R, C/16] float32."""
+    assert group == 16
+    r, c = x.shape
+    y = (e2m1_decode(q).astype(F32) * big_s_full).astype(F32)
+    d = (x - y).astype(F32)
+    sq = (d * d).astype(F32).reshape(r, c // 16, 2, 8)
+    acc = sq[..., 0].copy()
+    for i in range(1, 8):
+        acc = (acc + sq[..., i]).astype(F32)
+    return (acc[..., 0] + acc[..., 1]).astype(F32)
+
+
+def quantize_nvfp4(x: np.ndarray, group: int = 16, s_g=None, row_scaled: bool = False,
+                   four_over_six: bool = False):
     """NVFP4: E2M1 values in 1x16 blocks, an E4M3 scale per block and an outer
     FP32 scale ("Low Precision RL", "4. NVFP4 (Blackwell)"; RHT, 2-D blocks and
     stochastic rounding are switched off there, so plain RNE 1-D blocks).
@@ -172,22 +226,40 @@ def quantize_nvfp4(x: np.ndarray, group: int = 16, s_g=None):
       S_b = decode(s_b) * S_g                     (float32 multiply)
       q   = E2M1( x / S_b )                       (float32 division, then cast)
     A block whose s_b decodes to 0 gets all-zero codes (0x0).
-    Returns (packed codes [R, C/2], block scale codes [R, C/16], S_g).
+
+    row_scaled: the outer scale is per row (per token), S_g[r] from the row's
+    amax, instead of one per tensor.
+
+    four_over_six ("Advanced: four-over-six"): every block is quantised twice,
+    with its amax mapped to 6 (s_b from amax_b / 6) and to 4 (s_b from
+    amax_b / 4), under S_g = amax / (256 * 6); the block keeps the choice with
+    the smaller squared error (nvfp4_block_sq_error), the map-to-6 choice on a
+    tie.
+
+    s_g, when given, is used as the outer scale (a scalar, or [R] when
+    row_scaled).  Returns (packed codes [R, C/2], block scale codes [R, C/16],
+    S_g as a float32 scalar or [R] array).
     """
     x = np.asarray(x, dtype=F32)
     r, c = x.shape
     assert c % group == 0 and group % 2 == 0
     if s_g is None:
-        s_g = nvfp4_tensor_scale(x)
-    s_g = F32(s_g)
+        s_g = nvfp4_row_scales(x, four_over_six) if row_scaled else nvfp4_tensor_scale(x, four_over_six)
+    if row_scaled:
+        s_g = np.asarray(s_g, dtype=F32).reshape(r)
+        s_col = s_g[:, None]
+    else:
+        s_g = F32(s_g)
+        s_col = s_g
     amax_b = _group_amax_1d(x, group)
-    sb = e4m3_encode((amax_b / F32(E2M1_MAX)) / s_g)
-    big_s = (e4m3_decode(sb).astype(F32) * s_g).astype(F32)
-    big_s_full = _expand_cols(big_s, group, c)
-    zero = big_s_full == 0
-    with np.errstate(divide="ignore", invalid="ignore"):
-        t = x / np.where(zero, F32(1.0), big_s_full)
-    q = np.where(zero, np.uint8(0), e2m1_encode(t)).astype(np.uint8)
+    sb, q, big_s_full = _nvfp4_candidate(x, amax_b, s_col, E2M1_MAX, group)
+    if four_over_six:
+        sb4, q4, big_s4 = _nvfp4_candidate(x, amax_b, s_col, 4.0, group)
+        err6 = nvfp4_block_sq_error(x, q, big_s_full, group)
+        err4 = nvfp4_block_sq_error(x, q4, big_s4, group)
+        use4 = err4 < err6
+        sb = np.where(use4, sb4, sb).astype(np.uint8)
+        q = np.where(_expand_cols(use4, group, c), q4, q).astype(np.uint8)
     return pack_e2m1(q), sb, s_g
 
 

@@ -189,3 +189,24 @@ def test_dequantize_bf16_single_rounding():
             exact = (Fraction(float(F.E2M1_TABLE[q[i, j]])) * Fraction(float(F.E4M3_TABLE[sb[i, j // 16]]))
                      * Fraction(float(sg)))
             assert d[i, j] == rational_bf16(exact)
+
+
+def test_nvfp4_row_scaled_gemm_matches_loops():
+    """Per-token outer scales on A (one S_g per row), one per tensor on B:
+    D[i, j] = sum_t E2M1(qa) s_b(a) S_g[i] * E2M1(qb) s_b(b) S_g(B)."""
+    x = F.bf16_bits_to_f32(synth.activations((3, 64), seed=42))
+    x[1] *= np.float32(1e-2)
+    w = F.bf16_bits_to_f32(synth.weights((2, 64), seed=43))
+    for fos in (False, True):
+        pa, sba, ga = Q.quantize_nvfp4(x, row_scaled=True, four_over_six=fos)
+        pb, sbb, gb = Q.quantize_nvfp4(w, four_over_six=fos)
+        assert ga.shape == (3,)
+        qa, qb = F.unpack_e2m1(pa), F.unpack_e2m1(pb)
+        ref = np.zeros((3, 2))
+        for i in range(3):
+            for j in range(2):
+                for t in range(64):
+                    ref[i, j] += (F.E2M1_TABLE[qa[i, t]] * F.E4M3_TABLE[sba[i, t // 16]] * float(ga[i])
+                                  * F.E2M1_TABLE[qb[j, t]] * F.E4M3_TABLE[sbb[j, t // 16]] * float(gb))
+        d64 = G.gemm_f64(G.dequant_nvfp4(pa, sba, ga), G.dequant_nvfp4(pb, sbb, gb))
+        assert np.allclose(d64, ref, rtol=1e-12, atol=1e-20)

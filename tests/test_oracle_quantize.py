@@ -306,3 +306,94 @@ def test_pow2_amax_element_range_and_no_saturation(act):
     dec = np.abs(F.e4m3_decode(c)).reshape(256, 4, 128)
     top = dec.max(axis=2)
     assert np.all((top >= 224) & (top <= 448))
+
+
+# ---------------------------------------------------------------- NVFP4 per-token scale, four-over-six
+def test_nvfp4_row_scaled_is_per_row_tensor_scaling():
+    """Per-token outer scale: each row is quantised exactly as a one-row tensor
+    would be, with S_g[r] = row amax / 2688 (2688 -> 1 exactly; zero row -> 1)."""
+    x = F.bf16_bits_to_f32(synth.activations((6, 64), seed=51, outlier_frac=0.05, outlier_mult=100.0))
+    x[2] *= F32(1e-3)
+    x[3] = 0.0
+    x[4, 7] = F32(2688.0)
+    x[4, 8:] = 0.0
+    p, sb, sg = Q.quantize_nvfp4(x, row_scaled=True)
+    assert sg.shape == (6,) and sg[3] == 1.0 and sg[4] == 1.0
+    for r in range(6):
+        pr, sbr, sgr = Q.quantize_nvfp4(x[r:r + 1])
+        assert sg[r] == sgr
+        assert np.array_equal(p[r:r + 1], pr) and np.array_equal(sb[r:r + 1], sbr)
+    # a row 1000x smaller than the tensor keeps its resolution only with row scales
+    pt, sbt, _ = Q.quantize_nvfp4(x)
+    assert np.count_nonzero(F.unpack_e2m1(p)[2]) > np.count_nonzero(F.unpack_e2m1(pt)[2])
+
+
+def test_nvfp4_four_over_six_worked_example(golden_dir):
+    g = load(golden_dir, "nvfp4_4over6_worked.json")
+    x = np.array(g["x"], dtype=F32)[None, :]
+    p, sb, sg = Q.quantize_nvfp4(x, four_over_six=True)
+    assert sg == F32(g["tensor_scale"])
+    assert sb[0].tolist() == g["block_scale_codes"]
+    deq = F.e2m1_decode(F.unpack_e2m1(p)) * np.repeat(F.e4m3_decode(sb), 16, axis=1) * float(sg)
+    assert np.array_equal(deq, x.astype(np.float64))
+    # the same row without four-over-six cannot represent block 1 exactly
+    p6, sb6, sg6 = Q.quantize_nvfp4(x)
+    deq6 = F.e2m1_decode(F.unpack_e2m1(p6)) * np.repeat(F.e4m3_decode(sb6), 16, axis=1) * float(sg6)
+    assert not np.array_equal(deq6[0, 16:32], x[0, 16:32].astype(np.float64))
+
+
+def _exact_block_sq_error(blk, s_g, v_map):
+    """Squared error of one block mapped to v_map, in exact rational arithmetic,
+    with the scale and codes built by per-element loops."""
+    from fractions import Fraction
+    amax = max(abs(float(v)) for v in blk)
+    sb = int(F.e4m3_encode(F32(F32(amax) / F32(v_map)) / s_g))
+    big_s = F32(F32(F.E4M3_TABLE[sb]) * s_g)
+    err = Fraction(0)
+    for v in blk:
+        q = 0 if big_s == 0 else int(F.e2m1_encode(F32(v) / big_s))
+        d = Fraction(float(v)) - Fraction(float(F.E2M1_TABLE[q])) * Fraction(float(big_s))
+        err += d * d
+    return err, sb
+
+
+def test_nvfp4_four_over_six_picks_smaller_error():
+    """Against exact squared errors: wherever the two choices differ by more
+    than float32 summation can blur, the oracle keeps the one with the smaller
+    error; its scale code is that choice's code."""
+    x = F.bf16_bits_to_f32(synth.activations((8, 256), seed=52, outlier_frac=0.02, outlier_mult=30.0))
+    for row_scaled in (False, True):
+        p, sb, sg = Q.quantize_nvfp4(x, row_scaled=row_scaled, four_over_six=True)
+        chose4 = decided = 0
+        for i in range(8):
+            s_g = F32(sg[i] if row_scaled else sg)
+            if row_scaled:
+                assert s_g == F32(F32(np.abs(x[i]).max()) / F32(1536.0))
+            for b in range(16):
+                blk = x[i, 16 * b:16 * b + 16]
+                e6, sb6 = _exact_block_sq_error(blk, s_g, 6.0)
+                e4, sb4 = _exact_block_sq_error(blk, s_g, 4.0)
+                if abs(e6 - e4) <= 1e-4 * max(e6, e4):
+                    continue
+                decided += 1
+                want = sb4 if e4 < e6 else sb6
+                chose4 += int(e4 < e6)
+                assert int(sb[i, b]) == want
+        assert decided > 100 and 0 < chose4 < decided
+
+
+def test_nvfp4_four_over_six_error_never_worse():
+    """The kept choice's squared error is at most that of the map-to-6 choice
+    under the same outer scale, block by block."""
+    x = F.bf16_bits_to_f32(synth.activations((32, 512), seed=53, outlier_frac=0.01, outlier_mult=50.0))
+    s_g = Q.nvfp4_tensor_scale(x, four_over_six=True)
+    p, sb, _ = Q.quantize_nvfp4(x, four_over_six=True)
+    p6, sb6, _ = Q.quantize_nvfp4(x, s_g=s_g)
+    def block_err(pk, s):
+        deq = F.e2m1_decode(F.unpack_e2m1(pk)) * np.repeat(F.e4m3_decode(s), 16, axis=1) * float(s_g)
+        return ((deq - x) ** 2).reshape(32, 32, 16).sum(axis=2)
+    e, e6 = block_err(p, sb), block_err(p6, sb6)
+    assert np.all(e <= e6 * (1 + 1e-5) + 1e-30)
+    assert np.mean(e) < np.mean(e6)
+    # the largest block scale is 384 (map-to-4 of the amax block) or 256, never above
+    assert F.e4m3_decode(sb).max() <= 384.0
