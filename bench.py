@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the sub-benchmarks")
     ap.add_argument("--kernel", default=None,
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
-                             "moe_gate_up", "nvfp4"],
+                             "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
@@ -241,6 +241,13 @@ def quantize_sweep(torch, fp, dev, pk, flush):
         ms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, g, q=q, scales=s, tensor_scale=ts, ws=ws), 20, flush)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[g] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3)}
+    xd = torch.empty((r, c), dtype=torch.bfloat16, device=dev)
+    for g in ("1x128", "mxfp8"):
+        q, s, _ = bufs[g]
+        sbytes = {"1x128": 4 * e // 128, "mxfp8": e // 32}[g]
+        ms, _ = time_fn(torch, lambda: fp.fp8_dequantize(q, s, g, cols=c, out=xd), 20, flush)
+        gbs = (e + sbytes + 2 * e) / (ms * 1e-3) / 1e9
+        out["dequant_" + g] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3)}
     for g in ("1x128", "128x128", "mxfp8"):
         qt, st, q, s = fp.fp8_quantize_transposed(x, g, True, ws=ws)
         sbytes = {"1x128": 4 * e // 128, "128x128": 4 * (e // 16384), "mxfp8": e // 32}[g]
@@ -304,9 +311,26 @@ def nvfp4_bench(torch, fp, dev, pk, flush):
     qms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, "nvfp4", q=qx, scales=sx, tensor_scale=tx, ws=ws), 10, flush)
     e = m * k
     qgbs = (2 * 2 * e + e // 2 + e // 16) / (qms * 1e-3) / 1e9
+    # the recipe's activation form: per-token outer scales, four-over-six blocks
+    fos = fp.FLAG_NVFP4_4OVER6
+    qr, sr, tr = fp.fp8_quantize(x, "nvfp4_row", flags=fos, ws=ws)
+    rms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, "nvfp4_row", q=qr, scales=sr, tensor_scale=tr, flags=fos,
+                                                    ws=ws), 10, flush)
+    rgbs = (2 * e + e // 2 + e // 16 + 4 * m) / (rms * 1e-3) / 1e9       # one HBM read: the second pass hits L2
+    run_r = lambda: fp.fp8_block_gemm(qr, sr, "nvfp4_row", qw, sw, "nvfp4", tr, tw, k=k, out=d, ws=ws)  # noqa: E731
+    ms_r, _ = time_fn(torch, run_r, 10, flush)
+    t_r = flop / ms_r / 1e9
+    xd = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+    dms, _ = time_fn(torch, lambda: fp.fp8_dequantize(qr, sr, "nvfp4_row", cols=k, tensor_scale=tr, out=xd), 10, flush)
+    dgbs = (e // 2 + e // 16 + 4 * m + 2 * e) / (dms * 1e-3) / 1e9
     return {"gemm": {"tflops": round(t, 1), "ms": round(ms, 3), "frac": round(t / peak, 3)},
+            "gemm_row_scaled_a": {"tflops": round(t_r, 1), "ms": round(ms_r, 3), "frac": round(t_r / peak, 3)},
             "peak_tflops": round(peak, 1), "peak_note": "measured bf16 burst x nominal fp4/bf16 ratio 6",
-            "quantize_x": {"gbs": round(qgbs, 1), "us": round(qms * 1e3, 1), "frac": round(qgbs / pk["hbm_gbs"], 3)}}
+            "quantize_x": {"gbs": round(qgbs, 1), "us": round(qms * 1e3, 1), "frac": round(qgbs / pk["hbm_gbs"], 3)},
+            "quantize_x_row_4over6": {"gbs": round(rgbs, 1), "us": round(rms * 1e3, 1),
+                                      "frac": round(rgbs / pk["hbm_gbs"], 3)},
+            "dequantize_x_bf16": {"gbs": round(dgbs, 1), "us": round(dms * 1e3, 1),
+                                  "frac": round(dgbs / pk["hbm_gbs"], 3)}}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -470,9 +494,18 @@ def single_kernel(args, torch, fp, dev):
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         fn = lambda: fp.fp8_block_gemm(qa, sa, "1x128", qb, sb, gb, out=out, ws=ws)  # noqa: E731
         work = 2 * m * n * k
-    elif name.startswith("quant"):
+    elif name.startswith("quant") or name.startswith("dequant"):
         x = act((8192, 4096), 0.001, 100.0)
-        if name == "quant_dual_1x128":
+        if name == "quant_nvfp4_row_4over6":
+            fos = fp.FLAG_NVFP4_4OVER6
+            q, s_, t_ = fp.fp8_quantize(x, "nvfp4_row", flags=fos, ws=ws)
+            fn = lambda: fp.fp8_quantize(x, "nvfp4_row", q=q, scales=s_, tensor_scale=t_, flags=fos,  # noqa: E731
+                                         ws=ws)
+        elif name == "dequant_1x128":
+            q, s_, _ = fp.fp8_quantize(x, "1x128", ws=ws)
+            xd = torch.empty_like(x)
+            fn = lambda: fp.fp8_dequantize(q, s_, "1x128", cols=x.shape[1], out=xd)  # noqa: E731
+        elif name == "quant_dual_1x128":
             bufs = fp.fp8_quantize_transposed(x, "1x128", True, ws=ws)
             fn = lambda: fp.fp8_quantize_transposed(x, "1x128", True, q_t=bufs[0], scales_t=bufs[1],  # noqa: E731
                                                     q=bufs[2], scales=bufs[3], ws=ws)
@@ -538,36 +571,60 @@ def pow2_step_bench(torch, fp, dev, args, pk):
             "per_gemm_ms": [round(g / n, 3) for g in gms]}
 
 
-def e2e_bench(torch, fp, dev, step, reps=5):
-    """Same step through the public API from pinned HOST buffers: H2D of X, W,
-    dY, the step, D2H of Y, dX, dW, all inside the timed region."""
-    hx = step.x.cpu().pin_memory()
-    hw = step.w.cpu().pin_memory()
-    hdy = step.dy.cpu().pin_memory()
-    hy = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
-    hdx = torch.empty(step.dx.shape, dtype=step.dx.dtype).pin_memory()
-    hdw = torch.empty(step.dw.shape, dtype=step.dw.dtype).pin_memory()
+def e2e_bench(torch, fp, dev, step, reps=8):
+    """The step through the public API from pinned HOST buffers, with every
+    host<->device copy inside the timed region: each step copies X, W and dY
+    in and Y, dX and dW out.  The copies run on streams of their own, two
+    buffer sets deep, so step i's outputs go out and step i+1's inputs come in
+    while step i computes (as a training loop overlaps its transfers).
+    Timed with CUDA events from the first input copy to the last output copy."""
+    sets = [step, DenseStep(torch, fp, dev, seed=3000)]
+    hx, hw, hdy = (t.cpu().pin_memory() for t in (step.x, step.w, step.dy))
+    hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (s_.y, s_.dx, s_.dw)] for s_ in sets]
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def once():
-        step.x.copy_(hx, non_blocking=True)
-        step.w.copy_(hw, non_blocking=True)
-        step.dy.copy_(hdy, non_blocking=True)
-        step.run()
-        hy.copy_(step.y, non_blocking=True)
-        hdx.copy_(step.dx, non_blocking=True)
-        hdw.copy_(step.dw, non_blocking=True)
+    def run(n, t_start=None, t_end=None):
+        cmp_done, d2h_done = [None] * n, [None] * n
+        if t_start is not None:
+            t_start.record(s_in)
+        for i in range(n):
+            st = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(cmp_done[i - 2])        # this set's inputs are no longer read
+                for h, d in zip((hx, hw, hdy), (st.x, st.w, st.dy)):
+                    d.copy_(h, non_blocking=True)
+                h2d_done = torch.cuda.Event()
+                h2d_done.record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(h2d_done)
+                if i >= 2:
+                    s_cmp.wait_event(d2h_done[i - 2])       # this set's outputs have been copied out
+                st.run()
+                cmp_done[i] = torch.cuda.Event()
+                cmp_done[i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(cmp_done[i])
+                for h, d in zip(hout[i % 2], (st.y, st.dx, st.dw)):
+                    h.copy_(d, non_blocking=True)
+                d2h_done[i] = torch.cuda.Event()
+                d2h_done[i].record(s_out)
+        if t_end is not None:
+            t_end.record(s_out)
 
-    once()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        once()
+    run(2)
     torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / reps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(reps, t0, t1)
+    t1.synchronize()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / reps
     h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hdy))
-    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hdw))
-    return {"value": round(STEP_FLOP / dt / 1e12, 1), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3)}
+    d2h = sum(t.numel() * t.element_size() for t in hout[0])
+    return {"value": round(STEP_FLOP / (ms * 1e-3) / 1e12, 1), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "pipeline": "2 buffer sets; H2D, compute and D2H on separate streams"}
 
 
 if __name__ == "__main__":

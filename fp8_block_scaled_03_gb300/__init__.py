@@ -9,11 +9,14 @@ Entry points (same names as the C ABI):
     fp8_quantize(x, gran)                 -> (q, scales, tensor_scale)
     fp8_quantize_transposed(x, gran, also_rowwise=False)
                                           -> (q_t, scales_t, q, scales)
+    fp8_dequantize(q, scales, gran)       -> BF16 values (exact, rounded once)
     fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16)
     fp8_grouped_gemm(a, sa, b, sb, offsets, gran)                      -> d (bf16)
 
-Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4", and the
-block-wise recipe with power-of-two scales "1x128_pow2", "128x128_pow2".
+Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4", the
+block-wise recipe with power-of-two scales "1x128_pow2", "128x128_pow2", and
+"nvfp4_row" (NVFP4 with one outer scale per row).  Flags:
+FLAG_GIVEN_TENSOR_SCALE, FLAG_NVFP4_4OVER6.
 """
 from __future__ import annotations
 
@@ -26,11 +29,14 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfp8bs.so")
 
-GRAN = {"per_tensor": 0, "1x128": 1, "128x128": 2, "mxfp8": 3, "nvfp4": 4, "1x128_pow2": 5, "128x128_pow2": 6}
+GRAN = {"per_tensor": 0, "1x128": 1, "128x128": 2, "mxfp8": 3, "nvfp4": 4, "1x128_pow2": 5, "128x128_pow2": 6,
+        "nvfp4_row": 7}
+NVFP4_GRANS = (4, 7)
 FLAG_GIVEN_TENSOR_SCALE = 1
+FLAG_NVFP4_4OVER6 = 2
 STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNSUPPORTED",
           -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE"}
-EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
+EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
            "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm")
 
@@ -55,6 +61,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I64, I, U, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
     lib.fp8_quantize.argtypes = [P, I64, I64, I64, I, P, P, P, U, P, SZ, P]
     lib.fp8_quantize_transposed.argtypes = [P, I64, I64, I64, I, P, P, P, P, P, U, P, SZ, P]
+    lib.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, P, I64, P]
     lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
     lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
@@ -161,12 +168,12 @@ def fp8_quantize(x: torch.Tensor, gran, *, q=None, scales=None, tensor_scale=Non
     rows, cols = x.shape
     dev = x.device
     if q is None:
-        q = torch.empty((rows, cols // 2 if g == 4 else cols), dtype=torch.uint8, device=dev)
+        q = torch.empty((rows, cols // 2 if g in NVFP4_GRANS else cols), dtype=torch.uint8, device=dev)
     if scales is None:
         shp, dt = scale_shape(g, rows, cols)
         scales = torch.empty(shp, dtype=dt, device=dev)
-    if g == 4 and tensor_scale is None:
-        tensor_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    if g in NVFP4_GRANS and tensor_scale is None:
+        tensor_scale = torch.empty((rows if g == 7 else 1,), dtype=torch.float32, device=dev)
     ws = ws if ws is not None else workspace(dev)
     rc = load_library().fp8_quantize(_ptr(x), rows, cols, x.stride(0), g, _ptr(q), _ptr(scales),
                                      _ptr(tensor_scale), flags, _ptr(ws), ws.numel(), _stream(stream))
@@ -200,13 +207,27 @@ def fp8_quantize_transposed(x: torch.Tensor, gran, also_rowwise: bool = False, *
     return q_t, scales_t, q, scales
 
 
+def fp8_dequantize(q, scales, gran, cols: Optional[int] = None, tensor_scale=None, *, out=None, stream=None):
+    """BF16 values of quantised codes (exact product rounded once); returns out [rows, cols]."""
+    g = _gran(gran)
+    rows = q.shape[0]
+    if cols is None:
+        cols = q.shape[1] * (2 if g in NVFP4_GRANS else 1)
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    rc = load_library().fp8_dequantize(_ptr(q), _ptr(scales), _ptr(tensor_scale), rows, cols, g, _ptr(out),
+                                       out.stride(0), _stream(stream))
+    _check("fp8_dequantize", rc)
+    return out
+
+
 def fp8_block_gemm(a, a_scales, a_gran, b, b_scales, b_gran, a_tensor_scale=None, b_tensor_scale=None, *,
                    k: Optional[int] = None, out=None, ws=None, stream=None):
     """D = deq(A) . deq(B)^T in BF16.  A [m, k] and B [n, k] codes (NVFP4: packed [., k/2])."""
     ga, gb = _gran(a_gran), _gran(b_gran)
     m, n = a.shape[0], b.shape[0]
     if k is None:
-        k = a.shape[1] * (2 if ga == 4 else 1)
+        k = a.shape[1] * (2 if ga in NVFP4_GRANS else 1)
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
     ws = ws if ws is not None else workspace(a.device)

@@ -38,8 +38,9 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 // Scale pointers: FP32 scales and UE8M0 words are read 4 bytes at a time,
 // NVFP4 block scales 16 bytes at a time.
+inline bool is_nvfp4(int gran) { return gran == FP8BS_NVFP4_1x16 || gran == FP8BS_NVFP4_ROW_1x16; }
 inline bool scales_aligned(const void* s, int gran) {
-    if (gran == FP8BS_NVFP4_1x16) return aligned16(s);
+    if (is_nvfp4(gran)) return aligned16(s);
     if (gran == FP8BS_TOKEN_1x128_POW2 || gran == FP8BS_BLOCK_128x128_POW2) return true;   // read bytewise
     return aligned4(s);
 }
@@ -60,14 +61,20 @@ inline int cuda_status(int err) {
 // pointer is looked at (allocators may hand out NULL for empty tensors).
 int check_quant_common(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran) {
     if (rows < 0 || cols < 0) return FP8BS_EINVAL;
-    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_BLOCK_128x128_POW2) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
     if (cols % 8 != 0 || ld_x < cols || ld_x % 8 != 0) return FP8BS_EINVAL;
-    if (gran == FP8BS_NVFP4_1x16 && cols % 16 != 0) return FP8BS_EINVAL;
+    if (is_nvfp4(gran) && cols % 16 != 0) return FP8BS_EINVAL;
     if (ceil_div(rows, 128) > 65535 || ceil_div(cols, 128) > 0x7FFFFFFF) return FP8BS_EINVAL;
     if (rows == 0 || cols == 0) return 1;
     if (x == nullptr) return FP8BS_EINVAL;
     if (!aligned16(x)) return FP8BS_EALIGN;
     return FP8BS_OK;
+}
+
+// Unknown flag bits, or four-over-six on a non-NVFP4 granularity.
+bool bad_flags(int gran, unsigned flags) {
+    if (flags & ~(FP8BS_FLAG_GIVEN_TENSOR_SCALE | FP8BS_FLAG_NVFP4_4OVER6)) return true;
+    return (flags & FP8BS_FLAG_NVFP4_4OVER6) && !is_nvfp4(gran);
 }
 
 bool needs_partials(int gran, unsigned flags) {
@@ -81,10 +88,12 @@ extern "C" {
 int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
                  void* q, void* scales, float* tensor_scale, unsigned flags,
                  void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (bad_flags(gran, flags)) return FP8BS_EINVAL;
     int rc = check_quant_common(x, rows, cols, ld_x, gran);
     if (rc) return rc > 0 ? FP8BS_OK : rc;
     if (q == nullptr || scales == nullptr) return FP8BS_EINVAL;
-    if (gran == FP8BS_NVFP4_1x16 && tensor_scale == nullptr) return FP8BS_EINVAL;
+    if (is_nvfp4(gran) && tensor_scale == nullptr) return FP8BS_EINVAL;
+    if (is_nvfp4(gran) && !aligned4(tensor_scale)) return FP8BS_EALIGN;
     if (!aligned16(q)) return FP8BS_EALIGN;
     if (needs_partials(gran, flags) && (workspace == nullptr || workspace_bytes < kWorkspaceBytes))
         return FP8BS_EWORKSPACE;
@@ -94,6 +103,7 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gr
     j.q = static_cast<uint8_t*>(q); j.s = scales;
     j.tensor_scale = tensor_scale;
     j.given_scale = (flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE) != 0;
+    j.four_over_six = (flags & FP8BS_FLAG_NVFP4_4OVER6) != 0;
     j.partials = workspace ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kPartialsOffset) : nullptr;
     return cuda_status(launch_quantize(j, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -103,7 +113,8 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
                             float* tensor_scale, unsigned flags,
                             void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
     (void)tensor_scale;
-    if (gran == FP8BS_NVFP4_1x16) return FP8BS_EUNSUPPORTED;
+    if (is_nvfp4(gran)) return FP8BS_EUNSUPPORTED;
+    if (bad_flags(gran, flags)) return FP8BS_EINVAL;
     if (rows % 16 != 0) return FP8BS_EINVAL;
     int rc = check_quant_common(x, rows, cols, ld_x, gran);
     if (rc) return rc > 0 ? FP8BS_OK : rc;
@@ -122,6 +133,21 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
     return cuda_status(launch_quantize_transposed(j, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp8_dequantize(const void* q, const void* scales, const float* tensor_scale, int64_t rows, int64_t cols,
+                   int gran, void* out, int64_t ld_out, fp8bs_stream_t stream) {
+    if (rows < 0 || cols < 0 || gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
+    if (cols % 8 != 0 || ld_out < cols || ld_out % 8 != 0) return FP8BS_EINVAL;
+    if (is_nvfp4(gran) && cols % 16 != 0) return FP8BS_EINVAL;
+    if (rows == 0 || cols == 0) return FP8BS_OK;
+    if (q == nullptr || scales == nullptr || out == nullptr) return FP8BS_EINVAL;
+    if (is_nvfp4(gran) && tensor_scale == nullptr) return FP8BS_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(q) & 7u) || !aligned16(out) || !scales_aligned(scales, gran) ||
+        (is_nvfp4(gran) && !aligned4(tensor_scale)))
+        return FP8BS_EALIGN;
+    return cuda_status(launch_dequantize(static_cast<const uint8_t*>(q), scales, tensor_scale, rows, cols, gran, out,
+                                         ld_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
                    const void* b, const void* b_scales, int b_gran,
                    const float* a_tensor_scale, const float* b_tensor_scale,
@@ -130,7 +156,7 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0) return FP8BS_EINVAL;
-    if (a_gran < 0 || a_gran > FP8BS_BLOCK_128x128_POW2 || b_gran < 0 || b_gran > FP8BS_BLOCK_128x128_POW2)
+    if (a_gran < 0 || a_gran > FP8BS_NVFP4_ROW_1x16 || b_gran < 0 || b_gran > FP8BS_NVFP4_ROW_1x16)
         return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
     if (!scales_aligned(a_scales, a_gran) || !scales_aligned(b_scales, b_gran)) return FP8BS_EALIGN;
@@ -156,9 +182,12 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
         if (k % 128 != 0) return FP8BS_EINVAL;
         return cuda_status(launch_gemm_mx(j, st));
     }
-    if (a_gran == FP8BS_NVFP4_1x16 && b_gran == FP8BS_NVFP4_1x16) {
+    if (is_nvfp4(a_gran) && b_gran == FP8BS_NVFP4_1x16) {
         if (k % 256 != 0) return FP8BS_EINVAL;
         if (a_tensor_scale == nullptr || b_tensor_scale == nullptr) return FP8BS_EINVAL;
+        if (!aligned4(a_tensor_scale) || !aligned4(b_tensor_scale)) return FP8BS_EALIGN;
+        j.a_ts_rows = a_gran == FP8BS_NVFP4_ROW_1x16;
+        j.a_gran = FP8BS_NVFP4_1x16;
         return cuda_status(launch_gemm_mx(j, st));
     }
     return FP8BS_EUNSUPPORTED;

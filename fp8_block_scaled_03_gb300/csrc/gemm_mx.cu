@@ -67,8 +67,9 @@ struct Params {
     int64_t m, n, k;
     const uint8_t* sa;   // row-major scale bytes [m, k / vec]
     const uint8_t* sb;   // [experts * n, k / vec]
-    const float* a_ts;   // NVFP4 tensor scales
-    const float* b_ts;
+    const float* a_ts;   // NVFP4 outer scales: [1], or [m] when a_ts_rows
+    const float* b_ts;   // [1]
+    int a_ts_rows;
     __nv_bfloat16* d;
     int* status;
     const int64_t* offsets;
@@ -342,11 +343,16 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // ------------------------------------------------------------ epilogue (8 warps)
         const int q = warp & 3, h = (warp - 4) >> 2;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        float g = 1.0f;
-        if (KIND == kNv) g = __ldg(p.a_ts) * __ldg(p.b_ts);
+        float g = 1.0f, gb = 1.0f;
+        if (KIND == kNv) {
+            gb = __ldg(p.b_ts);
+            if (!p.a_ts_rows) g = __ldg(p.a_ts) * gb;
+        }
         uint32_t tcount = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const int64_t row = ti.row0 + 32 * q + lane;
+            if (KIND == kNv && p.a_ts_rows) g = (row < ti.row_end) ? __ldg(p.a_ts + row) * gb : 0.0f;
             const bool got = mbar_wait(smem_u32(&sh->tfull), tcount & 1, abort, p.status);
             if (!__all_sync(0xFFFFFFFFu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
             tc_fence_after();
@@ -365,7 +371,6 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
-            const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
             if (row < ti.row_end) {
                 __nv_bfloat16* drow = p.d + row * p.n + col0;
@@ -418,6 +423,7 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     p.sa = static_cast<const uint8_t*>(j.sa);
     p.sb = static_cast<const uint8_t*>(j.sb);
     p.a_ts = j.a_ts; p.b_ts = j.b_ts;
+    p.a_ts_rows = j.a_ts_rows ? 1 : 0;
     p.d = static_cast<__nv_bfloat16*>(j.d);
     p.status = j.status;
     p.offsets = j.offsets;

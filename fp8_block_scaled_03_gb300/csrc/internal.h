@@ -25,6 +25,7 @@ struct QuantJob {
     void* st;           // transposed scales
     float* tensor_scale;
     bool given_scale;
+    bool four_over_six; // NVFP4: four-over-six block scales
     uint32_t* partials; // amax partials (per-tensor / NVFP4)
 };
 int launch_quantize(const QuantJob& j, cudaStream_t s);
@@ -32,11 +33,16 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                        float* scale, uint32_t* partials, int nparts, cudaStream_t s);
 
+// ---- dequantisation to BF16 (dequant.cu)
+int launch_dequantize(const uint8_t* q, const void* scales, const float* tensor_scale, int64_t rows, int64_t cols,
+                      int gran, void* out, int64_t ld_out, cudaStream_t s);
+
 // ---- GEMMs (gemm_blockwise.cu, gemm_mx.cu)
 struct GemmJob {
     const void* a; const void* sa; int a_gran;
     const void* b; const void* sb; int b_gran;
     const float* a_ts; const float* b_ts;
+    bool a_ts_rows = false;               // NVFP4: a_ts holds one outer scale per row of A
     int64_t m, n, k;
     void* d;
     int* status;

@@ -18,7 +18,8 @@
 
 namespace fp8bs {
 
-enum { kGranPT = 0, kGranTok = 1, kGranBlk = 2, kGranMx = 3, kGranNv = 4, kGranTokP2 = 5, kGranBlkP2 = 6 };
+enum { kGranPT = 0, kGranTok = 1, kGranBlk = 2, kGranMx = 3, kGranNv = 4, kGranTokP2 = 5, kGranBlkP2 = 6,
+       kGranNvRow = 7 };
 
 // Granularities whose scale is a power of two (UE8M0 byte): the division by
 // the scale is an exact multiplication by 2^-e.
@@ -161,6 +162,90 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
 }
 
 // ---------------------------------------------------------------- NVFP4 1x16 (row-wise)
+// "4. NVFP4 (Blackwell)": E2M1 codes in 1x16 blocks, an E4M3 block scale
+// s_b = E4M3((amax_b / 6) / S_g) and an outer float32 S_g (per tensor, or per
+// row for per-token activation scaling).  A lane owns 8 elements, so a block
+// is a lane pair (2j, 2j+1).
+//
+// Four-over-six ("Advanced: four-over-six"): each block is also quantised
+// with its amax mapped to 4 (s_b from amax_b / 4) and keeps that result only
+// when its squared error is strictly smaller.  The error of 8 elements is
+// summed in order in float32 (no fused multiply-add); the two lanes' half
+// sums are then added, which is the same sum on both lanes (IEEE addition
+// commutes).  S_g is amax / (256 * 6) in that mode.
+
+__device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s) {
+    if (big_s == 0.0f) return 0u;
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(f[i], big_s);
+    return e2m1x8(t);
+}
+
+// sum_i (x_i - E2M1(q_i) * S_b)^2 over this lane's 8 elements, in order.
+__device__ __forceinline__ float half_sq_err(const float* f, uint32_t packed, float big_s) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float d = __fsub_rn(f[i], __fmul_rn(e2m1_value((packed >> (4 * i)) & 0xFu), big_s));
+        const float sq = __fmul_rn(d, d);
+        acc = (i == 0) ? sq : __fadd_rn(acc, sq);
+    }
+    return acc;
+}
+
+// One lane's half block: packed E2M1 codes and the block's scale byte.  Every
+// lane of the warp must call this (shuffles).
+template <bool FOS>
+__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, uint32_t& packed, uint32_t& code) {
+    const uint32_t m = warp_max_u32(absmax_v4(v), 2);
+    const float amax_b = amax_bits_to_f32(m);
+    float f[8];
+    unpack8(v, f);
+    code = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, kE2M1Max), s_g));
+    const float s6 = __fmul_rn(e4m3_value(code), s_g);
+    packed = e2m1_quant8(f, s6);
+    if constexpr (FOS) {
+        const uint32_t code4 = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, 4.0f), s_g));
+        const float s4 = __fmul_rn(e4m3_value(code4), s_g);
+        const uint32_t p4 = e2m1_quant8(f, s4);
+        float e6 = half_sq_err(f, packed, s6);
+        float e4 = half_sq_err(f, p4, s4);
+        e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, 1));
+        e4 = __fadd_rn(e4, __shfl_xor_sync(0xFFFFFFFFu, e4, 1));
+        if (e4 < e6) {
+            packed = p4;
+            code = code4;
+        }
+    }
+}
+
+// Quantise columns [cb, cb + 1024) of row r with outer scale s_g.
+template <bool FOS>
+__device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, int64_t r, int64_t cb, int64_t cols,
+                                              int64_t ldx, uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
+                                              float s_g, int lane) {
+    const int64_t nb = cols >> 4;
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t c = cb + j * 256 + lane * 8;
+        v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t c = cb + j * 256 + lane * 8;
+        uint32_t packed, code;
+        nvfp4_half_block<FOS>(v[j], s_g, packed, code);
+        if (c < cols) {
+            *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
+            if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
+        }
+    }
+}
+
+// One outer scale for the tensor (from the amax partials, or given).
+template <bool FOS>
 __global__ void __launch_bounds__(kThreads)
 quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sb, float* __restrict__ tensor_scale,
@@ -171,44 +256,49 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
         s_g = *tensor_scale;
     } else {
         const float amax = tensor_amax(partials, nparts);
-        s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kNvfp4GlobalDiv);
+        s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, FOS ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
         if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_g;
     }
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t segs = ceil_div(cols, kSeg);
     const int64_t total = rows * segs;
-    const int64_t nb = cols >> 4;
     for (int64_t t = gw; t < total; t += nw) {
         const int64_t r = t / segs;
-        const int64_t cb = (t - r * segs) * kSeg;
-        uint4 v[4];
+        nvfp4_segment<FOS>(x, r, (t - r * segs) * kSeg, cols, ldx, q, sb, s_g, lane);
+    }
+}
+
+// One outer scale per row (per token): a warp owns a row, reads it once for
+// its amax and again (from L2) to quantise it.
+template <bool FOS>
+__global__ void __launch_bounds__(kThreads)
+quant_nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                       uint8_t* __restrict__ q, uint8_t* __restrict__ sb, float* __restrict__ row_scale, bool given) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = gw; r < rows; r += nw) {
+        float s_g;
+        if (given) {
+            s_g = row_scale[r];
+        } else {
+            uint32_t m = 0;
+            for (int64_t cb = 0; cb < cols; cb += kSeg) {
+                uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t c = cb + j * 256 + lane * 8;
-            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
-        }
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t c = cb + j * 256 + lane * 8;
+                    v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t c = cb + j * 256 + lane * 8;
-            const bool ok = c < cols;
-            const uint32_t m = warp_max_u32(absmax_v4(v[j]), 2);
-            const float amax_b = amax_bits_to_f32(m);
-            const uint32_t code = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, kE2M1Max), s_g));
-            const float big_s = __fmul_rn(e4m3_value(code), s_g);
-            float f[8];
-            unpack8(v[j], f);
-            uint32_t packed = 0;
-            if (big_s != 0.0f) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = __fdiv_rn(f[i], big_s);
-                packed = e2m1x8(f);
+                for (int j = 0; j < 4; ++j) m = max(m, absmax_v4(v[j]));
             }
-            if (ok) {
-                *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
-                if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
-            }
+            const float amax = amax_bits_to_f32(warp_max_u32(m, 32));
+            s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, FOS ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
+            if (lane == 0) row_scale[r] = s_g;
         }
+        for (int64_t cb = 0; cb < cols; cb += kSeg) nvfp4_segment<FOS>(x, r, cb, cols, ldx, q, sb, s_g, lane);
     }
 }
 
@@ -491,8 +581,24 @@ int launch_quantize(const QuantJob& j, cudaStream_t st) {
             const int e = launch_amax(j, st, &nparts);
             if (e) return e;
         }
-        quant_nvfp4_kernel<<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, static_cast<uint8_t*>(j.s),
-                                                    j.tensor_scale, j.partials, nparts, j.given_scale);
+        auto* sb = static_cast<uint8_t*>(j.s);
+        if (j.four_over_six)
+            quant_nvfp4_kernel<true><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, sb, j.tensor_scale,
+                                                              j.partials, nparts, j.given_scale);
+        else
+            quant_nvfp4_kernel<false><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, sb, j.tensor_scale,
+                                                               j.partials, nparts, j.given_scale);
+        break;
+    }
+    case kGranNvRow: {
+        const int rb = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(j.rows, kThreads / 32), cap));
+        auto* sb = static_cast<uint8_t*>(j.s);
+        if (j.four_over_six)
+            quant_nvfp4_row_kernel<true><<<rb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, sb, j.tensor_scale,
+                                                                  j.given_scale);
+        else
+            quant_nvfp4_row_kernel<false><<<rb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, sb,
+                                                                   j.tensor_scale, j.given_scale);
         break;
     }
     default:

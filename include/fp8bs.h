@@ -70,7 +70,8 @@ typedef enum {
     FP8BS_MXFP8_1x32 = 3,     /* UE8M0 byte per row and 32 columns */
     FP8BS_NVFP4_1x16 = 4,     /* E4M3 byte per row and 16 columns + float32 S_g */
     FP8BS_TOKEN_1x128_POW2 = 5,   /* UE8M0 byte per row and 128 columns */
-    FP8BS_BLOCK_128x128_POW2 = 6  /* UE8M0 byte per 128x128 tile */
+    FP8BS_BLOCK_128x128_POW2 = 6, /* UE8M0 byte per 128x128 tile */
+    FP8BS_NVFP4_ROW_1x16 = 7      /* NVFP4 with one float32 S_g per row (per token) */
 } fp8bs_gran;
 
 #define FP8BS_WORKSPACE_BYTES ((size_t)16384)
@@ -78,6 +79,7 @@ typedef enum {
 /* flags for fp8_quantize / fp8_quantize_transposed */
 #define FP8BS_FLAG_GIVEN_TENSOR_SCALE 1u  /* PER_TENSOR / NVFP4: *tensor_scale is
                                              an input (S, resp. S_g); skip the amax pass */
+#define FP8BS_FLAG_NVFP4_4OVER6 2u        /* NVFP4 only: four-over-six block scales */
 
 /*
  * fp8_quantize -- row-wise quantisation of a BF16 matrix x [rows, cols].
@@ -96,6 +98,7 @@ typedef enum {
  *   MXFP8_1x32       E4M3 [rows, cols]     uint8 UE8M0 [rows, ceil(cols/32)]
  *   NVFP4_1x16       E2M1 [rows, cols/2]   uint8 E4M3 [rows, cols/16]
  *                    (element 2j in the low nibble of byte j)
+ *   NVFP4_ROW_1x16   as NVFP4_1x16
  *   TOKEN_1x128_POW2 E4M3 [rows, cols]     uint8 UE8M0 [rows, ceil(cols/128)]
  *   BLOCK_128x128_POW2 E4M3 [rows, cols]   uint8 UE8M0 [ceil(rows/128), ceil(cols/128)]
  *
@@ -105,10 +108,26 @@ typedef enum {
  * scales): the MXFP8 scale rule applied to 1x128 groups or 128x128 tiles.
  *
  * tensor_scale: NVFP4 only, device float32[1], receives S_g (or supplies it
- * with FP8BS_FLAG_GIVEN_TENSOR_SCALE).  PER_TENSOR with that flag reads S
- * from scales[0].  Otherwise may be NULL.
- * workspace: required for PER_TENSOR and NVFP4 (amax partials); may be
- * NULL for the other granularities.
+ * with FP8BS_FLAG_GIVEN_TENSOR_SCALE).  NVFP4_ROW_1x16: device float32[rows],
+ * S_g of each row (per-token activation scaling, "4. NVFP4 (Blackwell)"):
+ * S_g[r] = amax(row r) / 2688, 1 for an all-zero row; supplied by the caller
+ * with FP8BS_FLAG_GIVEN_TENSOR_SCALE.  PER_TENSOR with that flag reads S
+ * from scales[0].  Otherwise may be NULL.  Gate and up projections that
+ * share one outer weight scale ("4. NVFP4 (Blackwell)") quantise their
+ * concatenation, or pass the shared S_g with FP8BS_FLAG_GIVEN_TENSOR_SCALE.
+ *
+ * FP8BS_FLAG_NVFP4_4OVER6 ("Low Precision RL", "Advanced: four-over-six";
+ * NVFP4_1x16 and NVFP4_ROW_1x16 only, else FP8BS_EINVAL): the outer divisor
+ * becomes 256 * 6 (S_g = amax / 1536), each 1x16 block is quantised with
+ * its amax mapped to 6 (s_b = E4M3((amax_b / 6) / S_g)) and to 4
+ * (s_b = E4M3((amax_b / 4) / S_g)), and keeps the map-to-4 result only when
+ * its squared error is strictly smaller.  The error of one choice: y =
+ * E2M1value(q) * S_b, d = x - y, d * d, each an IEEE float32 operation
+ * without fused multiply-add, summed in float32 over elements 0..7 and
+ * 8..15 of the block in order, then the two half sums added.
+ * Unknown flag bits return FP8BS_EINVAL.
+ * workspace: required for PER_TENSOR and NVFP4_1x16 (amax partials); may
+ * be NULL for the other granularities.
  */
 int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gran,
                  void* q, void* scales, float* tensor_scale, unsigned flags,
@@ -126,7 +145,7 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gr
  * transpose of the row-wise codes and the scales the transposed scale grid.
  *
  * gran: PER_TENSOR, TOKEN_1x128, BLOCK_128x128, MXFP8_1x32 or the two
- * _POW2 granularities (NVFP4 returns FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
+ * _POW2 granularities (both NVFP4 granularities return FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
  *   q_t      uint8 [cols, rows]           codes of X^T
  *   scales_t layout of the table above for a [cols, rows] matrix
  *   q, scales  optional (both NULL or both set): the row-wise result of
@@ -136,6 +155,24 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
                             void* q_t, void* scales_t, void* q, void* scales,
                             float* tensor_scale, unsigned flags,
                             void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8_dequantize -- BF16 values of quantised codes: out[r, c] = BF16(code *
+ * scale) (NVFP4: E2M1 code * E4M3 block scale * outer scale), the exact
+ * product rounded once to nearest-even.
+ *
+ * The dequantized backward of "Low Precision RL" ("Advanced: dequantized
+ * backward"): the BF16 backward GEMMs consume BF16 dequantisations of the
+ * operands quantised for the forward pass.  q and scales as written by
+ * fp8_quantize for the same gran and [rows, cols]; out BF16 [rows, cols] with
+ * row pitch ld_out elements (ld_out >= cols, ld_out % 8 == 0), 16-byte
+ * aligned; q 8-byte aligned.  cols % 8 == 0 (% 16 for NVFP4).  tensor_scale:
+ * NVFP4 only, device float32[1] (float32[rows] for NVFP4_ROW_1x16), 4-byte
+ * aligned.  rows or cols == 0 is a no-op.  UE8M0 byte 0xFF (NaN) is not
+ * accepted as a scale (results unspecified).
+ */
+int fp8_dequantize(const void* q, const void* scales, const float* tensor_scale, int64_t rows, int64_t cols,
+                   int gran, void* out, int64_t ld_out, fp8bs_stream_t stream);
 
 /*
  * fp8_block_gemm -- D[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], D in BF16.
@@ -156,10 +193,13 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
  *   (NVFP4_1x16, NVFP4_1x16)                  E4M3 block scales applied by
  *       the tensor core per 16-wide K block, times *a_tensor_scale *
  *       *b_tensor_scale (k % 256 == 0); a, b are packed E2M1 [m|n, k/2]
+ *   (NVFP4_ROW_1x16, NVFP4_1x16)              as above, row i of D times
+ *       a_tensor_scale[i] * *b_tensor_scale (per-token activation scale)
  * Other pairs return FP8BS_EUNSUPPORTED.  Scale layouts are those written
  * by fp8_quantize for the operand's own [rows, k] shape.  m, n > 0,
  * n % 8 == 0; a, b, d 16-byte aligned.  a_tensor_scale / b_tensor_scale:
- * device float32[1], NVFP4 only (else ignored, may be NULL).
+ * device float32[1], NVFP4 only (else ignored, may be NULL);
+ * a_tensor_scale is float32[m] for NVFP4_ROW_1x16.
  * workspace: required (status word for the bounded pipeline waits).
  */
 int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,

@@ -205,13 +205,14 @@ def nvfp4_block_sq_error(x, q, big_s_full, group: int = 16):
     decides is reproducible).  Returns [R, C/16] float32."""
     assert group == 16
     r, c = x.shape
-    y = (e2m1_decode(q).astype(F32) * big_s_full).astype(F32)
-    d = (x - y).astype(F32)
-    sq = (d * d).astype(F32).reshape(r, c // 16, 2, 8)
-    acc = sq[..., 0].copy()
-    for i in range(1, 8):
-        acc = (acc + sq[..., i]).astype(F32)
-    return (acc[..., 0] + acc[..., 1]).astype(F32)
+    with np.errstate(over="ignore"):      # squares of values near the float32 limit are +inf, as in IEEE
+        y = (e2m1_decode(q).astype(F32) * big_s_full).astype(F32)
+        d = (x - y).astype(F32)
+        sq = (d * d).astype(F32).reshape(r, c // 16, 2, 8)
+        acc = sq[..., 0].copy()
+        for i in range(1, 8):
+            acc = (acc + sq[..., i]).astype(F32)
+        return (acc[..., 0] + acc[..., 1]).astype(F32)
 
 
 def quantize_nvfp4(x: np.ndarray, group: int = 16, s_g=None, row_scaled: bool = False,

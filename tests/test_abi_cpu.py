@@ -85,3 +85,41 @@ def test_grouped_gemm_rejects_bad_arguments(lib):
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 200, 3, FAKE, FAKE, 16384, None) == -1   # k
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 256, 3, FAKE, None, 0, None) == -6
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 0, 128, 256, 3, FAKE, FAKE, 16384, None) == 0     # empty: no-op
+
+
+ODD4 = ctypes.c_void_p(0x10002)        # not 4-byte aligned
+
+
+def test_quantize_flags_and_row_scaled_nvfp4(lib):
+    q = lib.fp8_quantize
+    assert q(FAKE, 4, 128, 128, 4, FAKE, FAKE, FAKE, 4, FAKE, 16384, None) == -1   # unknown flag bit
+    assert q(FAKE, 4, 128, 128, 1, FAKE, FAKE, None, 2, None, 0, None) == -1       # 4over6 on 1x128
+    assert q(FAKE, 4, 128, 128, 7, FAKE, FAKE, None, 0, None, 0, None) == -1       # row S_g pointer missing
+    assert q(FAKE, 4, 120, 120, 7, FAKE, FAKE, FAKE, 0, None, 0, None) == -1       # cols % 16
+    assert q(FAKE, 4, 128, 128, 7, FAKE, FAKE, ODD4, 0, None, 0, None) == -2       # S_g alignment
+    assert q(FAKE, 4, 128, 128, 8, FAKE, FAKE, FAKE, 0, None, 0, None) == -1       # no gran 8
+    assert q(None, 0, 128, 128, 7, None, None, None, 2, None, 0, None) == 0        # empty: no-op
+    t = lib.fp8_quantize_transposed
+    assert t(FAKE, 32, 128, 128, 7, FAKE, FAKE, None, None, FAKE, 0, None, 0, None) == -3
+    assert t(FAKE, 32, 128, 128, 1, FAKE, FAKE, None, None, None, 2, None, 0, None) == -1
+
+
+def test_dequantize_rejects_bad_arguments(lib):
+    d = lib.fp8_dequantize
+    assert d(None, FAKE, None, 4, 128, 1, FAKE, 128, None) == -1                 # null q
+    assert d(FAKE, FAKE, None, 4, 124, 1, FAKE, 128, None) == -1                 # cols % 8
+    assert d(FAKE, FAKE, None, 4, 128, 1, FAKE, 120, None) == -1                 # ld_out < cols
+    assert d(FAKE, FAKE, None, 4, 128, 8, FAKE, 128, None) == -1                 # bad gran
+    assert d(FAKE, FAKE, None, 4, 128, 4, FAKE, 128, None) == -1                 # NVFP4 needs S_g
+    assert d(FAKE, FAKE, ODD4, 4, 128, 7, FAKE, 128, None) == -2                 # S_g alignment
+    assert d(ctypes.c_void_p(0x10004), FAKE, None, 4, 128, 1, FAKE, 128, None) == -2   # q 8-byte aligned
+    assert d(FAKE, FAKE, None, 4, 128, 1, MISALIGNED, 128, None) == -2           # out 16-byte aligned
+    assert d(None, None, None, 0, 128, 1, None, 128, None) == 0                  # empty: no-op
+
+
+def test_gemm_row_scaled_nvfp4_arguments(lib):
+    g = lib.fp8_block_gemm
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 7, FAKE, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -3  # B per row
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, None, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -1  # A S_g
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, ODD4, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -2
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, FAKE, 16384, None) == -1  # k % 256

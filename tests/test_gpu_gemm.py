@@ -67,6 +67,43 @@ def test_blockwise_modes_and_ragged_shapes(a_gran, b_gran, m, n, k):
     assert_gemm_close(bf16_to_f64(d), ref)
 
 
+@pytest.mark.parametrize("a_gran,b_gran", [("1x128", "128x128"), ("1x128", "1x128"), ("per_tensor", "128x128")])
+@pytest.mark.parametrize("m,n,k", [(2048, 2304, 640), (129, 8, 128)])
+def test_blockwise_partial_tiles(a_gran, b_gran, m, n, k):
+    """Several tiles per CTA with a ragged last row and column tile, and a
+    single row tile narrower than one N tile."""
+    ab = synth.activations((m, k), seed=m + 2 * k, outlier_frac=0.01, outlier_mult=50.0)
+    bb = synth.weights((n, k), seed=n + 3 * k, std=0.02)
+    d = gpu_block_gemm(ab, a_gran, bb, b_gran)
+    ref = OG.gemm_bf16(oracle_deq(to_f32(ab), a_gran), oracle_deq(to_f32(bb), b_gran))
+    assert_gemm_close(bf16_to_f64(d), ref)
+    assert fp.read_status() == 0
+
+
+def test_blockwise_grouped_ragged_experts():
+    """FP32-scale grouped GEMM with empty, one-row, ragged and multi-tile experts."""
+    counts = [0, 1, 127, 129, 0, 3, 256, 300]
+    n, k = 264, 384
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    rows, e = int(offsets[-1]), len(counts)
+    ab = synth.activations((rows, k), seed=77, outlier_frac=0.01, outlier_mult=50.0)
+    bb = synth.weights((e * n, k), seed=78)
+    qa, sa, _ = fp.fp8_quantize(to_dev_bf16(ab), "1x128")
+    qbs, sbs = [], []
+    for i in range(e):
+        q_, s_, _ = fp.fp8_quantize(to_dev_bf16(bb[i * n:(i + 1) * n]), "128x128")
+        qbs.append(q_); sbs.append(s_)
+    d = fp.fp8_grouped_gemm(qa, sa, torch.stack(qbs), torch.stack(sbs), torch.from_numpy(offsets).cuda(), "1x128")
+    got = bf16_to_f64(d)
+    a64 = oracle_deq(to_f32(ab), "1x128")
+    for i in range(e):
+        lo, hi = offsets[i], offsets[i + 1]
+        if hi > lo:
+            ref = OG.gemm_bf16(a64[lo:hi], oracle_deq(to_f32(bb[i * n:(i + 1) * n]), "128x128"))
+            assert_gemm_close(got[lo:hi], ref)
+    assert fp.read_status() == 0
+
+
 def test_blockwise_many_tiles_persistent():
     """More tiles than SMs: every CTA walks several tiles and K blocks."""
     m, n, k = 2048, 2304, 640
@@ -219,8 +256,8 @@ def test_moe_grouped_full_size_sampled():
 
 
 # ------------------------------------------------------------------ NVFP4
-def nv_deq(x_f32, s_g=None):
-    p, sb, sg = OQ.quantize_nvfp4(x_f32, s_g=s_g)
+def nv_deq(x_f32, s_g=None, **kw):
+    p, sb, sg = OQ.quantize_nvfp4(x_f32, s_g=s_g, **kw)
     return OG.dequant_nvfp4(p, sb, sg)
 
 
@@ -236,24 +273,56 @@ def test_nvfp4_dense(m, n, k):
     assert fp.read_status() == 0
 
 
-def test_nvfp4_full_size_sampled():
-    """Qwen2.5-32B MLP-shaped NVFP4 linear: X [16384,5120], W [27648,5120]."""
+@pytest.mark.parametrize("fos", [False, True])
+@pytest.mark.parametrize("m,n,k", [(128, 256, 256), (300, 520, 512), (1, 8, 256), (1000, 1024, 2048)])
+def test_nvfp4_row_scaled_activation(m, n, k, fos):
+    """Per-token outer scales on A (rows spanning six orders of magnitude),
+    one outer scale on B; optionally four-over-six block scales on both."""
+    ab = synth.activations((m, k), seed=m + 7, outlier_frac=0.01, outlier_mult=20.0)
+    mag = np.float32(10.0) ** np.random.Generator(np.random.PCG64(m)).integers(-3, 3, m).astype(np.float32)
+    af = to_f32(ab) * mag[:, None]
+    ab = synth.f32_to_bf16_bits(af)
+    bb = synth.weights((n, k), seed=n + 8)
+    flags = fp.FLAG_NVFP4_4OVER6 if fos else 0
+    qa, sa, ta = fp.fp8_quantize(to_dev_bf16(ab), "nvfp4_row", flags=flags)
+    qb, sb, tb = fp.fp8_quantize(to_dev_bf16(bb), "nvfp4", flags=flags)
+    assert ta.shape == (m,)
+    d = fp.fp8_block_gemm(qa, sa, "nvfp4_row", qb, sb, "nvfp4", ta, tb, k=k)
+    ref = OG.gemm_bf16(nv_deq(to_f32(ab), row_scaled=True, four_over_six=fos),
+                       nv_deq(to_f32(bb), four_over_six=fos))
+    # rows differ in scale by up to 1e5: compare each magnitude class on its own
+    got = bf16_to_f64(d)
+    for e in np.unique(mag):
+        sel = mag == e
+        assert_gemm_close(got[sel], ref[sel])
+    assert fp.read_status() == 0
+
+
+@pytest.mark.parametrize("form", ["nvfp4", "nvfp4_row+4o6"])
+def test_nvfp4_full_size_sampled(form):
+    """Qwen2.5-32B MLP-shaped NVFP4 linear: X [16384,5120], W [27648,5120];
+    one outer activation scale, or per-token outer scales with four-over-six."""
     m, n, k = 16384, 27648, 5120
+    a_gran, _, opt = form.partition("+")
+    fos = opt == "4o6"
+    flags = fp.FLAG_NVFP4_4OVER6 if fos else 0
     xb = synth.activations((m, k), seed=0, outlier_frac=0.0)
     wb = synth.weights((n, k), seed=1)
-    qa, sa, ta = fp.fp8_quantize(to_dev_bf16(xb), "nvfp4")
-    qb, sb, tb = fp.fp8_quantize(to_dev_bf16(wb), "nvfp4")
-    d = fp.fp8_block_gemm(qa, sa, "nvfp4", qb, sb, "nvfp4", ta, tb, k=k)
+    qa, sa, ta = fp.fp8_quantize(to_dev_bf16(xb), a_gran, flags=flags)
+    qb, sb, tb = fp.fp8_quantize(to_dev_bf16(wb), "nvfp4", flags=flags)
+    d = fp.fp8_block_gemm(qa, sa, a_gran, qb, sb, "nvfp4", ta, tb, k=k)
     torch.cuda.synchronize()
     assert fp.read_status() == 0
     xf, wf = to_f32(xb), to_f32(wb)
-    sg_x, sg_w = OQ.nvfp4_tensor_scale(xf), OQ.nvfp4_tensor_scale(wf)
-    assert float(ta.item()) == float(sg_x) and float(tb.item()) == float(sg_w)
+    row = a_gran == "nvfp4_row"
+    sg_x = OQ.nvfp4_row_scales(xf, fos) if row else OQ.nvfp4_tensor_scale(xf, fos)
+    sg_w = OQ.nvfp4_tensor_scale(wf, fos)
+    assert np.array_equal(ta.cpu().numpy(), np.atleast_1d(sg_x)) and float(tb.item()) == float(sg_w)
     g = np.random.Generator(np.random.PCG64(8))
     rows = np.sort(g.choice(m, 32, replace=False))
     cols = np.sort(g.choice(n, 512, replace=False))
-    a64 = nv_deq(xf[rows], s_g=sg_x)
-    b64 = nv_deq(wf[cols], s_g=sg_w)
+    a64 = nv_deq(xf[rows], s_g=sg_x[rows] if row else sg_x, row_scaled=row, four_over_six=fos)
+    b64 = nv_deq(wf[cols], s_g=sg_w, four_over_six=fos)
     got = bf16_to_f64(d[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
     assert_gemm_close(got, OG.gemm_bf16(a64, b64))
 

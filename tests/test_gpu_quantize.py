@@ -3,7 +3,9 @@
 Cases: the tiny blockwise-linear operands, the full 8192x4096 quantise
 sweep (every granularity, row-wise, transposed and dual outputs), ragged
 groups and tiles, strided input rows, empty input, all-zero and extreme
-magnitude tensors, and a sweep of every BF16 bit pattern.
+magnitude tensors, and a sweep of every BF16 bit pattern.  NVFP4 runs in
+four forms: one outer scale per tensor or per row, each with and without
+four-over-six block scales.
 """
 import numpy as np
 import pytest
@@ -37,17 +39,27 @@ def built():
     assert torch.cuda.is_available()
 
 
+def nv_form(gran):
+    """'nvfp4', 'nvfp4_row', optionally '+4o6': (library gran, flags, oracle kwargs)."""
+    base, _, opt = gran.partition("+")
+    fos = opt == "4o6"
+    return base, (fp.FLAG_NVFP4_4OVER6 if fos else 0), {"row_scaled": base == "nvfp4_row", "four_over_six": fos}
+
+
 def check_rowwise(bits, gran, x_dev=None):
     x = to_f32(bits)
     xd = x_dev if x_dev is not None else to_dev_bf16(bits)
+    if gran.startswith("nvfp4"):
+        base, flags, kw = nv_form(gran)
+        q, s, ts = fp.fp8_quantize(xd, base, flags=flags)
+        torch.cuda.synchronize()
+        pq, sb, sg = OQ.quantize_nvfp4(x, **kw)
+        assert np.array_equal(np_u8(q), pq), f"{gran}: {(np_u8(q) != pq).sum()} code bytes differ"
+        assert np.array_equal(np_u8(s), sb), f"{gran}: {(np_u8(s) != sb).sum()} block scales differ"
+        assert np.array_equal(np_f32(ts), np.atleast_1d(np.asarray(sg, dtype=np.float32)))
+        return
     q, s, ts = fp.fp8_quantize(xd, gran)
     torch.cuda.synchronize()
-    if gran == "nvfp4":
-        pq, sb, sg = OQ.quantize_nvfp4(x)
-        assert np.array_equal(np_u8(q), pq)
-        assert np.array_equal(np_u8(s), sb)
-        assert np_f32(ts)[0] == sg
-        return
     rq, rs = ROW_ORACLE[gran](x)
     assert np.array_equal(np_u8(q), rq), f"{gran}: {(np_u8(q) != rq).sum()} codes differ"
     if gran in BYTE_SCALES:
@@ -77,6 +89,7 @@ def check_transposed(bits, gran, dual):
 
 
 GRANS = ["per_tensor", "1x128", "128x128", "mxfp8", "1x128_pow2", "128x128_pow2"]
+NV = ["nvfp4", "nvfp4_row", "nvfp4+4o6", "nvfp4_row+4o6"]
 
 
 # -------------------------------------------------------------- tiny blockwise linear operands
@@ -93,7 +106,7 @@ def sweep_bits():
     return synth.activations((8192, 4096), seed=0, outlier_frac=0.001, outlier_mult=100.0)
 
 
-@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+@pytest.mark.parametrize("gran", GRANS + NV)
 def test_sweep_rowwise(sweep_bits, gran):
     check_rowwise(sweep_bits, gran)
 
@@ -104,10 +117,10 @@ def test_sweep_transposed_dual(sweep_bits, gran):
 
 
 # -------------------------------------------------------------- shapes and edge cases
-@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
-@pytest.mark.parametrize("shape", [(1, 16), (3, 200), (130, 264), (257, 1032), (64, 4096)])
+@pytest.mark.parametrize("gran", GRANS + NV)
+@pytest.mark.parametrize("shape", [(1, 16), (3, 200), (130, 264), (257, 1032), (64, 4096), (5, 5136)])
 def test_ragged_rowwise(gran, shape):
-    if gran == "nvfp4" and shape[1] % 16:
+    if gran.startswith("nvfp4") and shape[1] % 16:
         pytest.skip("NVFP4 needs cols % 16")
     bits = synth.activations(shape, seed=sum(shape), outlier_frac=0.02, outlier_mult=80.0)
     check_rowwise(bits, gran)
@@ -121,7 +134,7 @@ def test_ragged_transposed(gran, dual, shape):
     check_transposed(bits, gran, dual)
 
 
-@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+@pytest.mark.parametrize("gran", GRANS + NV)
 def test_strided_rows(gran):
     bits = synth.activations((96, 384), seed=5)
     big = torch.zeros((96, 512), dtype=torch.bfloat16, device="cuda")
@@ -129,7 +142,7 @@ def test_strided_rows(gran):
     check_rowwise(bits, gran, x_dev=big[:, :384])
 
 
-@pytest.mark.parametrize("gran", GRANS + ["nvfp4"])
+@pytest.mark.parametrize("gran", GRANS + NV)
 def test_zero_and_extreme_tensors(gran):
     zeros = np.zeros((64, 256), dtype=np.uint16)
     zeros[3, 7] = 0x8000                                   # a negative zero
@@ -151,7 +164,7 @@ def test_every_bf16_pattern():
     perm = finite[g.permutation(finite.size)]
     n = (perm.size // 512) * 512
     bits = perm[:n].reshape(-1, 512)
-    for gran in GRANS + ["nvfp4"]:
+    for gran in GRANS + NV:
         check_rowwise(bits, gran)
     # every pattern with |x| <= 448 under a scale of exactly 1 (amax 448 in every group)
     small = finite[(finite & 0x7FFF) <= 0x43E0]
@@ -179,3 +192,60 @@ def test_given_tensor_scale():
     pq, sb, _ = fp.fp8_quantize(xd, "nvfp4", tensor_scale=sg, flags=fp.FLAG_GIVEN_TENSOR_SCALE)
     rq, rsb, _ = OQ.quantize_nvfp4(x, s_g=np.float32(0.01))
     assert np.array_equal(np_u8(pq), rq) and np.array_equal(np_u8(sb), rsb)
+
+
+def test_given_row_scales_and_shared_gate_up_scale():
+    """Per-row outer scales supplied by the caller; and gate and up weights
+    quantised separately with one shared outer scale equal the quantisation
+    of their concatenation (one outer weight scale for the fused GEMM)."""
+    bits = synth.activations((48, 256), seed=13, outlier_frac=0.02, outlier_mult=30.0)
+    x = to_f32(bits)
+    xd = to_dev_bf16(bits)
+    g = np.random.Generator(np.random.PCG64(14))
+    rs = (g.uniform(0.5, 2.0, 48) * 0.01).astype(np.float32)
+    for flags, fos in ((0, False), (fp.FLAG_NVFP4_4OVER6, True)):
+        ts = torch.from_numpy(rs.copy()).cuda()
+        pq, sb, _ = fp.fp8_quantize(xd, "nvfp4_row", tensor_scale=ts, flags=flags | fp.FLAG_GIVEN_TENSOR_SCALE)
+        rq, rsb, _ = OQ.quantize_nvfp4(x, s_g=rs, row_scaled=True, four_over_six=fos)
+        assert np.array_equal(np_u8(pq), rq) and np.array_equal(np_u8(sb), rsb)
+        assert np.array_equal(np_f32(ts), rs)                      # an input: left untouched
+    gate = synth.weights((96, 256), seed=15)
+    up = synth.weights((96, 256), seed=16, std=0.05)
+    both = np.concatenate([gate, up])
+    for flags, fos in ((0, False), (fp.FLAG_NVFP4_4OVER6, True)):
+        qc, sc, tc = fp.fp8_quantize(to_dev_bf16(both), "nvfp4", flags=flags)
+        shared = tc.clone()
+        qg, sg_, _ = fp.fp8_quantize(to_dev_bf16(gate), "nvfp4", tensor_scale=shared.clone(),
+                                     flags=flags | fp.FLAG_GIVEN_TENSOR_SCALE)
+        qu, su, _ = fp.fp8_quantize(to_dev_bf16(up), "nvfp4", tensor_scale=shared.clone(),
+                                    flags=flags | fp.FLAG_GIVEN_TENSOR_SCALE)
+        assert torch.equal(torch.cat([qg, qu]), qc) and torch.equal(torch.cat([sg_, su]), sc)
+        _, _, rsg = OQ.quantize_nvfp4(to_f32(both), four_over_six=fos)
+        assert np_f32(tc)[0] == rsg
+
+
+def test_nvfp4_full_size_activation_rows():
+    """The 16384 x 5120 NVFP4 activation of the dense FP4 linear, per-row and
+    per-tensor outer scales, with and without four-over-six: every outer
+    scale, and all codes of sampled rows (the oracle quantises just those
+    rows; a row's result depends only on the row and the outer scale)."""
+    bits = synth.activations((16384, 5120), seed=5, outlier_frac=0.01, outlier_mult=50.0)
+    xd = to_dev_bf16(bits)
+    rows = np.unique(np.concatenate([[0, 1, 16383], np.random.Generator(np.random.PCG64(6)).integers(0, 16384, 60)]))
+    x_all = to_f32(bits)
+    x_s = x_all[rows]
+    for gran in NV:
+        base, flags, kw = nv_form(gran)
+        q, s, ts = fp.fp8_quantize(xd, base, flags=flags)
+        torch.cuda.synchronize()
+        if kw["row_scaled"]:
+            sg_all = OQ.nvfp4_row_scales(x_all, kw["four_over_six"])
+            assert np.array_equal(np_f32(ts), sg_all)
+            sg_s = sg_all[rows]
+        else:
+            sg_s = OQ.nvfp4_tensor_scale(x_all, kw["four_over_six"])
+            assert np_f32(ts)[0] == sg_s
+        rq, rsb, _ = OQ.quantize_nvfp4(x_s, s_g=sg_s, **kw)
+        idx = torch.from_numpy(rows).cuda()
+        assert np.array_equal(np_u8(q.index_select(0, idx)), rq)
+        assert np.array_equal(np_u8(s.index_select(0, idx)), rsb)
