@@ -22,10 +22,18 @@
 //               kind::f8f6f4 (M128 N256 K32) per K block into partial
 //               buffer kb & 1, then tcgen05.commit to free the stage and to
 //               publish the partial.
-//   warps 2-3   idle (complete the producer warpgroup)
+//   warp 2      scale loader: for each group of 4 K blocks of a tile, the
+//               128 row scales of A and the 256 column scales of B, read as
+//               16-byte runs (4 K blocks of one row / column) and stored
+//               transposed ([K block][row], [K block][column]) into a 2-slot
+//               shared-memory ring.  The per-column B scales of the 1x128
+//               mode would otherwise cost every epilogue warp one scattered
+//               load per column per K block.
+//   warp 3      idle (completes the producer warpgroup)
 //   warps 4..11 epilogue: warp w reads TMEM lanes 32*(w%4).. (one D row per
 //               thread) and columns 128*((w-4)/4).. (one 128-column half);
-//               acc += partial * sa * sb, BF16 store at the end of the tile.
+//               acc += partial * sa * sb with both scales read from the
+//               ring, BF16 store at the end of the tile.
 // Scale modes (template): 0 per-tensor, 1 per row (1x128), 2 per 128-row block.
 #include <algorithm>
 
@@ -39,6 +47,8 @@ namespace fp8bs {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int SG = 4;          // K blocks per scale group
+constexpr int SRING = 2;       // scale groups in flight
 constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
@@ -57,22 +67,39 @@ struct Params {
 };
 
 struct alignas(16) Shared {
-    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    float sa[SRING][SG][BM];   // A scale of each tile row, per K block of the group
+    float sb[SRING][SG][BN];   // B scale of each tile column (modes 0 / 2: entries 0 and 128 only)
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], sfull[SRING], sempty[SRING], drain;
     uint32_t tmem_base;
     int abort;
-    float sbuf[8][2][128];
     SchedShared sched;
 };
 
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
 
-template <int MODE>
-__device__ __forceinline__ float a_scale(const float* __restrict__ sa, int64_t row, int64_t row_end, int64_t nkb,
-                                         int64_t kb) {
-    if (MODE == 0) return __ldg(sa);
-    if (row >= row_end) return 0.0f;
-    if (MODE == 1) return __ldg(sa + row * nkb + kb);
-    return __ldg(sa + (row >> 7) * nkb + kb);
+// Four consecutive K-block scales starting at kb0 from a row of `nkb` FP32
+// scales (zero past the row's end); one 16-byte load when `vec`.
+__device__ __forceinline__ float4 scales4(const float* __restrict__ src, int64_t kb0, int64_t nkb, bool vec) {
+    if (vec) return __ldg(reinterpret_cast<const float4*>(src + kb0));
+    float4 v;
+    v.x = __ldg(src + kb0);
+    v.y = (kb0 + 1 < nkb) ? __ldg(src + kb0 + 1) : 0.0f;
+    v.z = (kb0 + 2 < nkb) ? __ldg(src + kb0 + 2) : 0.0f;
+    v.w = (kb0 + 3 < nkb) ? __ldg(src + kb0 + 3) : 0.0f;
+    return v;
+}
+
+__device__ __forceinline__ void put4(float (*dst)[BN], int idx, float4 v) {
+    dst[0][idx] = v.x;
+    dst[1][idx] = v.y;
+    dst[2][idx] = v.z;
+    dst[3][idx] = v.w;
+}
+__device__ __forceinline__ void put4a(float (*dst)[BM], int idx, float4 v) {
+    dst[0][idx] = v.x;
+    dst[1][idx] = v.y;
+    dst[2][idx] = v.z;
+    dst[3][idx] = v.w;
 }
 
 template <int SA_MODE, int SB_MODE>
@@ -94,6 +121,10 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&sh->tfull[b]), 1);
             mbar_init(smem_u32(&sh->tempty[b]), 8);
+        }
+        for (int g = 0; g < SRING; ++g) {
+            mbar_init(smem_u32(&sh->sfull[g]), 32);    // every loader lane arrives
+            mbar_init(smem_u32(&sh->sempty[g]), 8);    // every epilogue warp arrives
         }
         mbar_init(smem_u32(&sh->drain), 1);
         sh->abort = 0;
@@ -169,6 +200,66 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             mbar_wait(smem_u32(&sh->drain), 0, abort, p.status);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale loader
+        const bool vec_a = SA_MODE == 1 && (nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(p.sa) & 15u) == 0;
+        const bool vec_b = SB_MODE == 1 && (nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(p.sb) & 15u) == 0;
+        const float sa0 = (SA_MODE == 0) ? __ldg(p.sa) : 0.0f;
+        uint32_t gg = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const float* sb_e = p.sb;
+            if (p.experts) {
+                const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
+                sb_e = p.sb + (int64_t)ti.expert * per;
+            }
+            for (int64_t kb0 = 0; kb0 < nkb; kb0 += SG, ++gg) {
+                const uint32_t g = gg % SRING, ph = (gg / SRING) & 1;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&sh->sempty[g]), ph ^ 1, abort, p.status, p.wait_ns))) {
+                    ok = false;
+                    break;
+                }
+                float4 va[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t row = ti.row0 + lane + 32 * i;
+                    if (SA_MODE == 0) va[i] = make_float4(sa0, sa0, sa0, sa0);
+                    else if (row >= ti.row_end) va[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    else if (SA_MODE == 1) va[i] = scales4(p.sa + row * nkb, kb0, nkb, vec_a);
+                    else va[i] = scales4(p.sa + (row >> 7) * nkb, kb0, nkb, false);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) put4a(sh->sa[g], lane + 32 * i, va[i]);
+                if (SB_MODE == 1) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float4 vb[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t col = ti.n0 + lane + 32 * (4 * half + i);
+                            vb[i] = (col < p.n) ? scales4(sb_e + col * nkb, kb0, nkb, vec_b) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) put4(sh->sb[g], lane + 32 * (4 * half + i), vb[i]);
+                    }
+                } else if (lane < 2) {
+                    const int64_t col = ti.n0 + 128 * lane;
+                    float4 vb = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (col < p.n) {
+                        if (SB_MODE == 0) {
+                            const float s0 = __ldg(sb_e);
+                            vb = make_float4(s0, s0, s0, s0);
+                        } else {
+                            vb = scales4(sb_e + (col >> 7) * nkb, kb0, nkb, false);
+                        }
+                    }
+                    put4(sh->sb[g], 128 * lane, vb);
+                }
+                mbar_arrive(smem_u32(&sh->sfull[g]));
+            }
+        }
+        __syncwarp();
     }
     } else {
         setmaxnreg_inc<216>();
@@ -177,73 +268,32 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int h = ew >> 2;           // 128-column half of the tile
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        float* sbuf0 = sh->sbuf[ew][0];
-        float* sbuf1 = sh->sbuf[ew][1];
-        uint32_t kbg = 0;
+        uint32_t kbg = 0, gg = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
-            const float* sb_e = p.sb;
-            if (p.experts) {
-                const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
-                sb_e = p.sb + (int64_t)ti.expert * per;
-            }
             uint64_t acc[64];   // FP32 pairs: columns (2j, 2j+1) of this thread's 128-column half
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0ull;
 
-            // Scales run PD K blocks ahead of their use in a register ring, so
-            // the L2 latency of these small scattered loads stays off the
-            // per-K-block critical path.
-            constexpr int PD = 4;
-            float fa_r[PD], fb_r[PD];
-            float4 fv_r[PD];
-#define FP8BS_LOAD_SCALES(D, KB)                                                                      \
-    do {                                                                                              \
-        fa_r[D] = a_scale<SA_MODE>(p.sa, row, ti.row_end, nkb, (KB));                                 \
-        if (SB_MODE == 0) {                                                                           \
-            fb_r[D] = __ldg(sb_e);                                                                    \
-        } else if (SB_MODE == 2) {                                                                    \
-            fb_r[D] = (col0 < p.n) ? __ldg(sb_e + (col0 >> 7) * nkb + (KB)) : 0.0f;                   \
-        } else {                                                                                      \
-            const int64_t c_ = col0 + 4 * lane;                                                       \
-            fv_r[D].x = (c_ + 0 < p.n) ? __ldg(sb_e + (c_ + 0) * nkb + (KB)) : 0.0f;                  \
-            fv_r[D].y = (c_ + 1 < p.n) ? __ldg(sb_e + (c_ + 1) * nkb + (KB)) : 0.0f;                  \
-            fv_r[D].z = (c_ + 2 < p.n) ? __ldg(sb_e + (c_ + 2) * nkb + (KB)) : 0.0f;                  \
-            fv_r[D].w = (c_ + 3 < p.n) ? __ldg(sb_e + (c_ + 3) * nkb + (KB)) : 0.0f;                  \
-        }                                                                                             \
-    } while (0)
-#pragma unroll
-            for (int d = 0; d < PD; ++d) {
-                fa_r[d] = fb_r[d] = 0.0f;
-                fv_r[d] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (d < nkb) FP8BS_LOAD_SCALES(d, d);
-            }
-
             for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
-                const float fa = fa_r[0];
-                const float fb = fb_r[0];
-                if (SB_MODE == 1) {
-                    float* buf = (kb & 1) ? sbuf1 : sbuf0;
-                    reinterpret_cast<float4*>(buf)[lane] = fv_r[0];
+                const uint32_t g = gg % SRING, kk = (uint32_t)(kb & (SG - 1));
+                if (kk == 0) {
+                    const bool got_s = mbar_wait(smem_u32(&sh->sfull[g]), (gg / SRING) & 1, abort, p.status, p.wait_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got_s)) { ok = false; break; }
                 }
-#pragma unroll
-                for (int d = 0; d + 1 < PD; ++d) {
-                    fa_r[d] = fa_r[d + 1];
-                    fb_r[d] = fb_r[d + 1];
-                    fv_r[d] = fv_r[d + 1];
-                }
-                if (kb + PD < nkb) FP8BS_LOAD_SCALES(PD - 1, kb + PD);
-                __syncwarp();
+                const float fa = sh->sa[g][kk][32 * q + lane];
+                const float* sbk = &sh->sb[g][kk][128 * h];
                 const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
                 const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
                 if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }   // tcgen05.ld is .sync.aligned
                 tc_fence_after();
+                const float fb = (SB_MODE == 1) ? 0.0f : sbk[0];
                 const uint64_t f2 = f2_pack(fa * fb, fa * fb);
                 const uint64_t fa2 = f2_pack(fa, fa);
-                const float4* buf4 = reinterpret_cast<const float4*>((kb & 1) ? sbuf1 : sbuf0);
+                const float4* buf4 = reinterpret_cast<const float4*>(sbk);
                 const uint32_t taddr = tmem + lane_base + b * BN + 128 * h;
                 // Promote one 16-column chunk held in r: acc += partial * scale.
                 auto promote = [&](const uint32_t* r, int c) {
@@ -282,8 +332,13 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                         promote(rb, c + 1);
                     }
                 }
+                if (kk == SG - 1 || kb + 1 == nkb) {
+                    // this warp's last read of the scale group: hand the slot back to the loader
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh->sempty[g]));
+                    ++gg;
+                }
             }
-#undef FP8BS_LOAD_SCALES
             if (!ok) break;
             // BF16 store of this thread's row: 128 columns = 16 x 16 bytes
             if (row < ti.row_end) {

@@ -186,10 +186,12 @@ __device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s) {
 __device__ __forceinline__ float half_sq_err(const float* f, uint32_t packed, float big_s) {
     float acc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float d = __fsub_rn(f[i], __fmul_rn(e2m1_value((packed >> (4 * i)) & 0xFu), big_s));
-        const float sq = __fmul_rn(d, d);
-        acc = (i == 0) ? sq : __fadd_rn(acc, sq);
+    for (int k = 0; k < 4; ++k) {
+        const float2 e = e2m1x2_to_float2((packed >> (8 * k)) & 0xFFu);
+        const float d0 = __fsub_rn(f[2 * k], __fmul_rn(e.x, big_s));
+        const float d1 = __fsub_rn(f[2 * k + 1], __fmul_rn(e.y, big_s));
+        acc = (k == 0) ? __fmul_rn(d0, d0) : __fadd_rn(acc, __fmul_rn(d0, d0));
+        acc = __fadd_rn(acc, __fmul_rn(d1, d1));
     }
     return acc;
 }
