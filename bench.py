@@ -612,7 +612,22 @@ def e2e_bench(torch, fp, dev, step, reps=8):
         if t_end is not None:
             t_end.record(s_out)
 
+    # the host link on its own: one step's input copy, then one step's output copy
+    def copy_gbs(pairs, stream, n=3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        nbytes = n * sum(src.numel() * src.element_size() for _, src in pairs)
+        return round(nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+
     torch.cuda.synchronize()
+    h2d_gbs = copy_gbs([(d, h) for h, d in zip((hx, hw, hdy), (step.x, step.w, step.dy))], s_in)
+    d2h_gbs = copy_gbs([(h, d) for h, d in zip(hout[0], (step.y, step.dx, step.dw))], s_out)
     run(2)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -624,7 +639,8 @@ def e2e_bench(torch, fp, dev, step, reps=8):
     d2h = sum(t.numel() * t.element_size() for t in hout[0])
     return {"value": round(STEP_FLOP / (ms * 1e-3) / 1e12, 1), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "pipeline": "2 buffer sets; H2D, compute and D2H on separate streams"}
+            "pipeline": "2 buffer sets; H2D, compute and D2H on separate streams",
+            "host_link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
 if __name__ == "__main__":

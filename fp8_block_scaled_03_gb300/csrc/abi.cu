@@ -130,6 +130,7 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
     j.q = static_cast<uint8_t*>(q); j.s = scales;
     j.given_scale = (flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE) != 0;
     j.partials = workspace ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kPartialsOffset) : nullptr;
+    j.status = (workspace != nullptr && workspace_bytes >= kWorkspaceBytes) ? static_cast<int*>(workspace) : nullptr;
     return cuda_status(launch_quantize_transposed(j, reinterpret_cast<cudaStream_t>(stream)));
 }
 

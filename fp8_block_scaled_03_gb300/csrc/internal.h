@@ -27,6 +27,7 @@ struct QuantJob {
     bool given_scale;
     bool four_over_six; // NVFP4: four-over-six block scales
     uint32_t* partials; // amax partials (per-tensor / NVFP4)
+    int* status;        // sticky status word of the workspace, or null
 };
 int launch_quantize(const QuantJob& j, cudaStream_t s);
 int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);

@@ -13,8 +13,12 @@
 // 128x128 and transposed kernels: one CTA per 128x128 tile, the tile held
 // in registers (16 rows x 4 columns per thread), per-column partial amaxes
 // combined through shared memory.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
 
 namespace fp8bs {
 
@@ -343,24 +347,28 @@ quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     }
 }
 
-// ---------------------------------------------------------------- transposed (+ optional row-wise)
-// CTA tile: 128 rows x 128 columns of X, 512 threads.  Warp w owns rows
-// 8w..8w+7, lane l owns columns 4l..4l+3 (8-byte loads, 256 bytes per warp
-// and row).  Column amaxes are combined through shared memory.  The codes
-// of X^T are staged in shared memory as a [column][row] byte tile (row pitch
-// 136 bytes, so the 8-byte stores of one warp spread over all banks) and
-// leave as whole 128-byte rows of X^T; the optional row-wise codes of X
-// leave straight from registers as 4-byte runs (128 bytes per warp and row).
-constexpr int kTileThreads = 512;
+// ---------------------------------------------------------------- transposed, one scale per tile
+// Per-tensor, 128x128 and 128x128 with power-of-two scales: one scale covers
+// the whole 128x128 tile, so the codes of X and of X^T are the same numbers.
+// CTA tile: 128 rows x 128 columns of X, 512 threads, two CTAs per SM, the
+// tile held in registers.  Warp w owns rows 8w..8w+7, lane l owns columns
+// 4l..4l+3 (8-byte loads, 256 bytes per warp and row).  The codes of X^T are
+// staged in shared memory as a [column][row] byte tile (row pitch 136 bytes,
+// so the 8-byte stores of one warp spread over all banks) and leave as whole
+// 128-byte rows of X^T; the row-wise codes of X (dual mode) are computed
+// again from the registers and leave as 4-byte runs (128 bytes per warp and
+// row).  On GB300 this
+// kernel is faster than the TMA-fed one below for these granularities.
+constexpr int kRegTileThreads = 512;
 constexpr int kTPitch = 136;
 
 template <int GRAN, bool DUAL>
-__global__ void __launch_bounds__(kTileThreads, 2)
-quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-                    uint8_t* __restrict__ qt, void* __restrict__ st,
-                    uint8_t* __restrict__ q, void* __restrict__ s,
-                    const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
-    __shared__ uint32_t red[16][128];
+__global__ void __launch_bounds__(kRegTileThreads, 2)
+quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                      uint8_t* __restrict__ qt, void* __restrict__ st,
+                      uint8_t* __restrict__ q, void* __restrict__ s,
+                      const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
+    static_assert(GRAN == kGranPT || GRAN == kGranBlk || GRAN == kGranBlkP2, "one scale per tile only");
     __shared__ __align__(16) uint8_t tq[128 * kTPitch];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t rt = blockIdx.y, ct = blockIdx.x;
@@ -370,15 +378,16 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
     const int64_t rw = r0 + 8 * w;           // first row of this warp
     const bool wok = rw < rows;              // rows % 16 == 0: 8 rows all valid or all not
 
-    float s_uniform = 1.0f;
+    float sc = 1.0f;                         // divisor (FP32 scales) or multiplier (power of two)
+    int e_blk = 0;
     if constexpr (GRAN == kGranPT) {
         if (given != nullptr) {
-            s_uniform = *given;
+            sc = *given;
         } else {
-            s_uniform = fp32_scale_from_amax(tensor_amax(partials, nparts));
+            sc = fp32_scale_from_amax(tensor_amax(partials, nparts));
             if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-                static_cast<float*>(st)[0] = s_uniform;
-                if (DUAL) static_cast<float*>(s)[0] = s_uniform;
+                static_cast<float*>(st)[0] = sc;
+                if (DUAL) static_cast<float*>(s)[0] = sc;
             }
         }
     }
@@ -388,54 +397,20 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
     for (int i = 0; i < 8; ++i)
         v[i] = (cok && wok) ? ldg_v2(x + (rw + i) * ldx + cc) : make_uint2(0, 0);
 
-    uint32_t cm[4] = {0, 0, 0, 0};
+    if constexpr (GRAN == kGranBlk || GRAN == kGranBlkP2) {
+        uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        cm[0] = max(cm[0], v[i].x & 0x7FFFu);
-        cm[1] = max(cm[1], (v[i].x >> 16) & 0x7FFFu);
-        cm[2] = max(cm[2], v[i].y & 0x7FFFu);
-        cm[3] = max(cm[3], (v[i].y >> 16) & 0x7FFFu);
-    }
-
-    float col_s[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // divisor (FP32 grans) or multiplier (power-of-two grans)
-    int col_e[4] = {0, 0, 0, 0};
-    float s_blk = 1.0f;
-    int e_blk = 0;
-    if constexpr (GRAN == kGranTok || GRAN == kGranMx || GRAN == kGranTokP2) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) red[w][lane * 4 + j] = cm[j];
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t m = 0;
-            if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) m = max(m, red[k][lane * 4 + j]);
-                if constexpr (GRAN == kGranTok) {
-                    col_s[j] = fp32_scale_from_amax(amax_bits_to_f32(m));
-                } else {
-                    col_e[j] = mx_exponent_from_amax_bits(m << 16);
-                    col_s[j] = exp2_neg(col_e[j]);
-                }
-            } else {
-                const int g = w & ~3;            // 32 rows = 4 warps
-#pragma unroll
-                for (int k = 0; k < 4; ++k) m = max(m, red[g + k][lane * 4 + j]);
-                col_e[j] = mx_exponent_from_amax_bits(m << 16);
-                col_s[j] = exp2_neg(col_e[j]);
-            }
-        }
-    } else if constexpr (GRAN == kGranBlk || GRAN == kGranBlkP2) {
-        const uint32_t bm = block_max_u32(max(max(cm[0], cm[1]), max(cm[2], cm[3])));
+        for (int i = 0; i < 8; ++i) m = max(m, max(bf16x2_absmax_bits(v[i].x), bf16x2_absmax_bits(v[i].y)));
+        const uint32_t bm = block_max_u32(m);
         if constexpr (GRAN == kGranBlk) {
-            s_blk = fp32_scale_from_amax(amax_bits_to_f32(bm));
+            sc = fp32_scale_from_amax(amax_bits_to_f32(bm));
         } else {
             e_blk = mx_exponent_from_amax_bits(bm << 16);
-            s_blk = exp2_neg(e_blk);
+            sc = exp2_neg(e_blk);
         }
     }
 
-    // ---- transposed codes: column cc + j, rows rw .. rw+7 -> shared tile
+    // ---- codes of column cc + j, rows rw .. rw+7 -> shared [column][row] tile
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float f[8];
@@ -444,14 +419,13 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
             const uint32_t word = (j < 2) ? v[i].x : v[i].y;
             f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
         }
-        const float d = (GRAN == kGranPT) ? s_uniform : ((GRAN == kGranBlk || GRAN == kGranBlkP2) ? s_blk : col_s[j]);
         uint2 o;
         if constexpr (kPow2<GRAN>) {
-            o.x = e4m3x4(__fmul_rn(f[0], d), __fmul_rn(f[1], d), __fmul_rn(f[2], d), __fmul_rn(f[3], d));
-            o.y = e4m3x4(__fmul_rn(f[4], d), __fmul_rn(f[5], d), __fmul_rn(f[6], d), __fmul_rn(f[7], d));
+            o.x = e4m3x4(__fmul_rn(f[0], sc), __fmul_rn(f[1], sc), __fmul_rn(f[2], sc), __fmul_rn(f[3], sc));
+            o.y = e4m3x4(__fmul_rn(f[4], sc), __fmul_rn(f[5], sc), __fmul_rn(f[6], sc), __fmul_rn(f[7], sc));
         } else {
-            o.x = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
-            o.y = e4m3x4(__fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
+            o.x = e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc));
+            o.y = e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc));
         }
         *reinterpret_cast<uint2*>(tq + (lane * 4 + j) * kTPitch + 8 * w) = o;
     }
@@ -459,7 +433,7 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
     // ---- whole rows of X^T: 128 columns x 128 bytes, 16 bytes per thread and pass
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
-        const int t = threadIdx.x + pass * kTileThreads;
+        const int t = threadIdx.x + pass * kRegTileThreads;
         const int qc = t >> 3, k = t & 7;    // column of X (row of X^T), 16-byte chunk
         const int64_t c = c0 + qc;
         if (c < cols && r0 + 16 * k < rows) {
@@ -469,66 +443,278 @@ quant_tile_t_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, 
             *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) = make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
     }
-    // ---- scales of X^T ([cols, *] grid)
-    if constexpr (GRAN == kGranTok) {
-        if (w == 0 && cok) {
-            const int64_t nrb = ceil_div(rows, 128);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) static_cast<float*>(st)[(cc + j) * nrb + rt] = col_s[j];
-        }
-    } else if constexpr (GRAN == kGranMx) {
-        if ((w & 3) == 0 && cok && wok) {
-            const int64_t nrb = ceil_div(rows, 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) static_cast<uint8_t*>(st)[(cc + j) * nrb + (rw >> 5)] = (uint8_t)(col_e[j] + 127);
-        }
-    } else if constexpr (GRAN == kGranTokP2) {
-        if (w == 0 && cok) {
-            const int64_t nrb = ceil_div(rows, 128);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) static_cast<uint8_t*>(st)[(cc + j) * nrb + rt] = (uint8_t)(col_e[j] + 127);
-        }
-    } else if constexpr (GRAN == kGranBlk) {
-        if (threadIdx.x == 0) static_cast<float*>(st)[ct * gridDim.y + rt] = s_blk;
+    if constexpr (GRAN == kGranBlk) {
+        if (threadIdx.x == 0) static_cast<float*>(st)[ct * gridDim.y + rt] = sc;
     } else if constexpr (GRAN == kGranBlkP2) {
         if (threadIdx.x == 0) static_cast<uint8_t*>(st)[ct * gridDim.y + rt] = (uint8_t)(e_blk + 127);
     }
 
     // ---- row-wise codes of X from the same registers
     if constexpr (DUAL) {
-        const int64_t ncb = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float f[4] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y)};
-            const uint32_t m4 = max(bf16x2_absmax_bits(v[i].x), bf16x2_absmax_bits(v[i].y));
-            uint32_t o;
-            if constexpr (GRAN == kGranTok) {
-                const float sr = fp32_scale_from_amax(amax_bits_to_f32(warp_max_u32(m4, 32)));
-                o = e4m3x4(__fdiv_rn(f[0], sr), __fdiv_rn(f[1], sr), __fdiv_rn(f[2], sr), __fdiv_rn(f[3], sr));
-                if (lane == 0 && wok) static_cast<float*>(s)[(rw + i) * ncb + ct] = sr;
-            } else if constexpr (GRAN == kGranMx) {
-                const int e = mx_exponent_from_amax_bits(warp_max_u32(m4, 8) << 16);
-                const float mm = exp2_neg(e);
-                o = e4m3x4(__fmul_rn(f[0], mm), __fmul_rn(f[1], mm), __fmul_rn(f[2], mm), __fmul_rn(f[3], mm));
-                if ((lane & 7) == 0 && cok && wok) static_cast<uint8_t*>(s)[(rw + i) * ncb + (cc >> 5)] = (uint8_t)(e + 127);
-            } else if constexpr (GRAN == kGranTokP2) {
-                const int e = mx_exponent_from_amax_bits(warp_max_u32(m4, 32) << 16);
-                const float mm = exp2_neg(e);
-                o = e4m3x4(__fmul_rn(f[0], mm), __fmul_rn(f[1], mm), __fmul_rn(f[2], mm), __fmul_rn(f[3], mm));
-                if (lane == 0 && wok) static_cast<uint8_t*>(s)[(rw + i) * ncb + ct] = (uint8_t)(e + 127);
-            } else if constexpr (GRAN == kGranBlkP2) {
-                o = e4m3x4(__fmul_rn(f[0], s_blk), __fmul_rn(f[1], s_blk), __fmul_rn(f[2], s_blk), __fmul_rn(f[3], s_blk));
-            } else {
-                const float d = (GRAN == kGranPT) ? s_uniform : s_blk;
-                o = e4m3x4(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d));
-            }
+            const float f0 = bf16_lo(v[i].x), f1 = bf16_hi(v[i].x), f2 = bf16_lo(v[i].y), f3 = bf16_hi(v[i].y);
+            const uint32_t o = kPow2<GRAN> ? e4m3x4(__fmul_rn(f0, sc), __fmul_rn(f1, sc), __fmul_rn(f2, sc), __fmul_rn(f3, sc))
+                                           : e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc), __fdiv_rn(f3, sc));
             if (cok && wok) *reinterpret_cast<uint32_t*>(q + (rw + i) * cols + cc) = o;
         }
         if constexpr (GRAN == kGranBlk) {
-            if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = s_blk;
+            if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = sc;
         } else if constexpr (GRAN == kGranBlkP2) {
             if (threadIdx.x == 0) static_cast<uint8_t*>(s)[rt * gridDim.x + ct] = (uint8_t)(e_blk + 127);
         }
+    }
+}
+
+// ---------------------------------------------------------------- transposed (+ optional row-wise), TMA-fed
+// 1x128, 1x128 with power-of-two scales, and MXFP8: a scale per column of X
+// (per row of X^T) and another per row of X.
+// Persistent CTAs of 256 threads, three per SM.  A 2-stage ring of 128x128
+// BF16 tiles (32 KB each) per CTA is filled by TMA ahead of the compute, so the
+// loads of later tiles are in flight while a tile is quantised.  Per tile:
+//   column pass (codes of X^T): thread t owns columns 2(t%64), 2(t%64)+1 and
+//     rows 32(t/64) .. +31 -- 4-byte reads, a warp reads 128 contiguous bytes
+//     of a row; one sweep for the amax, one for the codes (kept in
+//     registers).  Column amaxes of the four row quarters meet in shared
+//     memory (1x128), a row quarter is one 1x32 group (MXFP8).
+//   row pass (row-wise codes of X, dual mode): a half-warp owns a row, 16
+//     lanes x 8 columns, so each 16-byte read and each 8-byte code store of a
+//     warp covers two whole rows; group amaxes are xor-shuffles.
+//   X^T out: once every thread has read the BF16 values, the column codes go
+//     into the consumed stage as a [column][row] byte tile (16-byte chunks
+//     XOR-swizzled by column/2, so a quarter-warp's stores hit 8 different
+//     bank groups) and leave as whole 128-byte rows of X^T.
+// A tile's stage is refilled once every thread has passed the CTA barrier
+// that ends the tile (generic-proxy accesses, then an async-proxy fence).
+constexpr int kTileThreads = 256;
+constexpr int kTileStages = 2;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;
+
+struct TileShared {
+    uint32_t tile[kTileStages][128 * 64];   // BF16 pairs, row pitch 64 words
+    uint2 red[4][64];                        // column-pair amax of each row quarter
+    uint64_t full[kTileStages];
+    int abort;
+};
+constexpr size_t kTileSmem = sizeof(TileShared) + 1024;
+
+
+__device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+            if (status != nullptr) atomicExch(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// x / d or x * d (power-of-two grans) for two BF16 values packed in `word`.
+template <int GRAN>
+__device__ __forceinline__ float2 tile_scaled2(uint32_t word, float d0, float d1) {
+    const float a = bf16_lo(word), b = bf16_hi(word);
+    if constexpr (kPow2<GRAN>) return make_float2(__fmul_rn(a, d0), __fmul_rn(b, d1));
+    return make_float2(__fdiv_rn(a, d0), __fdiv_rn(b, d1));
+}
+
+template <int GRAN, bool DUAL>
+__global__ void __launch_bounds__(kTileThreads, 3)
+quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, int64_t cols,
+                      uint8_t* __restrict__ qt, void* __restrict__ st,
+                      uint8_t* __restrict__ q, void* __restrict__ s, int* status) {
+    static_assert(GRAN == kGranTok || GRAN == kGranTokP2 || GRAN == kGranMx, "per-column scales only");
+    extern __shared__ uint8_t tile_smem_raw[];
+    TileShared& sh = *reinterpret_cast<TileShared*>((reinterpret_cast<uintptr_t>(tile_smem_raw) + 1023) &
+                                                    ~uintptr_t(1023));
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int64_t tiles_c = ceil_div(cols, 128), tiles_r = ceil_div(rows, 128);
+    const int64_t ntiles = tiles_c * tiles_r;
+
+    if (tid == 0) {
+        for (int k = 0; k < kTileStages; ++k) mbar_init(smem_u32(&sh.full[k]), 1);
+        sh.abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_x);
+    }
+    __syncthreads();
+    int64_t issued = 0;     // tiles whose load thread 0 has issued
+    auto issue = [&](int64_t i) {  // i-th tile of this CTA into stage i % kTileStages
+        const int64_t t = blockIdx.x + i * (int64_t)gridDim.x;
+        const int64_t rt = t / tiles_c, ct = t - rt * tiles_c;
+        const uint32_t bar = smem_u32(&sh.full[i % kTileStages]);
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        tma_load_2d(smem_u32(sh.tile[i % kTileStages]), &tm_x, bar, (int32_t)(ct * 128), (int32_t)(rt * 128));
+    };
+    const int64_t mine = (ntiles > blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (tid == 0) {
+        for (; issued < mine && issued < kTileStages; ++issued) issue(issued);
+    }
+
+    const int cp = tid & 63, rq = tid >> 6;        // column pass
+    int64_t consumed = 0;   // tiles whose load has been waited for
+    for (int64_t i = 0; i < mine; ++i) {
+        const int stg = (int)(i % kTileStages);
+        const bool got = tile_wait(smem_u32(&sh.full[stg]), (uint32_t)((i / kTileStages) & 1), status);
+        if (!__syncthreads_and(got)) break;
+        consumed = i + 1;
+        const int64_t t = blockIdx.x + i * (int64_t)gridDim.x;
+        const int64_t rt = t / tiles_c, ct = t - rt * tiles_c;
+        const int64_t r0 = rt * 128, c0 = ct * 128;
+        const uint32_t* tile = sh.tile[stg];
+
+        // ---------------- column pass, sweep 1: amax of columns 2cp, 2cp+1 over rows 32rq..+31
+        const uint32_t* colp = tile + (32 * rq) * 64 + cp;
+        uint32_t mm = 0;   // |x| bits of both columns, 16 bits each
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mm = __vmaxu2(mm, colp[k * 64] & 0x7FFF7FFFu);
+        uint32_t m0 = mm & 0xFFFFu, m1 = mm >> 16;
+        float d0 = 1.0f, d1 = 1.0f;       // divisors (FP32 scales) or multipliers (power-of-two scales)
+        int e0 = 0, e1 = 0;
+        if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
+            sh.red[rq][cp] = make_uint2(m0, m1);
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint2 o = sh.red[k][cp];
+                m0 = max(m0, o.x);
+                m1 = max(m1, o.y);
+            }
+            if constexpr (GRAN == kGranTok) {
+                d0 = fp32_scale_from_amax(amax_bits_to_f32(m0));
+                d1 = fp32_scale_from_amax(amax_bits_to_f32(m1));
+            } else {
+                e0 = mx_exponent_from_amax_bits(m0 << 16);
+                e1 = mx_exponent_from_amax_bits(m1 << 16);
+                d0 = exp2_neg(e0);
+                d1 = exp2_neg(e1);
+            }
+        } else {   // MXFP8: a row quarter is one 1x32 group of X^T
+            e0 = mx_exponent_from_amax_bits(m0 << 16);
+            e1 = mx_exponent_from_amax_bits(m1 << 16);
+            d0 = exp2_neg(e0);
+            d1 = exp2_neg(e1);
+        }
+        // ---------------- column pass, sweep 2: codes of X^T into registers (4 rows per word)
+        uint32_t c0w[8], c1w[8];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+            const float2 a = tile_scaled2<GRAN>(colp[k * 64], d0, d1);
+            const float2 b = tile_scaled2<GRAN>(colp[(k + 1) * 64], d0, d1);
+            const float2 c = tile_scaled2<GRAN>(colp[(k + 2) * 64], d0, d1);
+            const float2 d = tile_scaled2<GRAN>(colp[(k + 3) * 64], d0, d1);
+            c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
+            c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
+        }
+        // scales of X^T ([cols, *] grid)
+        {
+            const int64_t rbase = r0 + 32 * rq;
+            if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
+                if (rq == 0) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int64_t c = c0 + 2 * cp + j;
+                        if (c < cols) {
+                            if constexpr (GRAN == kGranTok) static_cast<float*>(st)[c * tiles_r + rt] = j ? d1 : d0;
+                            else static_cast<uint8_t*>(st)[c * tiles_r + rt] = (uint8_t)((j ? e1 : e0) + 127);
+                        }
+                    }
+                }
+            } else {
+                const int64_t nrb = ceil_div(rows, 32);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int64_t c = c0 + 2 * cp + j;
+                    if (c < cols && rbase < rows)
+                        static_cast<uint8_t*>(st)[c * nrb + (rbase >> 5)] = (uint8_t)((j ? e1 : e0) + 127);
+                }
+            }
+        }
+
+        // ---------------- row pass: row-wise codes of X.  A half-warp owns a
+        // row (16 lanes x 8 columns), so every 16-byte read and every 8-byte
+        // store of a warp covers two whole rows.
+        if constexpr (DUAL) {
+            const int ch = lane & 15;
+            const int64_t ncb = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
+#pragma unroll 2
+            for (int it2 = 0; it2 < 8; ++it2) {
+                const int rloc = 16 * w + 2 * it2 + (lane >> 4);
+                const int64_t r = r0 + rloc;
+                const uint4 v = *reinterpret_cast<const uint4*>(tile + rloc * 64 + ch * 4);
+                const uint32_t a = absmax_v4(v);
+                float dd;
+                int ee = 0;
+                if constexpr (GRAN == kGranMx) {
+                    ee = mx_exponent_from_amax_bits(warp_max_u32(a, 4) << 16);
+                    dd = exp2_neg(ee);
+                } else {
+                    const uint32_t m = warp_max_u32(a, 16);
+                    if constexpr (GRAN == kGranTok) {
+                        dd = fp32_scale_from_amax(amax_bits_to_f32(m));
+                    } else {
+                        ee = mx_exponent_from_amax_bits(m << 16);
+                        dd = exp2_neg(ee);
+                    }
+                }
+                const int64_t c = c0 + 8 * ch;
+                if (r < rows) {
+                    if (c < cols) {
+                        const float2 x0 = tile_scaled2<GRAN>(v.x, dd, dd);
+                        const float2 x1 = tile_scaled2<GRAN>(v.y, dd, dd);
+                        const float2 x2 = tile_scaled2<GRAN>(v.z, dd, dd);
+                        const float2 x3 = tile_scaled2<GRAN>(v.w, dd, dd);
+                        *reinterpret_cast<uint2*>(q + r * cols + c) =
+                            make_uint2(e4m3x4(x0.x, x0.y, x1.x, x1.y), e4m3x4(x2.x, x2.y, x3.x, x3.y));
+                    }
+                    if constexpr (GRAN == kGranMx) {
+                        if ((ch & 3) == 0 && c < cols) static_cast<uint8_t*>(s)[r * ncb + (c >> 5)] = (uint8_t)(ee + 127);
+                    } else if constexpr (GRAN == kGranTok) {
+                        if (ch == 0) static_cast<float*>(s)[r * ncb + ct] = dd;
+                    } else if constexpr (GRAN == kGranTokP2) {
+                        if (ch == 0) static_cast<uint8_t*>(s)[r * ncb + ct] = (uint8_t)(ee + 127);
+                    }
+                }
+            }
+        }
+
+        // ---------------- X^T codes: through the consumed stage as a [column][row]
+        // byte tile (16-byte chunks XOR-swizzled by column/2), then out as
+        // whole 128-byte rows of X^T
+        __syncthreads();   // every read of the BF16 values is done
+        {
+            uint8_t* ct8 = reinterpret_cast<uint8_t*>(sh.tile[stg]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = 2 * cp + j;
+                const uint32_t* cw = j ? c1w : c0w;
+                const int sw = (col >> 1) & 7;
+                *reinterpret_cast<uint4*>(ct8 + col * 128 + 16 * ((2 * rq) ^ sw)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                *reinterpret_cast<uint4*>(ct8 + col * 128 + 16 * ((2 * rq + 1) ^ sw)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int xr = (tid >> 3) + 32 * pass, k = tid & 7;   // row of X^T within the tile, 16-byte chunk
+                const int64_t c = c0 + xr;
+                if (c < cols && r0 + 16 * k < rows)
+                    *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) =
+                        *reinterpret_cast<const uint4*>(ct8 + xr * 128 + 16 * (k ^ ((xr >> 1) & 7)));
+            }
+        }
+        __syncthreads();   // every read of this stage (and of red) is done
+        if (tid == 0 && issued < mine) {
+            fence_proxy_async_smem();
+            issue(issued);
+            ++issued;
+        }
+    }
+    // After an abort, copies issued but not yet waited for must land before
+    // the CTA exits (each stage has at most one such copy).
+    if (tid == 0) {
+        for (int64_t i = consumed; i < issued; ++i)
+            mbar_wait_drain(smem_u32(&sh.full[i % kTileStages]), (uint32_t)((i / kTileStages) & 1), kWaitLimitNs);
     }
 }
 
@@ -609,37 +795,66 @@ int launch_quantize(const QuantJob& j, cudaStream_t st) {
     return (int)cudaGetLastError();
 }
 
-template <int GRAN>
-static void launch_tile(const QuantJob& j, cudaStream_t st, int nparts, const float* given) {
-    dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
-    if (j.q != nullptr)
-        quant_tile_t_kernel<GRAN, true><<<grid, kTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q, j.s,
-                                                                   j.partials, nparts, given);
-    else
-        quant_tile_t_kernel<GRAN, false><<<grid, kTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, nullptr,
-                                                                    nullptr, j.partials, nparts, given);
+template <int GRAN, bool DUAL>
+static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int grid, cudaStream_t st) {
+    static bool attr_set[64] = {false};   // one flag per kernel instantiation and device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(quant_tile_tma_kernel<GRAN, DUAL>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileSmem);
+        if (e != cudaSuccess) return (int)e;
+        attr_set[dev] = true;
+    }
+    quant_tile_tma_kernel<GRAN, DUAL><<<grid, kTileThreads, kTileSmem, st>>>(
+        tm, j.rows, j.cols, j.qt, j.st, DUAL ? j.q : nullptr, DUAL ? j.s : nullptr, j.status);
+    return (int)cudaGetLastError();
 }
 
+template <int GRAN>
+static int launch_tile(const QuantJob& j, cudaStream_t st) {
+    CUtensorMap tm;
+    if (!make_tmap_b16(&tm, j.x, (uint64_t)j.cols, (uint64_t)j.rows, (uint64_t)j.ldx, 128, 128))
+        return (int)cudaErrorInvalidValue;
+    const int64_t tiles = ceil_div(j.cols, 128) * ceil_div(j.rows, 128);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, 3 * (int64_t)sm_count()));
+    if (j.q != nullptr) return launch_tile_k<GRAN, true>(tm, j, grid, st);
+    return launch_tile_k<GRAN, false>(tm, j, grid, st);
+}
+
+template <int GRAN>
+static int launch_tile_reg(const QuantJob& j, cudaStream_t st, int nparts, const float* given) {
+    const dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
+    if (j.q != nullptr)
+        quant_tile_reg_kernel<GRAN, true><<<grid, kRegTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q,
+                                                                          j.s, j.partials, nparts, given);
+    else
+        quant_tile_reg_kernel<GRAN, false><<<grid, kRegTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st,
+                                                                           nullptr, nullptr, j.partials, nparts, given);
+    return (int)cudaGetLastError();
+}
+
+// Granularities with a scale per column of X (1x128, 1x32 groups of X^T's
+// rows) take the TMA-fed kernel; those with one scale per tile the
+// register-resident one (each the faster of the two on GB300).
 int launch_quantize_transposed(const QuantJob& j, cudaStream_t st) {
     int nparts = 0;
     switch (j.gran) {
-    case kGranTok: launch_tile<kGranTok>(j, st, 0, nullptr); break;
-    case kGranMx: launch_tile<kGranMx>(j, st, 0, nullptr); break;
-    case kGranBlk: launch_tile<kGranBlk>(j, st, 0, nullptr); break;
-    case kGranTokP2: launch_tile<kGranTokP2>(j, st, 0, nullptr); break;
-    case kGranBlkP2: launch_tile<kGranBlkP2>(j, st, 0, nullptr); break;
+    case kGranTok: return launch_tile<kGranTok>(j, st);
+    case kGranMx: return launch_tile<kGranMx>(j, st);
+    case kGranTokP2: return launch_tile<kGranTokP2>(j, st);
+    case kGranBlk: return launch_tile_reg<kGranBlk>(j, st, 0, nullptr);
+    case kGranBlkP2: return launch_tile_reg<kGranBlkP2>(j, st, 0, nullptr);
     case kGranPT: {
         if (!j.given_scale) {
             const int e = launch_amax(j, st, &nparts);
             if (e) return e;
         }
-        launch_tile<kGranPT>(j, st, nparts, j.given_scale ? static_cast<const float*>(j.st) : nullptr);
-        break;
+        return launch_tile_reg<kGranPT>(j, st, nparts, j.given_scale ? static_cast<const float*>(j.st) : nullptr);
     }
     default:
         return (int)cudaErrorInvalidValue;
     }
-    return (int)cudaGetLastError();
 }
 
 }  // namespace fp8bs
