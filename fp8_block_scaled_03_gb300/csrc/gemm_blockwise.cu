@@ -17,7 +17,7 @@
 // producer warpgroup gives registers back (72) and the two epilogue
 // warpgroups take them (216): 128*72 + 256*216 = 384*168.
 //   warp 0      TMA producer (one lane): A 128x128 and B 256x128 boxes,
-//               128-byte swizzle, 4-stage ring.
+//               128-byte swizzle, 3-stage ring.
 //   warp 1      TMEM owner + MMA issuer (one lane): 4 x tcgen05.mma
 //               kind::f8f6f4 (M128 N256 K32) per K block into partial
 //               buffer kb & 1, then tcgen05.commit to free the stage and to
@@ -33,7 +33,10 @@
 //   warps 4..11 epilogue: warp w reads TMEM lanes 32*(w%4).. (one D row per
 //               thread) and columns 128*((w-4)/4).. (one 128-column half);
 //               acc += partial * sa * sb with both scales read from the
-//               ring, BF16 store at the end of the tile.
+//               ring.  At the end of the tile each warp writes its 32 rows as
+//               BF16 into a 4 KB staging buffer, 64 columns at a time, and a
+//               TMA store takes them out, so the warp is back to promoting
+//               while the store drains (its stores used to hold the MMA up).
 // Scale modes (template): 0 per-tensor, 1 per row (1x128), 2 per 128-row block.
 #include <algorithm>
 
@@ -46,7 +49,8 @@
 namespace fp8bs {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3;
+constexpr int OSTAGE_BYTES = 32 * 128;   // per epilogue warp: 32 rows x 64 BF16 columns
 constexpr int SG = 4;          // K blocks per scale group
 constexpr int SRING = 2;       // scale groups in flight
 constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
@@ -75,7 +79,7 @@ struct alignas(16) Shared {
     SchedShared sched;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 8 * OSTAGE_BYTES + sizeof(Shared);
 
 // Four consecutive K-block scales starting at kb0 from a row of `nkb` FP32
 // scales (zero past the row's end); one 16-byte load when `vec`.
@@ -104,10 +108,12 @@ __device__ __forceinline__ void put4a(float (*dst)[BM], int idx, float4 v) {
 
 template <int SA_MODE, int SB_MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
+gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_d, Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared* sh = reinterpret_cast<Shared*>(stages + (size_t)STAGES * STAGE_BYTES);
+    uint8_t* ostage = stages + (size_t)STAGES * STAGE_BYTES;   // 1024-byte aligned
+    Shared* sh = reinterpret_cast<Shared*>(ostage + 8 * OSTAGE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = p.k / BK;
@@ -340,8 +346,40 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 }
             }
             if (!ok) break;
-            // BF16 store of this thread's row: 128 columns = 16 x 16 bytes
-            if (row < ti.row_end) {
+            // This warp's 32 rows leave by TMA when they all belong to the
+            // tile's row group (always for a dense GEMM; an expert's last,
+            // partial row block may end inside them, and the rows after it
+            // belong to the next expert).
+            if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
+                // BF16 tile rows through this warp's staging buffer (128-byte
+                // swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)), then a
+                // TMA store of the 32 x 64 box; the TMA clips rows and columns
+                // past the matrix
+                uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float lo, hi;
+                            f2_unpack(acc[32 * half + 4 * c + u], lo, hi);
+                            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+                            o[u] = *reinterpret_cast<uint32_t*>(&v);
+                        }
+                        *reinterpret_cast<uint4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 64 * half), (int32_t)(ti.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            } else if (row < ti.row_end) {
                 __nv_bfloat16* drow = p.d + row * p.n + col0;
 #pragma unroll
                 for (int j = 0; j < 128; j += 8) {
@@ -365,6 +403,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 }
             }
         }
+        if (lane == 0) bulk_wait0();   // this warp's output stores are complete
     }
 
     tc_fence_before();
@@ -376,7 +415,8 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
 }
 
 template <int SA, int SB>
-int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t st) {
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
+                 cudaStream_t st) {
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -386,7 +426,7 @@ int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, 
         if (e != cudaSuccess) return (int)e;
         attr_set[dev] = true;
     }
-    gemm_blockwise_kernel<SA, SB><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    gemm_blockwise_kernel<SA, SB><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, td, p);
     return (int)cudaGetLastError();
 }
 
@@ -401,6 +441,8 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
     if (!make_tmap_u8(&ta, j.a, (uint64_t)j.k, (uint64_t)j.m, (uint64_t)j.k, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_u8(&tb, j.b, (uint64_t)j.k, b_rows, (uint64_t)j.k, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return (int)cudaErrorInvalidValue;
+    CUtensorMap td;
+    if (!make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n)) return (int)cudaErrorInvalidValue;
     Params p{};
     p.m = j.m; p.n = j.n; p.k = j.k;
     p.sa = static_cast<const float*>(j.sa);
@@ -419,7 +461,7 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
     }
     const int sa = mode_of(j.a_gran), sb = mode_of(j.b_gran);
 #define FP8BS_BW_CASE(A, B) \
-    if (sa == A && sb == B) return launch_typed<A, B>(ta, tb, p, grid, st);
+    if (sa == A && sb == B) return launch_typed<A, B>(ta, tb, td, p, grid, st);
     FP8BS_BW_CASE(1, 2) FP8BS_BW_CASE(1, 1) FP8BS_BW_CASE(1, 0)
     FP8BS_BW_CASE(2, 2) FP8BS_BW_CASE(2, 1) FP8BS_BW_CASE(2, 0)
     FP8BS_BW_CASE(0, 2) FP8BS_BW_CASE(0, 1) FP8BS_BW_CASE(0, 0)
