@@ -18,9 +18,10 @@
 //               atoms to TMEM, then 4 block-scaled MMAs (M128 N256; K32 for
 //               MXFP8, K64 for NVFP4), accumulating the whole K range in TMEM.
 //   warp 2      scale loader: reads the row-major scale bytes of the stage's
-//               rows and writes them in the 32 x 16-byte atom layout that
-//               tcgen05.cp 32x128b.warpx4 replicates into all TMEM lane
-//               quarters (row r0 + 32*r1 at byte r0*16 + r1*4).
+//               rows (power-of-two scales: four stages per load) and writes
+//               them in the 32 x 16-byte atom layout that tcgen05.cp
+//               32x128b.warpx4 replicates into all TMEM lane quarters (row
+//               r0 + 32*r1 at byte r0*16 + r1*4).
 //   warp 3      idle
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
 //               128 columns per thread) to BF16 registers, release TMEM, store.
@@ -110,24 +111,7 @@ template <int KIND, int SA, int SB>
 __device__ __forceinline__ void load_scales(ScaleRegs<KIND>& r, const Params& p, const TileInfo& ti, int64_t kb,
                                             int lane, int64_t sf_pitch) {
     constexpr int W = ScaleRegs<KIND>::W;
-    if constexpr (KIND == kP2) {
-        // SA / SB: 1 = one byte per row, 2 = one byte per 128-row block (rows of
-        // the operand's own scale grid; B grids stacked per expert).
-#pragma unroll
-        for (int r1 = 0; r1 < 4; ++r1) {
-            const int64_t row = ti.row0 + lane + 32 * r1;
-            const int64_t idx = (SA == 1 ? row : (row >> 7)) * sf_pitch + kb;
-            r.a[r1][0] = row < p.m ? (uint32_t)__ldg(p.sa + idx) * 0x01010101u : 0u;
-        }
-        const int64_t nb_e = (p.n + 127) / 128;
-#pragma unroll
-        for (int r1 = 0; r1 < 8; ++r1) {
-            const int64_t n = ti.n0 + lane + 32 * r1;
-            const int64_t srow = (SB == 1) ? (int64_t)ti.expert * p.n + n : (int64_t)ti.expert * nb_e + (n >> 7);
-            r.b[r1][0] = n < p.n ? (uint32_t)__ldg(p.sb + srow * sf_pitch + kb) * 0x01010101u : 0u;
-        }
-        return;
-    }
+    static_assert(KIND != kP2, "power-of-two scales use load_scales_group");
     const int64_t koff = kb * Cfg<KIND>::SF_BYTES_PER_ROW;
 #pragma unroll
     for (int r1 = 0; r1 < 4; ++r1) {
@@ -175,6 +159,64 @@ __device__ __forceinline__ void store_scales(const ScaleRegs<KIND>& r, uint8_t* 
                 make_uint4(r.b[4 * c + 0][j], r.b[4 * c + 1][j], r.b[4 * c + 2][j], r.b[4 * c + 3][j]);
         }
     }
+}
+
+// Power-of-two scales, four stages at a time: word g of a row slot holds
+// the byte of stage kb0 + g, replicated to the four 32-wide sub-blocks.  One
+// 4-byte load per row covers the four stages when the row pitch and base
+// allow it; per-stage byte loads would cost one 32-sector request per row
+// slot and stage (the rows of a stage are 32 apart).  (MXFP8 keeps the
+// per-stage loader: 16-byte groups measured slower there, partly because
+// the MoE down projection's 24-byte rows rule them out.)
+constexpr int kSfGroup = 4;
+struct WideRegs {
+    uint32_t a[4][kSfGroup];
+    uint32_t b[8][kSfGroup];
+};
+
+__device__ __forceinline__ void load_row_group(uint32_t* w, const uint8_t* __restrict__ src, int64_t kb0, int64_t nkb,
+                                               bool ok, bool vec) {
+    if (!ok) {
+#pragma unroll
+        for (int g = 0; g < kSfGroup; ++g) w[g] = 0u;
+        return;
+    }
+    const uint8_t* p = src + kb0;
+    if (vec && kb0 + kSfGroup <= nkb) {
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
+#pragma unroll
+        for (int g = 0; g < kSfGroup; ++g) w[g] = ((v >> (8 * g)) & 0xFFu) * 0x01010101u;
+    } else {
+#pragma unroll
+        for (int g = 0; g < kSfGroup; ++g) w[g] = (kb0 + g < nkb) ? (uint32_t)__ldg(p + g) * 0x01010101u : 0u;
+    }
+}
+
+// SA / SB: 1 = one byte per row, 2 = one byte per 128-row block.
+template <int SA, int SB>
+__device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, const TileInfo& ti, int64_t kb0,
+                                                  int64_t nkb, int lane, int64_t sf_pitch, bool vec) {
+    const int64_t nb_e = (p.n + 127) / 128;
+#pragma unroll
+    for (int r1 = 0; r1 < 4; ++r1) {
+        const int64_t row = ti.row0 + lane + 32 * r1;
+        const int64_t srow = (SA == 2) ? (row >> 7) : row;
+        load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
+    }
+#pragma unroll
+    for (int r1 = 0; r1 < 8; ++r1) {
+        const int64_t n = ti.n0 + lane + 32 * r1;
+        const int64_t srow = (SB == 2) ? (int64_t)ti.expert * nb_e + (n >> 7) : (int64_t)ti.expert * p.n + n;
+        load_row_group(w.b[r1], p.sb + srow * sf_pitch, kb0, nkb, n < p.n, vec);
+    }
+}
+
+template <int KIND>
+__device__ __forceinline__ void group_stage(ScaleRegs<KIND>& r, const WideRegs& w, int g) {
+#pragma unroll
+    for (int r1 = 0; r1 < 4; ++r1) r.a[r1][0] = w.a[r1][g];
+#pragma unroll
+    for (int r1 = 0; r1 < 8; ++r1) r.b[r1][0] = w.b[r1][g];
 }
 
 template <int KIND, int SA, int SB>
@@ -289,42 +331,69 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             mbar_wait(smem_u32(&sh->drain), 0, abort, p.status);
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ scale loader
-        // A load cursor runs SF_PD stages ahead of the store cursor; the
-        // loaded words wait in a register ring (slot = stage mod SF_PD, the
-        // loop unrolled so every slot index is a constant), which keeps the
-        // L2 latency of the scale loads off the per-stage path.
-        constexpr int SF_PD = (KIND == kNv) ? 2 : 4;   // NVFP4 stages carry 4x the scale words
-        ScaleRegs<KIND> ring[SF_PD];
-        int64_t lt = blockIdx.x, lkb = 0;                 // load cursor
+    } else if (warp == 2 && KIND == kP2) {
+        // ------------------------------------------------------------ scale loader (power of two)
+        // Groups of four stages are loaded one group ahead of the one being
+        // written out (two register buffers, the loop unrolled by two so
+        // both buffer names are constants).
+        const bool vec = (sf_pitch & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.sa) | reinterpret_cast<uintptr_t>(p.sb)) & 3u) == 0;
+        int64_t lt = blockIdx.x, lkb0 = 0;                // load cursor (tile, first stage of the group)
         TileInfo lti{};
         if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
-#pragma unroll
-        for (int d = 0; d < SF_PD; ++d) {
-            if (lt < total) {
-                load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
-                if (++lkb == nkb) {
-                    lkb = 0;
-                    lt += gridDim.x;
-                    if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
-                }
+        auto load_next = [&](WideRegs& w, int64_t& kb0_out) -> bool {
+            if (lt >= total) return false;
+            load_scales_group<SA, SB>(w, p, lti, lkb0, nkb, lane, sf_pitch, vec);
+            kb0_out = lkb0;
+            lkb0 += kSfGroup;
+            if (lkb0 >= nkb) {
+                lkb0 = 0;
+                lt += gridDim.x;
+                if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
             }
-        }
-        int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
+            return true;
+        };
         uint32_t it = 0;
         bool ok = true;
-        while (st_t < total && ok) {
+        auto store_group = [&](const WideRegs& w, int64_t kb0) {
 #pragma unroll
-            for (int d = 0; d < SF_PD; ++d) {
-                if (st_t >= total || !ok) break;
+            for (int g = 0; g < kSfGroup; ++g) {
+                if (!ok || kb0 + g >= nkb) break;
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                 if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
-                store_scales<KIND>(ring[d], stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
+                ScaleRegs<KIND> r;
+                group_stage<KIND>(r, w, g);
+                store_scales<KIND>(r, stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
                 ++it;
+            }
+        };
+        WideRegs w0, w1;
+        int64_t k0 = 0, k1 = 0;
+        bool h0 = load_next(w0, k0), h1 = load_next(w1, k1);
+        while (h0 && ok) {
+            store_group(w0, k0);
+            h0 = load_next(w0, k0);
+            if (!h1 || !ok) break;
+            store_group(w1, k1);
+            h1 = load_next(w1, k1);
+            if (!h0) break;
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale loader (MXFP8, NVFP4)
+        if constexpr (KIND != kP2) {
+            // A load cursor runs SF_PD stages ahead of the store cursor; the
+            // loaded words wait in a register ring (slot = stage mod SF_PD, the
+            // loop unrolled so every slot index is a constant), which keeps the
+            // L2 latency of the scale loads off the per-stage path.
+            constexpr int SF_PD = (KIND == kNv) ? 2 : 4;   // NVFP4 stages carry 4x the scale words
+            ScaleRegs<KIND> ring[SF_PD];
+            int64_t lt = blockIdx.x, lkb = 0;                 // load cursor
+            TileInfo lti{};
+            if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+    #pragma unroll
+            for (int d = 0; d < SF_PD; ++d) {
                 if (lt < total) {
                     load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
                     if (++lkb == nkb) {
@@ -333,9 +402,33 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                         if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
                     }
                 }
-                if (++st_kb == nkb) {
-                    st_kb = 0;
-                    st_t += gridDim.x;
+            }
+            int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
+            uint32_t it = 0;
+            bool ok = true;
+            while (st_t < total && ok) {
+    #pragma unroll
+                for (int d = 0; d < SF_PD; ++d) {
+                    if (st_t >= total || !ok) break;
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
+                    store_scales<KIND>(ring[d], stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
+                    ++it;
+                    if (lt < total) {
+                        load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
+                        if (++lkb == nkb) {
+                            lkb = 0;
+                            lt += gridDim.x;
+                            if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+                        }
+                    }
+                    if (++st_kb == nkb) {
+                        st_kb = 0;
+                        st_t += gridDim.x;
+                    }
                 }
             }
         }
