@@ -37,6 +37,10 @@ GEMM_FLOP = 2 * M3 * H3 * I3                    # one of fprop / dgrad / wgrad
 STEP_FLOP = 3 * GEMM_FLOP
 FP8_PER_BF16 = 2.0                              # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 FP4_PER_BF16 = 6.0                              # nominal dense ratio (13.5 / 2.25 PFLOP/s)
+# DRAM bytes (read + write) per blockwise-GEMM launch of the step, averaged
+# over fprop, dgrad and wgrad, from one ncu capture of this kernel
+# (profiles/gemm_blockwise_fprop.md); None once the kernel changes.
+GEMM_TRAFFIC_BYTES = 138438400
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -454,7 +458,7 @@ def main():
     peak_fp8 = pk["bf16_tflops_sustained"] * FP8_PER_BF16
     roofline = {"bound": "tensor", "kernel": "gemm_blockwise_kernel<1x128,128x128|1x128>",
                 "achieved": round(achieved, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak_fp8, 3), "traffic": None,
+                "frac": round(achieved / peak_fp8, 3), "traffic": GEMM_TRAFFIC_BYTES, "traffic_unit": "bytes per launch",
                 "peak_note": f"{pk['source']} bf16 sustained x nominal fp8/bf16 ratio 2 (of {pk['source']})",
                 "per_gemm_ms": [round(statistics.mean(r[j] for r in gemm_ms), 3) for j in range(3)]}
 
