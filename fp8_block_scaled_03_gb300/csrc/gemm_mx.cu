@@ -17,12 +17,12 @@
 //   warp 1      TMEM owner + MMA issuer: per stage, tcgen05.cp of the scale
 //               atoms to TMEM, then 4 block-scaled MMAs (M128 N256; K32 for
 //               MXFP8, K64 for NVFP4), accumulating the whole K range in TMEM.
-//   warp 2      scale loader: reads the row-major scale bytes of the stage's
-//               rows (power-of-two scales: four stages per load) and writes
-//               them in the 32 x 16-byte atom layout that tcgen05.cp
+//   warps 2-3   scale loaders, taking turns by stage (power-of-two scales:
+//               by group of four stages, read with one load per row): read
+//               the row-major scale bytes of the stage's rows and write them
+//               in the 32 x 16-byte atom layout that tcgen05.cp
 //               32x128b.warpx4 replicates into all TMEM lane quarters (row
 //               r0 + 32*r1 at byte r0*16 + r1*4).
-//   warp 3      idle
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
 //               128 columns per thread) to BF16 registers, release TMEM, store.
 // TMEM: columns 0..255 accumulator, 256.. scale factors per stage.
@@ -193,21 +193,41 @@ __device__ __forceinline__ void load_row_group(uint32_t* w, const uint8_t* __res
 }
 
 // SA / SB: 1 = one byte per row, 2 = one byte per 128-row block.
+// part 0: A rows and B rows 0..127; part 1: B rows 128..255.
 template <int SA, int SB>
 __device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, const TileInfo& ti, int64_t kb0,
-                                                  int64_t nkb, int lane, int64_t sf_pitch, bool vec) {
+                                                  int64_t nkb, int lane, int64_t sf_pitch, bool vec, int part) {
     const int64_t nb_e = (p.n + 127) / 128;
-#pragma unroll
-    for (int r1 = 0; r1 < 4; ++r1) {
-        const int64_t row = ti.row0 + lane + 32 * r1;
-        const int64_t srow = (SA == 2) ? (row >> 7) : row;
-        load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
-    }
-#pragma unroll
-    for (int r1 = 0; r1 < 8; ++r1) {
+    auto brow = [&](int r1) {
         const int64_t n = ti.n0 + lane + 32 * r1;
         const int64_t srow = (SB == 2) ? (int64_t)ti.expert * nb_e + (n >> 7) : (int64_t)ti.expert * p.n + n;
         load_row_group(w.b[r1], p.sb + srow * sf_pitch, kb0, nkb, n < p.n, vec);
+    };
+    if (part == 0) {
+#pragma unroll
+        for (int r1 = 0; r1 < 4; ++r1) {
+            const int64_t row = ti.row0 + lane + 32 * r1;
+            const int64_t srow = (SA == 2) ? (row >> 7) : row;
+            load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
+        }
+#pragma unroll
+        for (int r1 = 0; r1 < 4; ++r1) brow(r1);
+    } else {
+#pragma unroll
+        for (int r1 = 4; r1 < 8; ++r1) brow(r1);
+    }
+}
+
+// One loader's share of a stage's atoms: part 0 the A atoms and B rows
+// 0..127, part 1 B rows 128..255 (power-of-two scales: one word per row).
+template <int KIND>
+__device__ __forceinline__ void store_scales_part(const ScaleRegs<KIND>& r, uint8_t* sf, int lane, int part) {
+    uint8_t* sfb = sf + Cfg<KIND>::A_ATOMS * 512;
+    if (part == 0) {
+        *reinterpret_cast<uint4*>(sf + lane * 16) = make_uint4(r.a[0][0], r.a[1][0], r.a[2][0], r.a[3][0]);
+        *reinterpret_cast<uint4*>(sfb + lane * 16) = make_uint4(r.b[0][0], r.b[1][0], r.b[2][0], r.b[3][0]);
+    } else {
+        *reinterpret_cast<uint4*>(sfb + 512 + lane * 16) = make_uint4(r.b[4][0], r.b[5][0], r.b[6][0], r.b[7][0]);
     }
 }
 
@@ -236,7 +256,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&sh->full[s]), 2);   // TMA bytes + scale loader
+            mbar_init(smem_u32(&sh->full[s]), KIND == kP2 ? 3 : 2);   // TMA bytes + scale loader(s)
             mbar_init(smem_u32(&sh->empty[s]), 1);
         }
         mbar_init(smem_u32(&sh->tfull), 1);
@@ -331,18 +351,21 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             mbar_wait(smem_u32(&sh->drain), 0, abort, p.status);
         }
         __syncwarp();
-    } else if (warp == 2 && KIND == kP2) {
-        // ------------------------------------------------------------ scale loader (power of two)
-        // Groups of four stages are loaded one group ahead of the one being
-        // written out (two register buffers, the loop unrolled by two so
-        // both buffer names are constants).
+    } else if ((warp == 2 || warp == 3) && KIND == kP2) {
+        // ------------------------------------------------------------ scale loaders (power of two)
+        // Both warps walk every stage in order and split the rows: warp 2
+        // writes the A atom and B rows 0..127, warp 3 B rows 128..255 (the
+        // stage's full barrier counts both).  Groups of four stages are
+        // loaded one group ahead of the one being written out (two register
+        // buffers, the loop unrolled by two so both names are constants).
+        const int part = warp - 2;
         const bool vec = (sf_pitch & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.sa) | reinterpret_cast<uintptr_t>(p.sb)) & 3u) == 0;
         int64_t lt = blockIdx.x, lkb0 = 0;                // load cursor (tile, first stage of the group)
         TileInfo lti{};
         if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
         auto load_next = [&](WideRegs& w, int64_t& kb0_out) -> bool {
             if (lt >= total) return false;
-            load_scales_group<SA, SB>(w, p, lti, lkb0, nkb, lane, sf_pitch, vec);
+            load_scales_group<SA, SB>(w, p, lti, lkb0, nkb, lane, sf_pitch, vec, part);
             kb0_out = lkb0;
             lkb0 += kSfGroup;
             if (lkb0 >= nkb) {
@@ -362,7 +385,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                 ScaleRegs<KIND> r;
                 group_stage<KIND>(r, w, g);
-                store_scales<KIND>(r, stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
+                store_scales_part<KIND>(r, stages + s * STAGE_B + A_BYTES + B_BYTES, lane, part);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
@@ -380,34 +403,50 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             h1 = load_next(w1, k1);
             if (!h0) break;
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ scale loader (MXFP8, NVFP4)
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------------------ scale loaders (MXFP8, NVFP4)
         if constexpr (KIND != kP2) {
-            // A load cursor runs SF_PD stages ahead of the store cursor; the
-            // loaded words wait in a register ring (slot = stage mod SF_PD, the
-            // loop unrolled so every slot index is a constant), which keeps the
-            // L2 latency of the scale loads off the per-stage path.
+            // Two warps take turns by stage (warp 2 the even stages, warp 3 the
+            // odd ones).  Each keeps a load cursor SF_PD of its stages ahead of
+            // its store cursor; the loaded words wait in a register ring (slot
+            // = stage mod SF_PD, the loop unrolled so every slot index is a
+            // constant), which keeps the L2 latency of the scale loads off the
+            // per-stage path.
             constexpr int SF_PD = (KIND == kNv) ? 2 : 4;   // NVFP4 stages carry 4x the scale words
             ScaleRegs<KIND> ring[SF_PD];
             int64_t lt = blockIdx.x, lkb = 0;                 // load cursor
             TileInfo lti{};
             if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
-    #pragma unroll
+            auto step_load = [&]() {
+                if (++lkb == nkb) {
+                    lkb = 0;
+                    lt += gridDim.x;
+                    if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
+                }
+            };
+            int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
+            auto step_store = [&]() {
+                if (++st_kb == nkb) {
+                    st_kb = 0;
+                    st_t += gridDim.x;
+                }
+            };
+            uint32_t it = (uint32_t)(warp - 2);
+            if (warp == 3) {
+                step_load();
+                step_store();
+            }
+#pragma unroll
             for (int d = 0; d < SF_PD; ++d) {
                 if (lt < total) {
                     load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
-                    if (++lkb == nkb) {
-                        lkb = 0;
-                        lt += gridDim.x;
-                        if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
-                    }
+                    step_load();
+                    if (lt < total) step_load();
                 }
             }
-            int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
-            uint32_t it = 0;
             bool ok = true;
             while (st_t < total && ok) {
-    #pragma unroll
+#pragma unroll
                 for (int d = 0; d < SF_PD; ++d) {
                     if (st_t >= total || !ok) break;
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
@@ -416,19 +455,14 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
-                    ++it;
+                    it += 2;
                     if (lt < total) {
                         load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
-                        if (++lkb == nkb) {
-                            lkb = 0;
-                            lt += gridDim.x;
-                            if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, lt);
-                        }
+                        step_load();
+                        if (lt < total) step_load();
                     }
-                    if (++st_kb == nkb) {
-                        st_kb = 0;
-                        st_t += gridDim.x;
-                    }
+                    step_store();
+                    if (st_t < total) step_store();
                 }
             }
         }
