@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the sub-benchmarks")
     ap.add_argument("--kernel", default=None,
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
-                             "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "nvfp4"],
+                             "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "moe_gather_quant",
+                             "moe_swiglu_quant", "nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
@@ -264,36 +265,59 @@ def quantize_sweep(torch, fp, dev, pk, flush):
 
 
 def moe_bench(torch, fp, dev, pk, flush):
-    """MoE grouped MXFP8 GEMMs, Qwen3-30B-A3B shapes (gate+up and down)."""
+    """The MoE expert MLP in MXFP8, Qwen3-30B-A3B shapes: gather + quantise of
+    the routed tokens into expert order, grouped gate+up GEMM, SwiGLU +
+    quantise, grouped down GEMM; each kernel alone and the four chained."""
     import synth
     tokens, experts, hidden, inter = 16384, 128, 2048, 768
-    _, offsets = synth.moe_routing(tokens, experts, 8, seed=0)
+    token_index, offsets = synth.moe_routing(tokens, experts, 8, seed=0)
     rows = int(offsets[-1])
     act, wt = device_inputs(torch, 200, dev)
-    a = act((rows, hidden), 0.001, 100.0)
-    h = act((rows, inter), 0.001, 100.0)
+    x = act((tokens, hidden), 0.001, 100.0)
     wgu = wt((experts * 2 * inter, hidden))
     wdn = wt((experts * hidden, inter))
     ws = fp.workspace(dev)
-    qa, sa, _ = fp.fp8_quantize(a, "mxfp8", ws=ws)
-    qh, shh, _ = fp.fp8_quantize(h, "mxfp8", ws=ws)
+    idx = torch.from_numpy(token_index).to(dev)
+    qa, sa = fp.fp8_quantize_gathered(x, idx, "mxfp8", ws=ws)
     qgu, sgu, _ = fp.fp8_quantize(wgu, "mxfp8", ws=ws)
     qdn, sdn, _ = fp.fp8_quantize(wdn, "mxfp8", ws=ws)
+    qgu, sgu = qgu.view(experts, 2 * inter, hidden), sgu.view(experts, 2 * inter, hidden // 32)
+    qdn, sdn = qdn.view(experts, hidden, inter), sdn.view(experts, hidden, inter // 32)
     off = torch.from_numpy(offsets).to(dev)
     d_gu = torch.empty((rows, 2 * inter), dtype=torch.bfloat16, device=dev)
     d_dn = torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev)
+    fp.fp8_grouped_gemm(qa, sa, qgu, sgu, off, "mxfp8", out=d_gu, ws=ws)
+    qy, sy = fp.fp8_swiglu_quantize(d_gu, "mxfp8")
     f_gu = 2 * rows * 2 * inter * hidden
     f_dn = 2 * rows * hidden * inter
-    run_gu = lambda: fp.fp8_grouped_gemm(qa, sa, qgu.view(experts, 2 * inter, hidden),  # noqa: E731
-                                         sgu.view(experts, 2 * inter, hidden // 32), off, "mxfp8", out=d_gu, ws=ws)
-    run_dn = lambda: fp.fp8_grouped_gemm(qh, shh, qdn.view(experts, hidden, inter),  # noqa: E731
-                                         sdn.view(experts, hidden, inter // 32), off, "mxfp8", out=d_dn, ws=ws)
+    run_ga = lambda: fp.fp8_quantize_gathered(x, idx, "mxfp8", q=qa, scales=sa, ws=ws)  # noqa: E731
+    run_gu = lambda: fp.fp8_grouped_gemm(qa, sa, qgu, sgu, off, "mxfp8", out=d_gu, ws=ws)  # noqa: E731
+    run_sw = lambda: fp.fp8_swiglu_quantize(d_gu, "mxfp8", q=qy, scales=sy)  # noqa: E731
+    run_dn = lambda: fp.fp8_grouped_gemm(qy, sy, qdn, sdn, off, "mxfp8", out=d_dn, ws=ws)  # noqa: E731
+
+    def layer():
+        run_ga(); run_gu(); run_sw(); run_dn()  # noqa: E702
+
+    ms_ga, _ = time_fn(torch, run_ga, 10, flush)
     ms_gu, _ = time_fn(torch, run_gu, 10, flush)
+    ms_sw, _ = time_fn(torch, run_sw, 10, flush)
     ms_dn, _ = time_fn(torch, run_dn, 10, flush)
+    ms_layer, _ = time_fn(torch, layer, 10, flush)
     peak = pk["bf16_tflops"] * FP8_PER_BF16
     t_gu, t_dn = f_gu / ms_gu / 1e9, f_dn / ms_dn / 1e9
+    # algorithmic bytes: x read once (the gathered re-reads of a token are L2 hits), the
+    # index, the codes and UE8M0 scales written; SwiGLU reads [gate | up] once
+    b_ga = tokens * hidden * 2 + rows * 8 + rows * hidden + rows * hidden // 32
+    b_sw = rows * 2 * inter * 2 + rows * inter + rows * inter // 32
+    g_ga, g_sw = b_ga / (ms_ga * 1e-3) / 1e9, b_sw / (ms_sw * 1e-3) / 1e9
     return {"gate_up": {"tflops": round(t_gu, 1), "ms": round(ms_gu, 3), "frac": round(t_gu / peak, 3)},
             "down": {"tflops": round(t_dn, 1), "ms": round(ms_dn, 3), "frac": round(t_dn / peak, 3)},
+            "gather_quantize": {"gbs": round(g_ga, 1), "us": round(ms_ga * 1e3, 2),
+                                "frac": round(g_ga / pk["hbm_gbs"], 3), "bytes": b_ga},
+            "swiglu_quantize": {"gbs": round(g_sw, 1), "us": round(ms_sw * 1e3, 2),
+                                "frac": round(g_sw / pk["hbm_gbs"], 3), "bytes": b_sw},
+            "layer": {"ms": round(ms_layer, 3), "tflops": round((f_gu + f_dn) / ms_layer / 1e9, 1),
+                      "kernels": 4},
             "peak_tflops": round(peak, 1), "peak_note": "measured bf16 burst x nominal fp8/bf16 ratio 2"}
 
 
@@ -517,6 +541,20 @@ def single_kernel(args, torch, fp, dev):
             g = "1x128" if name == "quant_1x128" else "mxfp8"
             q, s_, _ = fp.fp8_quantize(x, g, ws=ws)
             fn = lambda: fp.fp8_quantize(x, g, q=q, scales=s_, ws=ws)  # noqa: E731
+        work = 0
+    elif name in ("moe_gather_quant", "moe_swiglu_quant"):
+        import synth
+        token_index, offsets = synth.moe_routing(16384, 128, 8, seed=0)
+        rows = int(offsets[-1])
+        if name == "moe_gather_quant":
+            x = act((16384, 2048), 0.001, 100.0)
+            idx = torch.from_numpy(token_index).to(dev)
+            q, s_ = fp.fp8_quantize_gathered(x, idx, "mxfp8", ws=ws)
+            fn = lambda: fp.fp8_quantize_gathered(x, idx, "mxfp8", q=q, scales=s_, ws=ws)  # noqa: E731
+        else:
+            h = act((rows, 2 * 768), 0.0, 1.0)
+            q, s_ = fp.fp8_swiglu_quantize(h, "mxfp8")
+            fn = lambda: fp.fp8_swiglu_quantize(h, "mxfp8", q=q, scales=s_)  # noqa: E731
         work = 0
     elif name == "moe_gate_up":
         import synth

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
     fp8_dequantize(q, scales, gran)       -> BF16 values (exact, rounded once)
     fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16)
     fp8_grouped_gemm(a, sa, b, sb, offsets, gran)                      -> d (bf16)
+    fp8_quantize_gathered(x, token_index, gran) -> (q, scales)   rows x[token_index]
+    fp8_swiglu_quantize(h, gran)          -> (q, scales)   of BF16(silu(gate) * up)
 
 Granularities: "per_tensor", "1x128", "128x128", "mxfp8", "nvfp4", the
 block-wise recipe with power-of-two scales "1x128_pow2", "128x128_pow2", and
@@ -35,8 +37,10 @@ NVFP4_GRANS = (4, 7)
 FLAG_GIVEN_TENSOR_SCALE = 1
 FLAG_NVFP4_4OVER6 = 2
 STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNSUPPORTED",
-          -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE"}
+          -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE", -7: "FP8BS_EINDEX"}
+EINDEX = -7
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
+           "fp8_quantize_gathered", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
            "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm")
 
@@ -64,6 +68,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, P, I64, P]
     lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
     lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
+    lib.fp8_quantize_gathered.argtypes = [P, I64, I64, I64, P, I64, I, P, P, P, SZ, P]
+    lib.fp8_swiglu_quantize.argtypes = [P, I64, I64, I64, I, P, P, P]
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
@@ -72,7 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8bs_status_string.restype = ctypes.c_char_p
     lib.fp8bs_status_string.argtypes = [I]
     lib.fp8bs_version.argtypes = []
-    for name in ("fp8_quantize", "fp8_quantize_transposed", "fp8_block_gemm", "fp8_grouped_gemm",
+    for name in ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
+                 "fp8_quantize_gathered", "fp8_swiglu_quantize",
                  "fp8bs_read_status", "fp8bs_clear_status", "fp8bs_version", "fp8bs_test_stalled_gemm"):
         getattr(lib, name).restype = I
     _lib = lib
@@ -253,6 +260,55 @@ def fp8_grouped_gemm(a, a_scales, b, b_scales, offsets, gran, *, out=None, ws=No
                                          _stream(stream))
     _check("fp8_grouped_gemm", rc)
     return out
+
+
+def fp8_quantize_gathered(x: torch.Tensor, token_index: torch.Tensor, gran, *, q=None, scales=None, ws=None,
+                          stream=None):
+    """Quantise the rows x[token_index] (MoE dispatch into expert order); returns (q, scales).
+    An index outside [0, tokens) zeroes its row and sets FP8BS_EINDEX in the workspace
+    status word (read_status)."""
+    x = _as_bf16_2d(x)
+    g = _gran(gran)
+    tokens, cols = x.shape
+    if token_index.dtype != torch.int64 or not token_index.is_cuda or token_index.dim() != 1:
+        raise ValueError("token_index must be a 1-D CUDA int64 tensor")
+    if not token_index.is_contiguous():
+        raise ValueError("token_index must be contiguous")
+    rows = token_index.numel()
+    dev = x.device
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        shp, dt = scale_shape(g, rows, cols)
+        scales = torch.empty(shp, dtype=dt, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    rc = load_library().fp8_quantize_gathered(_ptr(x), tokens, cols, x.stride(0), _ptr(token_index), rows, g,
+                                              _ptr(q), _ptr(scales), _ptr(ws), ws.numel(), _stream(stream))
+    _check("fp8_quantize_gathered", rc)
+    return q, scales
+
+
+def fp8_swiglu_quantize(h: torch.Tensor, gran, inter: Optional[int] = None, *, q=None, scales=None, stream=None):
+    """Quantise y = BF16(silu(h[:, :inter]) * h[:, inter:2*inter]) row-wise; returns (q, scales)."""
+    h = _as_bf16_2d(h)
+    g = _gran(gran)
+    rows = h.shape[0]
+    if inter is None:
+        if h.shape[1] % 2:
+            raise ValueError("h must hold [gate | up] of equal widths")
+        inter = h.shape[1] // 2
+    if 2 * inter > h.shape[1]:
+        raise ValueError("h is narrower than 2 * inter")
+    dev = h.device
+    if q is None:
+        q = torch.empty((rows, inter), dtype=torch.uint8, device=dev)
+    if scales is None:
+        shp, dt = scale_shape(g, rows, inter)
+        scales = torch.empty(shp, dtype=dt, device=dev)
+    rc = load_library().fp8_swiglu_quantize(_ptr(h), rows, inter, h.stride(0), g, _ptr(q), _ptr(scales),
+                                            _stream(stream))
+    _check("fp8_swiglu_quantize", rc)
+    return q, scales
 
 
 def test_stalled_gemm(a, a_scales, b, b_scales, wait_limit_ns: int, *, out=None, ws=None, stream=None) -> int:

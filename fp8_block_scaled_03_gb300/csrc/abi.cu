@@ -77,6 +77,12 @@ bool bad_flags(int gran, unsigned flags) {
     return (flags & FP8BS_FLAG_NVFP4_4OVER6) && !is_nvfp4(gran);
 }
 
+// The row-wise granularities the MoE entry points produce (those a grouped
+// or dense GEMM consumes along K with one scale per row and group).
+inline bool is_moe_rowwise(int gran) {
+    return gran == FP8BS_TOKEN_1x128 || gran == FP8BS_MXFP8_1x32 || gran == FP8BS_TOKEN_1x128_POW2;
+}
+
 bool needs_partials(int gran, unsigned flags) {
     return (gran == FP8BS_PER_TENSOR || gran == FP8BS_NVFP4_1x16) && !(flags & FP8BS_FLAG_GIVEN_TENSOR_SCALE);
 }
@@ -147,6 +153,45 @@ int fp8_dequantize(const void* q, const void* scales, const float* tensor_scale,
         return FP8BS_EALIGN;
     return cuda_status(launch_dequantize(static_cast<const uint8_t*>(q), scales, tensor_scale, rows, cols, gran, out,
                                          ld_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quantize_gathered(const void* x, int64_t tokens, int64_t cols, int64_t ld_x,
+                          const int64_t* token_index, int64_t rows, int gran, void* q, void* scales,
+                          void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (tokens < 0 || rows < 0 || cols < 0) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
+    if (!is_moe_rowwise(gran)) return FP8BS_EUNSUPPORTED;
+    if (cols % 8 != 0 || ld_x < cols || ld_x % 8 != 0) return FP8BS_EINVAL;
+    if (rows == 0 || cols == 0) return FP8BS_OK;
+    // with no tokens x is never read (every index is out of range) and may be NULL
+    if ((x == nullptr && tokens > 0) || token_index == nullptr || q == nullptr || scales == nullptr)
+        return FP8BS_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || !scales_aligned(scales, gran) ||
+        (reinterpret_cast<uintptr_t>(token_index) & 7u))
+        return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    QuantJob j{};
+    j.x = static_cast<const uint16_t*>(x);
+    j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
+    j.q = static_cast<uint8_t*>(q); j.s = scales;
+    j.status = static_cast<int*>(workspace);
+    return cuda_status(launch_quantize_rows_src(j, token_index, tokens, 0, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h, int gran, void* q, void* scales,
+                        fp8bs_stream_t stream) {
+    if (rows < 0 || inter < 0) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
+    if (!is_moe_rowwise(gran)) return FP8BS_EUNSUPPORTED;
+    if (inter % 8 != 0 || ld_h < 2 * inter || ld_h % 8 != 0) return FP8BS_EINVAL;
+    if (rows == 0 || inter == 0) return FP8BS_OK;
+    if (h == nullptr || q == nullptr || scales == nullptr) return FP8BS_EINVAL;
+    if (!aligned16(h) || !aligned16(q) || !scales_aligned(scales, gran)) return FP8BS_EALIGN;
+    QuantJob j{};
+    j.x = static_cast<const uint16_t*>(h);
+    j.rows = rows; j.cols = inter; j.ldx = ld_h; j.gran = gran;
+    j.q = static_cast<uint8_t*>(q); j.s = scales;
+    return cuda_status(launch_quantize_rows_src(j, nullptr, 0, inter, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
@@ -276,6 +321,7 @@ const char* fp8bs_status_string(int status) {
     case FP8BS_ECUDA: return "CUDA runtime error or launch failure";
     case FP8BS_ETIMEOUT: return "a bounded device wait timed out";
     case FP8BS_EWORKSPACE: return "workspace missing or too small";
+    case FP8BS_EINDEX: return "a token index was out of range (its row was zeroed)";
     default: return "unknown status";
     }
 }

@@ -31,6 +31,12 @@ struct QuantJob {
 };
 int launch_quantize(const QuantJob& j, cudaStream_t s);
 int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
+// Row-wise quantisation (1x128, MXFP8, 1x128 power-of-two) of rows that
+// are not a plain matrix: gathered rows (token_index != null: row r is row
+// token_index[r] of x, x has `tokens` rows) or the SwiGLU activation (up > 0:
+// row r is silu(x[r, 0:cols]) * x[r, up:up+cols]).
+int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int64_t tokens, int64_t up,
+                             cudaStream_t s);
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                        float* scale, uint32_t* partials, int nparts, cudaStream_t s);
 

@@ -12,6 +12,7 @@
 namespace fp8bs {
 
 constexpr int kStatusTimeout = -5;                       // FP8BS_ETIMEOUT
+constexpr int kStatusIndex = -7;                         // FP8BS_EINDEX
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000 * 1000;  // 1 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

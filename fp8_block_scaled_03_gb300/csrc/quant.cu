@@ -105,12 +105,67 @@ amax_partials_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
     if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
+// ---------------------------------------------------------------- row sources
+// Where a row-wise quantiser's row r comes from: row r of x (plain); row
+// idx[r] of x (the MoE gather, rows in expert order); or the SwiGLU of row r
+// of the gate+up output, y = BF16(silu(gate) * up) with gate at columns
+// 0.. and up at columns `up`.. of that row.
+enum { kSrcPlain = 0, kSrcGather = 1, kSrcSwiglu = 2 };
+struct RowSrc {
+    const int64_t* idx;   // gather: source token of each row
+    int64_t tokens;       // gather: rows of x
+    int64_t up;           // SwiGLU: column where up starts
+    int* status;          // gather: sticky status word for an index out of range
+};
+
+// e^x in float32 by one fixed sequence (each operation one IEEE rounding,
+// no fused multiply-add): Cody and Waite's reduction x = n ln2 + r ("Software
+// Manual for the Elementary Functions", 1980) with ln 2 split into a 16-bit
+// head and a tail, the Taylor series of e^r to r^7 in Horner form, and the
+// scaling by 2^(n-1) * 2.  +inf above 89, 0 below -87 (where 1 + e^x is 1 in
+// float32 already).  Within 2 float32 ulps of e^x.
+__device__ __forceinline__ float exp_seq(float x) {
+    if (x > 0x1.64p+6f) return __int_as_float(0x7F800000);    // 89
+    if (x < -0x1.5cp+6f) return 0.0f;                           // -87
+    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));        // x / ln 2
+    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0x1.62e4p-1f)), __fmul_rn(n, 0x1.7f7d1cp-20f));
+    float p = 0x1.a01a02p-13f;                                  // 1/7!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);            // 1/6!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);             // 1/5!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);             // 1/4!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);             // 1/3!
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const int ni = max(min((int)n, 128), -126) - 1;             // 2^(n-1) is a float32 (>= 2^-127)
+    const float half = ni >= -126 ? __int_as_float((ni + 127) << 23) : __int_as_float(0x00400000);
+    return __fmul_rn(__fmul_rn(p, half), 2.0f);
+}
+
+// Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up.
+__device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
+    float g[8], u[8], y[8];
+    unpack8(gv, g);
+    unpack8(uv, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(__fdiv_rn(g[i], __fadd_rn(1.0f, exp_seq(-g[i]))), u[i]);
+    uint4 o;
+    uint32_t* ow = &o.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+        ow[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return o;
+}
+
 // ---------------------------------------------------------------- row-wise 1x128 / 1x32 / per-tensor
-template <int GRAN>
+template <int GRAN, int SRC = kSrcPlain>
 __global__ void __launch_bounds__(kThreads)
 quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                   uint8_t* __restrict__ q, void* __restrict__ sout,
-                  const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
+                  const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given,
+                  RowSrc src = RowSrc{}) {
     const int lane = threadIdx.x & 31;
     float s_uniform = 1.0f;
     if constexpr (GRAN == kGranPT) {
@@ -129,11 +184,31 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
     for (int64_t t = gw; t < total; t += nw) {
         const int64_t r = t / segs;
         const int64_t cb = (t - r * segs) * kSeg;
+        const uint16_t* xr = x + r * ldx;
+        bool valid = true;
+        if constexpr (SRC == kSrcGather) {
+            const int64_t tok = __ldg(src.idx + r);
+            valid = tok >= 0 && tok < src.tokens;
+            xr = x + (valid ? tok : 0) * ldx;
+            if (!valid && lane == 0 && cb == 0 && src.status != nullptr) atomicExch(src.status, kStatusIndex);
+        }
         uint4 v[4];
+        if constexpr (SRC == kSrcSwiglu) {
+            uint4 gv[4], uv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t c = cb + j * 256 + lane * 8;
-            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 4; ++j) {
+                const int64_t c = cb + j * 256 + lane * 8;
+                gv[j] = (c < cols) ? ldg_v4(xr + c) : make_uint4(0, 0, 0, 0);
+                uv[j] = (c < cols) ? ldg_v4(xr + src.up + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = swiglu8(gv[j], uv[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t c = cb + j * 256 + lane * 8;
+                v[j] = (c < cols && valid) ? ldg_v4(xr + c) : make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -793,6 +868,35 @@ int launch_quantize(const QuantJob& j, cudaStream_t st) {
         return (int)cudaErrorInvalidValue;
     }
     return (int)cudaGetLastError();
+}
+
+template <int SRC>
+static int launch_rows_src(const QuantJob& j, const RowSrc& src, int nb, cudaStream_t st) {
+    switch (j.gran) {
+    case kGranTok:
+        quant_rows_kernel<kGranTok, SRC><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0,
+                                                                  nullptr, src);
+        break;
+    case kGranMx:
+        quant_rows_kernel<kGranMx, SRC><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0,
+                                                                 nullptr, src);
+        break;
+    case kGranTokP2:
+        quant_rows_kernel<kGranTokP2, SRC><<<nb, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.q, j.s, nullptr, 0,
+                                                                    nullptr, src);
+        break;
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+    return (int)cudaGetLastError();
+}
+
+int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int64_t tokens, int64_t up,
+                             cudaStream_t st) {
+    const int nb = rowwise_blocks(j.rows, j.cols, sm_count() * 8);
+    RowSrc src{token_index, tokens, up, j.status};
+    if (token_index != nullptr) return launch_rows_src<kSrcGather>(j, src, nb, st);
+    return launch_rows_src<kSrcSwiglu>(j, src, nb, st);
 }
 
 template <int GRAN, bool DUAL>

@@ -35,7 +35,8 @@
  *   - `workspace` is a caller-owned device buffer of at least
  *     FP8BS_WORKSPACE_BYTES bytes, zero-filled once by the caller before its
  *     first use.  Its first 4 bytes are a sticky device status word that
- *     kernels set (never clear) when a bounded wait gives up; read it with
+ *     kernels set (never clear) when a bounded wait gives up or a gathered
+ *     token index is out of range; read it with
  *     fp8bs_read_status and clear it with fp8bs_clear_status.  The rest is
  *     scratch for the per-tensor / NVFP4 amax reduction.  Calls that share a
  *     workspace must be ordered on the GPU (same stream or events).
@@ -60,7 +61,8 @@ typedef enum {
     FP8BS_EUNSUPPORTED = -3,  /* valid request this library does not implement */
     FP8BS_ECUDA = -4,         /* a CUDA runtime call or launch failed */
     FP8BS_ETIMEOUT = -5,      /* (status word) a bounded device wait gave up */
-    FP8BS_EWORKSPACE = -6     /* workspace NULL or smaller than required */
+    FP8BS_EWORKSPACE = -6,    /* workspace NULL or smaller than required */
+    FP8BS_EINDEX = -7         /* (status word) a gathered token index was out of range */
 } fp8bs_status;
 
 typedef enum {
@@ -175,6 +177,58 @@ int fp8_dequantize(const void* q, const void* scales, const float* tensor_scale,
                    int gran, void* out, int64_t ld_out, fp8bs_stream_t stream);
 
 /*
+ * fp8_quantize_gathered -- quantise the rows x[token_index[r]] (r = 0 ..
+ * rows-1) of a BF16 token matrix x [tokens, cols] in one pass: the MoE
+ * dispatch that lays the routed tokens out in expert order for the grouped
+ * GEMM ("Low Precision RL", section "3. Unified MXFP8 (Blackwell)": MoE
+ * layers run their own GEMM backend on the routed tokens).  The pages do not
+ * describe this step; it computes exactly fp8_quantize of the gathered BF16
+ * matrix.
+ *
+ *   x            BF16 [tokens, cols], pitch ld_x (ld_x >= cols, ld_x % 8 == 0),
+ *                16-byte aligned; cols % 8 == 0
+ *   token_index  DEVICE int64 [rows], 8-byte aligned: the source token of
+ *                each output row (repeats allowed: a token routed to k
+ *                experts appears k times)
+ *   gran         TOKEN_1x128, MXFP8_1x32 or TOKEN_1x128_POW2 (the other
+ *                valid granularities return FP8BS_EUNSUPPORTED)
+ *   q, scales    as fp8_quantize for [rows, cols] at `gran`
+ *   workspace    required (FP8BS_WORKSPACE_BYTES): its status word receives
+ *                FP8BS_EINDEX when an index is outside [0, tokens); such a
+ *                row is quantised as an all-zero row (zero codes, scale of
+ *                an all-zero group) and the other rows are unaffected.
+ * rows or cols == 0 is a no-op.  tokens may be 0 (then every index is out
+ * of range and x may be NULL).
+ */
+int fp8_quantize_gathered(const void* x, int64_t tokens, int64_t cols, int64_t ld_x,
+                          const int64_t* token_index, int64_t rows, int gran, void* q, void* scales,
+                          void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8_swiglu_quantize -- the SwiGLU activation between the gate+up and the
+ * down projection of an expert MLP, quantised row-wise for the down GEMM
+ * (Qwen3 MoE experts, "Low Precision RL", section "3. Unified MXFP8
+ * (Blackwell)"; the pages do not describe this step).
+ *
+ *   h       BF16 [rows, 2 * inter] = [gate | up] (gate in columns 0 ..
+ *           inter-1, up in inter .. 2*inter-1), pitch ld_h >= 2 * inter,
+ *           ld_h % 8 == 0, 16-byte aligned; inter % 8 == 0
+ *   y[r,c]  = BF16_RNE(silu(g) * u), g = h[r,c], u = h[r,inter+c],
+ *           silu(g) = g / (1 + e^-g), all in IEEE float32 without fused
+ *           multiply-add; e^t is evaluated by one fixed sequence: n =
+ *           rint(t * RN(log2 e)), r = (t - n * L_hi) - n * L_lo with ln 2 =
+ *           L_hi + L_lo (L_hi = 0x1.62e4p-1), Taylor series of e^r to r^7 by
+ *           Horner's rule, times 2^(n-1), times 2; +inf for t > 89, 0 for
+ *           t < -87 (within 2 float32 ulps of e^t)
+ *   gran    TOKEN_1x128, MXFP8_1x32 or TOKEN_1x128_POW2 (other valid
+ *           granularities return FP8BS_EUNSUPPORTED)
+ *   q, scales  as fp8_quantize of y [rows, inter] at `gran`
+ * rows or inter == 0 is a no-op.  y itself is not written.
+ */
+int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h, int gran, void* q, void* scales,
+                        fp8bs_stream_t stream);
+
+/*
  * fp8_block_gemm -- D[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], D in BF16.
  *
  * The matching low-precision GEMM of "Low Precision RL" ("Unified training
@@ -284,7 +338,8 @@ int fp8_quantize_per_tensor_noalloc(const void* x, int64_t rows, int64_t cols, i
 size_t fp8bs_workspace_size(void);
 
 /* Synchronises `stream`, then returns the sticky device status word of
- * `workspace` (FP8BS_OK, or FP8BS_ETIMEOUT if a bounded wait gave up), or
+ * `workspace` (FP8BS_OK, FP8BS_ETIMEOUT if a bounded wait gave up, or
+ * FP8BS_EINDEX if fp8_quantize_gathered met an index out of range), or
  * FP8BS_ECUDA if the copy failed. */
 int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream);
 

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings_and_sizes(lib):
     assert lib.fp8bs_workspace_size() == 16384
     assert lib.fp8bs_version() == 100
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert fp.status_string(code) != "unknown status"
     assert fp.status_string(7) == "unknown status"
 
@@ -67,7 +67,6 @@ def test_quantize_transposed_rejects_bad_arguments(lib):
 
 def test_gemm_rejects_bad_arguments(lib):
     g = lib.fp8_block_gemm
-    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, FAKE, 16384, None) != 0 or True
     assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, None, 0, None) == -6
     assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 132, 256, FAKE, FAKE, 16384, None) == -1  # n % 8
     assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 0, 128, 256, FAKE, FAKE, 16384, None) == -1
@@ -123,3 +122,37 @@ def test_gemm_row_scaled_nvfp4_arguments(lib):
     assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, None, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -1  # A S_g
     assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, ODD4, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -2
     assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, FAKE, 16384, None) == -1  # k % 256
+
+
+def test_gathered_quantize_rejects_bad_arguments(lib):
+    g = lib.fp8_quantize_gathered
+    WS = 16384
+    assert g(None, 8, 128, 128, FAKE, 4, 1, FAKE, FAKE, FAKE, WS, None) == -1       # null x
+    assert g(FAKE, 8, 128, 128, None, 4, 1, FAKE, FAKE, FAKE, WS, None) == -1       # null index
+    assert g(FAKE, 8, 124, 128, FAKE, 4, 1, FAKE, FAKE, FAKE, WS, None) == -1       # cols % 8
+    assert g(FAKE, 8, 128, 120, FAKE, 4, 1, FAKE, FAKE, FAKE, WS, None) == -1       # ld < cols
+    assert g(FAKE, -1, 128, 128, FAKE, 4, 1, FAKE, FAKE, FAKE, WS, None) == -1      # negative tokens
+    assert g(FAKE, 8, 128, 128, FAKE, 4, 9, FAKE, FAKE, FAKE, WS, None) == -1       # bad gran
+    for unsupported in (0, 2, 4, 6, 7):
+        assert g(FAKE, 8, 128, 128, FAKE, 4, unsupported, FAKE, FAKE, FAKE, WS, None) == -3
+    assert g(FAKE, 8, 128, 128, ODD4, 4, 3, FAKE, FAKE, FAKE, WS, None) == -2       # index 8-byte aligned
+    assert g(MISALIGNED, 8, 128, 128, FAKE, 4, 3, FAKE, FAKE, FAKE, WS, None) == -2
+    assert g(FAKE, 8, 128, 128, FAKE, 4, 1, FAKE, ODD4, FAKE, WS, None) == -2       # FP32 scales
+    assert g(FAKE, 8, 128, 128, FAKE, 4, 3, FAKE, FAKE, None, 0, None) == -6        # status word needed
+    assert g(FAKE, 8, 128, 128, FAKE, 4, 3, FAKE, FAKE, FAKE, 1024, None) == -6
+    assert g(None, 0, 128, 128, None, 0, 3, None, None, None, 0, None) == 0         # empty: no-op
+
+
+def test_swiglu_quantize_rejects_bad_arguments(lib):
+    s = lib.fp8_swiglu_quantize
+    assert s(None, 4, 128, 256, 3, FAKE, FAKE, None) == -1          # null h
+    assert s(FAKE, 4, 124, 256, 3, FAKE, FAKE, None) == -1          # inter % 8
+    assert s(FAKE, 4, 128, 248, 3, FAKE, FAKE, None) == -1          # ld_h < 2 * inter
+    assert s(FAKE, 4, 128, 260, 3, FAKE, FAKE, None) == -1          # ld_h % 8
+    assert s(FAKE, -4, 128, 256, 3, FAKE, FAKE, None) == -1
+    for unsupported in (0, 2, 4, 6, 7):
+        assert s(FAKE, 4, 128, 256, unsupported, FAKE, FAKE, None) == -3
+    assert s(MISALIGNED, 4, 128, 256, 3, FAKE, FAKE, None) == -2
+    assert s(FAKE, 4, 128, 256, 5, MISALIGNED, FAKE, None) == -2
+    assert s(None, 0, 128, 256, 3, None, None, None) == 0           # empty: no-op
+    assert s(None, 4, 0, 0, 3, None, None, None) == 0
