@@ -14,15 +14,18 @@
 // CTA: 384 threads, one CTA per SM (persistent), tile 128 x 256.
 //   warp 0      TMA producer: A 128 x 128 B and B 256 x 128 B boxes per stage
 //               (128 FP8 or 256 FP4 K-elements), 128-byte swizzle.
-//   warp 1      TMEM owner + MMA issuer: per stage, tcgen05.cp of the scale
-//               atoms to TMEM, then 4 block-scaled MMAs (M128 N256; K32 for
-//               MXFP8, K64 for NVFP4), accumulating the whole K range in TMEM.
+//   warp 1      TMEM owner + MMA issuer: per stage 4 block-scaled MMAs
+//               (M128 N256; K32 for MXFP8, K64 for NVFP4), accumulating the
+//               whole K range in TMEM (MXFP8 and power-of-two: after the
+//               tcgen05.cp of the stage's scale atoms).
 //   warps 2-3   scale loaders, taking turns by stage (power-of-two scales:
 //               by group of four stages, read with one load per row): read
 //               the row-major scale bytes of the stage's rows and write them
 //               in the 32 x 16-byte atom layout that tcgen05.cp
 //               32x128b.warpx4 replicates into all TMEM lane quarters (row
-//               r0 + 32*r1 at byte r0*16 + r1*4).
+//               r0 + 32*r1 at byte r0*16 + r1*4); for NVFP4 they also issue
+//               the tcgen05.cp of those atoms to TMEM (elsewhere the MMA
+//               thread does, before its MMAs).
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
 //               128 columns per thread) to BF16 registers, release TMEM, store.
 // TMEM: columns 0..255 accumulator, 256.. scale factors per stage.
@@ -82,6 +85,7 @@ struct Params {
 template <int STAGES>
 struct alignas(16) Shared {
     uint64_t full[STAGES], empty[STAGES], tfull, tempty, drain;
+    uint64_t ldrain[2];    // per scale loader: its scale copies have landed (exit path)
     uint32_t tmem_base;
     int abort;
     SchedShared sched;
@@ -239,6 +243,33 @@ __device__ __forceinline__ void group_stage(ScaleRegs<KIND>& r, const WideRegs& 
     for (int r1 = 0; r1 < 8; ++r1) r.b[r1][0] = w.b[r1][g];
 }
 
+// Copy a stage's scale atoms from shared memory into its TMEM columns
+// (tcgen05.cp 32x128b.warpx4, one per 512-byte atom: A atoms first, then B).
+// One copy takes about 60 cycles to issue.  An NVFP4 stage has 12, more
+// than its MMAs take, so there the loader that wrote the atoms issues them
+// (copies of alternate stages go out from two threads, and the loader's
+// tcgen05.commit on the stage's full barrier arrives once they have landed).
+// MXFP8 and power-of-two stages have 3, and measured faster issued by the
+// MMA thread just before its MMAs.
+template <int KIND> constexpr bool kLoaderCopies = (KIND == kNv);
+
+template <int KIND>
+__device__ __forceinline__ void copy_scales_to_tmem(uint32_t sf_tmem, uint32_t sf_smem) {
+    constexpr int NA = Cfg<KIND>::A_ATOMS, NB = Cfg<KIND>::B_ATOMS;
+#pragma unroll
+    for (int j = 0; j < NA + NB; ++j) tmem_cp_32x128b_x4(sf_tmem + 4 * j, smem_desc(sf_smem + 512 * j, 0, 128, 0));
+}
+
+// Before a loader warp exits, its last scale copies must have landed (on an
+// aborted run the MMA thread may not have waited for them).
+__device__ __forceinline__ void drain_scale_copies(uint32_t bar, int lane, uint64_t limit_ns) {
+    if (lane == 0) {
+        mma_commit(bar);
+        mbar_wait_drain(bar, 0, limit_ns);
+    }
+    __syncwarp();
+}
+
 template <int KIND, int SA, int SB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
@@ -262,6 +293,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         mbar_init(smem_u32(&sh->tfull), 1);
         mbar_init(smem_u32(&sh->tempty), 8);
         mbar_init(smem_u32(&sh->drain), 1);
+        mbar_init(smem_u32(&sh->ldrain[0]), 1);
+        mbar_init(smem_u32(&sh->ldrain[1]), 1);
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -322,15 +355,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const uint32_t a_addr = smem_u32(st);
                     const uint64_t adesc = kmajor_sw128_desc(a_addr);
                     const uint64_t bdesc = kmajor_sw128_desc(a_addr + A_BYTES);
-                    const uint32_t sf_addr = a_addr + A_BYTES + B_BYTES;
                     const uint32_t sfa = tmem + 256 + s * SF_COLS;
                     const uint32_t sfb = sfa + 4 * Cfg<KIND>::A_ATOMS;
-#pragma unroll
-                    for (int j = 0; j < Cfg<KIND>::A_ATOMS; ++j)
-                        tmem_cp_32x128b_x4(sfa + 4 * j, smem_desc(sf_addr + 512 * j, 0, 128, 0));
-#pragma unroll
-                    for (int j = 0; j < Cfg<KIND>::B_ATOMS; ++j)
-                        tmem_cp_32x128b_x4(sfb + 4 * j, smem_desc(sf_addr + 512 * (Cfg<KIND>::A_ATOMS + j), 0, 128, 0));
+                    if constexpr (!kLoaderCopies<KIND>)
+                        copy_scales_to_tmem<KIND>(sfa, a_addr + A_BYTES + B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -451,10 +479,18 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     if (st_t >= total || !ok) break;
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
-                    store_scales<KIND>(ring[d], stages + s * STAGE_B + A_BYTES + B_BYTES, lane);
+                    uint8_t* sf = stages + s * STAGE_B + A_BYTES + B_BYTES;
+                    store_scales<KIND>(ring[d], sf, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
+                    if (lane == 0) {
+                        if constexpr (kLoaderCopies<KIND>) {
+                            copy_scales_to_tmem<KIND>(tmem + 256 + s * SF_COLS, smem_u32(sf));
+                            mma_commit(smem_u32(&sh->full[s]));
+                        } else {
+                            mbar_arrive(smem_u32(&sh->full[s]));
+                        }
+                    }
                     it += 2;
                     if (lt < total) {
                         load_scales<KIND, SA, SB>(ring[d], p, lti, lkb, lane, sf_pitch);
@@ -465,6 +501,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     if (st_t < total) step_store();
                 }
             }
+            if constexpr (kLoaderCopies<KIND>) drain_scale_copies(smem_u32(&sh->ldrain[warp - 2]), lane, p.wait_ns);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue (8 warps)

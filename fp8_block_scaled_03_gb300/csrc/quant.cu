@@ -79,6 +79,30 @@ __device__ __forceinline__ float tensor_amax(const uint32_t* __restrict__ partia
     return amax_bits_to_f32(block_max_u32(m));
 }
 
+// ---------------------------------------------------------------- warp task cursor
+// A warp's tasks are t = gw, gw + nw, ...; task t is segment t % segs of row
+// t / segs.  Both parts advance by a constant per stride, so a task loop
+// divides once, not once per task.
+struct TaskCursor {
+    int64_t r, si;               // current row and segment
+    int64_t dr, ds, segs;
+    __device__ __forceinline__ TaskCursor(int64_t gw, int64_t nw, int64_t segs_) : segs(segs_) {
+        r = gw / segs;
+        si = gw - r * segs;
+        dr = nw / segs;
+        ds = nw - dr * segs;
+    }
+    __device__ __forceinline__ int64_t next_row() const { return r + dr + (si + ds >= segs ? 1 : 0); }
+    __device__ __forceinline__ void advance() {
+        si += ds;
+        r += dr;
+        if (si >= segs) {
+            si -= segs;
+            ++r;
+        }
+    }
+};
+
 // ---------------------------------------------------------------- pass 1: amax partials
 __global__ void __launch_bounds__(kThreads)
 amax_partials_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
@@ -181,28 +205,32 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
     const int64_t segs = ceil_div(cols, kSeg);
     const int64_t total = rows * segs;
     const int64_t ng = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
-    for (int64_t t = gw; t < total; t += nw) {
-        const int64_t r = t / segs;
-        const int64_t cb = (t - r * segs) * kSeg;
+    TaskCursor tc(gw, nw, segs);
+    int64_t tok_next = 0;     // gather: the next task's token, loaded one task ahead
+    if constexpr (SRC == kSrcGather) {
+        if (gw < total) tok_next = __ldg(src.idx + tc.r);
+    }
+    for (int64_t t = gw; t < total; t += nw, tc.advance()) {
+        const int64_t r = tc.r;
+        const int64_t cb = tc.si * kSeg;
         const uint16_t* xr = x + r * ldx;
         bool valid = true;
         if constexpr (SRC == kSrcGather) {
-            const int64_t tok = __ldg(src.idx + r);
+            const int64_t tok = tok_next;
+            if (t + nw < total) tok_next = __ldg(src.idx + tc.next_row());
             valid = tok >= 0 && tok < src.tokens;
             xr = x + (valid ? tok : 0) * ldx;
             if (!valid && lane == 0 && cb == 0 && src.status != nullptr) atomicExch(src.status, kStatusIndex);
         }
         uint4 v[4];
+        uint4 uv[SRC == kSrcSwiglu ? 4 : 1];   // SwiGLU: v holds gate, uv up, until group j is formed
         if constexpr (SRC == kSrcSwiglu) {
-            uint4 gv[4], uv[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int64_t c = cb + j * 256 + lane * 8;
-                gv[j] = (c < cols) ? ldg_v4(xr + c) : make_uint4(0, 0, 0, 0);
+                v[j] = (c < cols) ? ldg_v4(xr + c) : make_uint4(0, 0, 0, 0);
                 uv[j] = (c < cols) ? ldg_v4(xr + src.up + c) : make_uint4(0, 0, 0, 0);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = swiglu8(gv[j], uv[j]);
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -214,6 +242,9 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
         for (int j = 0; j < 4; ++j) {
             const int64_t c = cb + j * 256 + lane * 8;
             const bool ok = c < cols;
+            if constexpr (SRC == kSrcSwiglu) {
+                if (ok) v[j] = swiglu8(v[j], uv[j]);
+            }
             float f[8];
             unpack8(v[j], f);
             uint2 o;
@@ -235,7 +266,12 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
             } else {
                 o = cast8_div(f, s_uniform);
             }
-            if (ok) *reinterpret_cast<uint2*>(q + r * cols + c) = o;
+            if (ok) {
+                if constexpr (SRC == kSrcGather)
+                    stg_cs_v2(q + r * cols + c, o);
+                else
+                    *reinterpret_cast<uint2*>(q + r * cols + c) = o;
+            }
         }
     }
 }
@@ -344,10 +380,8 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t segs = ceil_div(cols, kSeg);
     const int64_t total = rows * segs;
-    for (int64_t t = gw; t < total; t += nw) {
-        const int64_t r = t / segs;
-        nvfp4_segment<FOS>(x, r, (t - r * segs) * kSeg, cols, ldx, q, sb, s_g, lane);
-    }
+    TaskCursor tc(gw, nw, segs);
+    for (int64_t t = gw; t < total; t += nw, tc.advance()) nvfp4_segment<FOS>(x, tc.r, tc.si * kSeg, cols, ldx, q, sb, s_g, lane);
 }
 
 // One outer scale per row (per token): a warp owns a row, reads it once for
