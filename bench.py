@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--kernel", default=None,
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
                              "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "moe_gather_quant",
-                             "moe_swiglu_quant", "nvfp4"],
+                             "moe_swiglu_quant", "moe_layer", "nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
@@ -542,6 +542,29 @@ def single_kernel(args, torch, fp, dev):
             q, s_, _ = fp.fp8_quantize(x, g, ws=ws)
             fn = lambda: fp.fp8_quantize(x, g, q=q, scales=s_, ws=ws)  # noqa: E731
         work = 0
+    elif name == "moe_layer":
+        # the four kernels of the expert MLP, as the bench's moe_mxfp8.layer times them
+        import synth
+        token_index, offsets = synth.moe_routing(16384, 128, 8, seed=0)
+        rows = int(offsets[-1])
+        x = act((16384, 2048), 0.001, 100.0)
+        idx = torch.from_numpy(token_index).to(dev)
+        off = torch.from_numpy(offsets).to(dev)
+        qgu, sgu, _ = fp.fp8_quantize(wt((128 * 1536, 2048)), "mxfp8", ws=ws)
+        qdn, sdn, _ = fp.fp8_quantize(wt((128 * 2048, 768)), "mxfp8", ws=ws)
+        qgu, sgu = qgu.view(128, 1536, 2048), sgu.view(128, 1536, 64)
+        qdn, sdn = qdn.view(128, 2048, 768), sdn.view(128, 2048, 24)
+        qa, sa = fp.fp8_quantize_gathered(x, idx, "mxfp8", ws=ws)
+        h = torch.empty((rows, 1536), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((rows, 2048), dtype=torch.bfloat16, device=dev)
+        qy, sy = fp.fp8_swiglu_quantize(h, "mxfp8")
+
+        def fn():
+            fp.fp8_quantize_gathered(x, idx, "mxfp8", q=qa, scales=sa, ws=ws)
+            fp.fp8_grouped_gemm(qa, sa, qgu, sgu, off, "mxfp8", out=h, ws=ws)
+            fp.fp8_swiglu_quantize(h, "mxfp8", q=qy, scales=sy)
+            fp.fp8_grouped_gemm(qy, sy, qdn, sdn, off, "mxfp8", out=out, ws=ws)
+        work = 2 * rows * 1536 * 2048 + 2 * rows * 2048 * 768
     elif name in ("moe_gather_quant", "moe_swiglu_quant"):
         import synth
         token_index, offsets = synth.moe_routing(16384, 128, 8, seed=0)

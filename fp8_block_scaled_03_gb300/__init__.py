@@ -42,7 +42,7 @@ EINDEX = -7
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
            "fp8_quantize_gathered", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
-           "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm")
+           "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4")
 
 _lib = None
 
@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_quantize_gathered.argtypes = [P, I64, I64, I64, P, I64, I, P, P, P, SZ, P]
     lib.fp8_swiglu_quantize.argtypes = [P, I64, I64, I64, I, P, P, P]
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
+    lib.fp8bs_test_stalled_gemm_nvfp4.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
+    lib.fp8bs_test_stalled_gemm_nvfp4.restype = I
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
     lib.fp8bs_read_status.argtypes = [P, P]
@@ -323,3 +325,17 @@ def test_stalled_gemm(a, a_scales, b, b_scales, wait_limit_ns: int, *, out=None,
     return load_library().fp8bs_test_stalled_gemm(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), m, n, k,
                                                   _ptr(out), int(wait_limit_ns), _ptr(ws), ws.numel(),
                                                   _stream(stream))
+
+
+def test_stalled_gemm_nvfp4(a, a_scales, b, b_scales, a_tensor_scale, b_tensor_scale, wait_limit_ns: int, *, k=None,
+                            out=None, ws=None, stream=None) -> int:
+    """As test_stalled_gemm, for the NVFP4 GEMM (packed codes [rows, k/2])."""
+    m, n = a.shape[0], b.shape[0]
+    k = k if k is not None else 2 * a.shape[1]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    ws = ws if ws is not None else workspace(a.device)
+    return load_library().fp8bs_test_stalled_gemm_nvfp4(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales),
+                                                        _ptr(a_tensor_scale), _ptr(b_tensor_scale), m, n, k,
+                                                        _ptr(out), int(wait_limit_ns), _ptr(ws), ws.numel(),
+                                                        _stream(stream))

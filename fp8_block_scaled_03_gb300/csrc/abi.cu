@@ -296,6 +296,31 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
     return cuda_status(launch_gemm_mx(j, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const void* b, const void* b_scales,
+                                  const float* a_tensor_scale, const float* b_tensor_scale, int64_t m, int64_t n,
+                                  int64_t k, void* d, uint64_t wait_limit_ns, void* workspace,
+                                  size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr ||
+        a_tensor_scale == nullptr || b_tensor_scale == nullptr)
+        return FP8BS_EINVAL;
+    if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 256 != 0) return FP8BS_EINVAL;
+    if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return FP8BS_EINVAL;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(a_scales) || !aligned16(b_scales) ||
+        !aligned4(a_tensor_scale) || !aligned4(b_tensor_scale))
+        return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    GemmJob j{};
+    j.a = a; j.sa = a_scales; j.a_gran = FP8BS_NVFP4_1x16;
+    j.b = b; j.sb = b_scales; j.b_gran = FP8BS_NVFP4_1x16;
+    j.a_ts = a_tensor_scale; j.b_ts = b_tensor_scale;
+    j.m = m; j.n = n; j.k = k; j.d = d;
+    j.status = static_cast<int*>(workspace);
+    j.offsets = nullptr; j.experts = 0;
+    j.wait_ns = wait_limit_ns;
+    j.stall_stage0 = 1;
+    return cuda_status(launch_gemm_mx(j, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t fp8bs_workspace_size(void) { return kWorkspaceBytes; }
 
 int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream) {

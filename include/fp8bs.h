@@ -302,6 +302,18 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
                             void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
 
 /*
+ * fp8bs_test_stalled_gemm_nvfp4 -- as fp8bs_test_stalled_gemm for the
+ * NVFP4 GEMM (both operands NVFP4_1x16, tensor scales as fp8_block_gemm,
+ * k % 256 == 0, block scales 16-byte aligned).  Its scale loaders issue the
+ * scale copies to tensor memory themselves, so this also covers their
+ * drain on the abort path.  The contents of d are unspecified afterwards.
+ */
+int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const void* b, const void* b_scales,
+                                  const float* a_tensor_scale, const float* b_tensor_scale, int64_t m, int64_t n,
+                                  int64_t k, void* d, uint64_t wait_limit_ns, void* workspace,
+                                  size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
  * fp8_quantize_per_tensor_noalloc -- fp8_quantize(gran = PER_TENSOR) for
  * callers that cannot allocate device memory.  The pages have no
  * counterpart: this is an interface variant, not a different computation.

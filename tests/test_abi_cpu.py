@@ -156,3 +156,13 @@ def test_swiglu_quantize_rejects_bad_arguments(lib):
     assert s(FAKE, 4, 128, 256, 5, MISALIGNED, FAKE, None) == -2
     assert s(None, 0, 128, 256, 3, None, None, None) == 0           # empty: no-op
     assert s(None, 4, 0, 0, 3, None, None, None) == 0
+
+
+def test_stalled_gemm_nvfp4_rejects_bad_arguments(lib):
+    t = lib.fp8bs_test_stalled_gemm_nvfp4
+    WS = 16384
+    assert t(FAKE, FAKE, FAKE, FAKE, None, FAKE, 128, 128, 256, FAKE, 1000, FAKE, WS, None) == -1   # S_g A
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 128, FAKE, 1000, FAKE, WS, None) == -1   # k % 256
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 0, FAKE, WS, None) == -1      # no bound
+    assert t(FAKE, ODD4, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 1000, FAKE, WS, None) == -2   # scales
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 1000, None, 0, None) == -6

@@ -35,3 +35,25 @@ def test_stalled_pipeline_times_out_and_recovers():
     cb, eb = OQ.quantize_mxfp8(to_f32(bb))
     assert_gemm_close(bf16_to_f64(d), OG.gemm_bf16(OG.dequant_mxfp8(ca, ea), OG.dequant_mxfp8(cb, eb)))
     assert fp.read_status(ws) == 0
+
+
+def test_stalled_nvfp4_pipeline_times_out_and_recovers():
+    """The NVFP4 GEMM's scale loaders issue the tensor-memory copies and
+    drain them before exit; a stalled stage must still end in a timeout
+    status with the context usable and the next GEMM correct."""
+    ws = torch.zeros(fp.load_library().fp8bs_workspace_size(), dtype=torch.uint8, device="cuda")
+    ab = synth.activations((256, 512), seed=3)
+    bb = synth.weights((256, 512), seed=4)
+    qa, sa, ta = fp.fp8_quantize(to_dev_bf16(ab), "nvfp4", ws=ws)
+    qb, sb, tb = fp.fp8_quantize(to_dev_bf16(bb), "nvfp4", ws=ws)
+    assert fp.read_status(ws) == 0
+    rc = fp.test_stalled_gemm_nvfp4(qa, sa, qb, sb, ta, tb, 50_000_000, ws=ws)   # 50 ms bound
+    assert rc == 0
+    assert fp.read_status(ws) == -5
+    fp.clear_status(ws)
+    d = fp.fp8_block_gemm(qa, sa, "nvfp4", qb, sb, "nvfp4", ta, tb, k=512, ws=ws)
+    pa, sba, sga = OQ.quantize_nvfp4(to_f32(ab))
+    pb, sbb, sgb = OQ.quantize_nvfp4(to_f32(bb))
+    ref = OG.gemm_bf16(OG.dequant_nvfp4(pa, sba, sga), OG.dequant_nvfp4(pb, sbb, sgb))
+    assert_gemm_close(bf16_to_f64(d), ref)
+    assert fp.read_status(ws) == 0
