@@ -42,7 +42,8 @@ EINDEX = -7
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
            "fp8_quantize_gathered", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
-           "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4")
+           "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4",
+           "fp8bs_test_quotient_sweep")
 
 _lib = None
 
@@ -73,6 +74,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.restype = I
+    lib.fp8bs_test_quotient_sweep.argtypes = [P, P]
+    lib.fp8bs_test_quotient_sweep.restype = I
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
     lib.fp8bs_read_status.argtypes = [P, P]
@@ -339,3 +342,11 @@ def test_stalled_gemm_nvfp4(a, a_scales, b, b_scales, a_tensor_scale, b_tensor_s
                                                         _ptr(a_tensor_scale), _ptr(b_tensor_scale), m, n, k,
                                                         _ptr(out), int(wait_limit_ns), _ptr(ws), ws.numel(),
                                                         _stream(stream))
+
+
+def test_quotient_sweep(stream=None):
+    """Run fp8bs_test_quotient_sweep; returns (pairs, code mismatches, fast-path amax values)."""
+    counts = torch.zeros(3, dtype=torch.int64, device="cuda")
+    _check("fp8bs_test_quotient_sweep", load_library().fp8bs_test_quotient_sweep(_ptr(counts), _stream(stream)))
+    c = counts.cpu().tolist()
+    return c[0], c[1], c[2]

@@ -43,10 +43,10 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 }
 
 // Eight elements x / S -> eight E4M3 bytes.
-__device__ __forceinline__ uint2 cast8_div(const float* f, float s) {
+__device__ __forceinline__ uint2 cast8_div(const float* f, const ScaleDiv& d) {
     uint2 o;
-    o.x = e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-    o.y = e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    o.x = e4m3x4(div_scale(f[0], d), div_scale(f[1], d), div_scale(f[2], d), div_scale(f[3], d));
+    o.y = e4m3x4(div_scale(f[4], d), div_scale(f[5], d), div_scale(f[6], d), div_scale(f[7], d));
     return o;
 }
 
@@ -200,6 +200,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
             if (blockIdx.x == 0 && threadIdx.x == 0) static_cast<float*>(sout)[0] = s_uniform;
         }
     }
+    const ScaleDiv sd_uniform = scale_div(s_uniform, given == nullptr);
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t segs = ceil_div(cols, kSeg);
@@ -251,7 +252,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
             if constexpr (GRAN == kGranTok) {
                 const uint32_t m = warp_max_u32(absmax_v4(v[j]), 16);
                 const float s = fp32_scale_from_amax(amax_bits_to_f32(m));
-                o = cast8_div(f, s);
+                o = cast8_div(f, scale_div(s, true));
                 if (ok && (lane & 15) == 0) static_cast<float*>(sout)[r * ng + (c >> 7)] = s;
             } else if constexpr (GRAN == kGranMx) {
                 const uint32_t m = warp_max_u32(absmax_v4(v[j]), 4);
@@ -264,7 +265,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
                 o = cast8_mul(f, exp2_neg(e));
                 if (ok && (lane & 15) == 0) static_cast<uint8_t*>(sout)[r * ng + (c >> 7)] = (uint8_t)(e + 127);
             } else {
-                o = cast8_div(f, s_uniform);
+                o = cast8_div(f, sd_uniform);
             }
             if (ok) {
                 if constexpr (SRC == kSrcGather)
@@ -451,7 +452,7 @@ quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
         if (cok && r < rows) {
             float f[8];
             unpack8(v[i], f);
-            *reinterpret_cast<uint2*>(q + r * cols + c) = P2 ? cast8_mul(f, sc) : cast8_div(f, sc);
+            *reinterpret_cast<uint2*>(q + r * cols + c) = P2 ? cast8_mul(f, sc) : cast8_div(f, scale_div(sc, true));
         }
     }
 }
@@ -520,6 +521,8 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
     }
 
     // ---- codes of column cc + j, rows rw .. rw+7 -> shared [column][row] tile
+    // (IEEE division here: this kernel measured slower with the reciprocal
+    // and correction step of the other casts)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float f[8];
@@ -620,12 +623,13 @@ __device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, int* st
     }
 }
 
-// x / d or x * d (power-of-two grans) for two BF16 values packed in `word`.
+// x / S (FP32 grans) or x * 2^-e (power-of-two grans) for two BF16 values
+// packed in `word`; d0, d1 carry S (and its reciprocal) or 2^-e in .s.
 template <int GRAN>
-__device__ __forceinline__ float2 tile_scaled2(uint32_t word, float d0, float d1) {
+__device__ __forceinline__ float2 tile_scaled2(uint32_t word, const ScaleDiv& d0, const ScaleDiv& d1) {
     const float a = bf16_lo(word), b = bf16_hi(word);
-    if constexpr (kPow2<GRAN>) return make_float2(__fmul_rn(a, d0), __fmul_rn(b, d1));
-    return make_float2(__fdiv_rn(a, d0), __fdiv_rn(b, d1));
+    if constexpr (kPow2<GRAN>) return make_float2(__fmul_rn(a, d0.s), __fmul_rn(b, d1.s));
+    return make_float2(div_scale(a, d0), div_scale(b, d1));
 }
 
 template <int GRAN, bool DUAL>
@@ -706,13 +710,15 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
             d1 = exp2_neg(e1);
         }
         // ---------------- column pass, sweep 2: codes of X^T into registers (4 rows per word)
+        const ScaleDiv sd0 = kPow2<GRAN> ? ScaleDiv{d0, 0.0f, false} : scale_div(d0, true);
+        const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : scale_div(d1, true);
         uint32_t c0w[8], c1w[8];
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
-            const float2 a = tile_scaled2<GRAN>(colp[k * 64], d0, d1);
-            const float2 b = tile_scaled2<GRAN>(colp[(k + 1) * 64], d0, d1);
-            const float2 c = tile_scaled2<GRAN>(colp[(k + 2) * 64], d0, d1);
-            const float2 d = tile_scaled2<GRAN>(colp[(k + 3) * 64], d0, d1);
+            const float2 a = tile_scaled2<GRAN>(colp[k * 64], sd0, sd1);
+            const float2 b = tile_scaled2<GRAN>(colp[(k + 1) * 64], sd0, sd1);
+            const float2 c = tile_scaled2<GRAN>(colp[(k + 2) * 64], sd0, sd1);
+            const float2 d = tile_scaled2<GRAN>(colp[(k + 3) * 64], sd0, sd1);
             c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
             c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
         }
@@ -768,12 +774,13 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                     }
                 }
                 const int64_t c = c0 + 8 * ch;
+                const ScaleDiv sdd = kPow2<GRAN> ? ScaleDiv{dd, 0.0f, false} : scale_div(dd, true);
                 if (r < rows) {
                     if (c < cols) {
-                        const float2 x0 = tile_scaled2<GRAN>(v.x, dd, dd);
-                        const float2 x1 = tile_scaled2<GRAN>(v.y, dd, dd);
-                        const float2 x2 = tile_scaled2<GRAN>(v.z, dd, dd);
-                        const float2 x3 = tile_scaled2<GRAN>(v.w, dd, dd);
+                        const float2 x0 = tile_scaled2<GRAN>(v.x, sdd, sdd);
+                        const float2 x1 = tile_scaled2<GRAN>(v.y, sdd, sdd);
+                        const float2 x2 = tile_scaled2<GRAN>(v.z, sdd, sdd);
+                        const float2 x3 = tile_scaled2<GRAN>(v.w, sdd, sdd);
                         *reinterpret_cast<uint2*>(q + r * cols + c) =
                             make_uint2(e4m3x4(x0.x, x0.y, x1.x, x1.y), e4m3x4(x2.x, x2.y, x3.x, x3.y));
                     }
@@ -901,6 +908,34 @@ int launch_quantize(const QuantJob& j, cudaStream_t st) {
     default:
         return (int)cudaErrorInvalidValue;
     }
+    return (int)cudaGetLastError();
+}
+
+// Every (amax, x) pair of the FP32-scale casts: amax a positive finite BF16
+// value, x a finite BF16 value with |x| <= amax, S = fp32_scale_from_amax(amax).
+// Counts the pairs, the pairs whose E4M3 code through div_scale differs from
+// the code of the IEEE quotient, and the amax values that take the fast path.
+__global__ void __launch_bounds__(256) quotient_sweep_kernel(unsigned long long* __restrict__ counts) {
+    const uint32_t ai = blockIdx.x * blockDim.x + threadIdx.x;
+    if (ai == 0 || ai > 0x7F7Fu) return;
+    const float amax = __uint_as_float(ai << 16);
+    const float sc = fp32_scale_from_amax(amax);
+    const ScaleDiv d = scale_div(sc, true);
+    unsigned long long n = 0, bad = 0;
+    for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
+        if (((xb >> 7) & 0xFFu) == 0xFFu) continue;
+        const float x = __uint_as_float(xb << 16);
+        if (fabsf(x) > amax) continue;
+        ++n;
+        bad += (e4m3_byte(div_scale(x, d)) != e4m3_byte(__fdiv_rn(x, sc))) ? 1 : 0;
+    }
+    atomicAdd(&counts[0], n);
+    atomicAdd(&counts[1], bad);
+    if (d.fast) atomicAdd(&counts[2], 1ull);
+}
+
+int launch_quotient_sweep(unsigned long long* counts, cudaStream_t st) {
+    quotient_sweep_kernel<<<(0x7F80 + 255) / 256, 256, 0, st>>>(counts);
     return (int)cudaGetLastError();
 }
 

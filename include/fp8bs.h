@@ -17,7 +17,8 @@
  * Arithmetic contract (bit-exact against the CPU oracle):
  *   amax is exact; FP32 scales are IEEE float32 S = amax / 448 (S = 1 when
  *   amax = 0); codes are the saturating round-to-nearest-even E4M3 cast of
- *   the IEEE float32 quotient x / S.  MXFP8: S = 2^e with e the smallest
+ *   the IEEE float32 quotient x / S (the kernels reach the same codes by a
+ *   reciprocal and one correction step, see fp8bs_test_quotient_sweep).  MXFP8: S = 2^e with e the smallest
  *   integer such that 448 * 2^e >= amax, clamped to [-127, 127], stored as
  *   the UE8M0 byte e + 127 (amax = 0 gives byte 0).  NVFP4: S_g = amax_T /
  *   2688 (1 when amax_T = 0), block byte s_b = E4M3((amax_b / 6) / S_g),
@@ -312,6 +313,23 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
                                   const float* a_tensor_scale, const float* b_tensor_scale, int64_t m, int64_t n,
                                   int64_t k, void* d, uint64_t wait_limit_ns, void* workspace,
                                   size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8bs_test_quotient_sweep -- exhaustive check of how the FP32-scale casts
+ * divide.  The casts do not call IEEE division per element.  They take one
+ * correctly rounded reciprocal r = RN(1/S) per group, then
+ * q = RN(y + RN(x - y S) r) with y = RN(x r) (Markstein's correction step).
+ * That q can differ from RN(x / S) in its last bit, but never in its E4M3
+ * code, on the casts' whole domain.  This call enumerates that domain: every
+ * positive finite BF16 amax, S = amax / 448, every finite BF16 x with
+ * |x| <= amax.  It compares the two codes.
+ *   counts  DEVICE uint64[3], zero-filled by the caller, 8-byte aligned;
+ *           receives [0] pairs checked (about 1.03e9), [1] pairs whose codes
+ *           differ (0 is the contract), [2] amax values on the fast path
+ *           (amax >= 2^-80; smaller ones divide exactly).
+ * Runs for about a millisecond.  No counterpart on the pages.
+ */
+int fp8bs_test_quotient_sweep(unsigned long long* counts, fp8bs_stream_t stream);
 
 /*
  * fp8_quantize_per_tensor_noalloc -- fp8_quantize(gran = PER_TENSOR) for

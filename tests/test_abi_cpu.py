@@ -166,3 +166,8 @@ def test_stalled_gemm_nvfp4_rejects_bad_arguments(lib):
     assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 0, FAKE, WS, None) == -1      # no bound
     assert t(FAKE, ODD4, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 1000, FAKE, WS, None) == -2   # scales
     assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 1000, None, 0, None) == -6
+
+
+def test_quotient_sweep_rejects_bad_arguments(lib):
+    assert lib.fp8bs_test_quotient_sweep(None, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(ODD4, None) == -2

@@ -249,3 +249,14 @@ def test_nvfp4_full_size_activation_rows():
         idx = torch.from_numpy(rows).cuda()
         assert np.array_equal(np_u8(q.index_select(0, idx)), rq)
         assert np.array_equal(np_u8(s.index_select(0, idx)), rsb)
+
+
+def test_fp32_scale_division_matches_ieee_codes_exhaustively():
+    """The FP32-scale casts divide by a reciprocal plus one correction step
+    instead of an IEEE division per element.  Over the whole domain (every
+    positive BF16 amax, S = amax / 448, every BF16 x with |x| <= amax) the
+    E4M3 codes must equal those of the IEEE quotient."""
+    pairs, bad, fast = fp.test_quotient_sweep()
+    assert bad == 0
+    assert pairs > 1_000_000_000
+    assert fast > 26_000          # every amax >= 2^-80 takes the fast path
