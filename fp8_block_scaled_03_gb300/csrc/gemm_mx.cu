@@ -520,21 +520,25 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             const bool got = mbar_wait(smem_u32(&sh->tfull), tcount & 1, abort, p.status);
             if (!__all_sync(0xFFFFFFFFu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
             tc_fence_after();
-            uint32_t packed[64];
+            // All four loads in flight, one wait, then the accumulator goes back
+            // to the MMA thread before any conversion: with one accumulator
+            // buffer the next tile's MMAs start only after this drain.
+            uint32_t r[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + 128 * h + 32 * c, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * g, __uint_as_float(r[2 * j + 1]) * g);
-                    packed[16 * c + j] = *reinterpret_cast<uint32_t*>(&v);
-                }
-            }
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tmem + lane_base + 128 * h + 32 * c, r + 32 * c);
+            tmem_ld_wait(r);
+            tmem_ld_wait(r + 32);
+            tmem_ld_wait(r + 64);
+            tmem_ld_wait(r + 96);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
+            uint32_t packed[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * g, __uint_as_float(r[2 * j + 1]) * g);
+                packed[j] = *reinterpret_cast<uint32_t*>(&v);
+            }
             const int64_t col0 = ti.n0 + 128 * h;
             if (row < ti.row_end) {
                 __nv_bfloat16* drow = p.d + row * p.n + col0;
