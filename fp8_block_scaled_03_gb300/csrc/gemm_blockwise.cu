@@ -159,7 +159,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+                const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
@@ -214,7 +214,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         uint32_t gg = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const float* sb_e = p.sb;
             if (p.experts) {
                 const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
@@ -277,7 +277,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         uint32_t kbg = 0, gg = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.experts, p.m, n_tiles, t);
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
             uint64_t acc[64];   // FP32 pairs: columns (2j, 2j+1) of this thread's 128-column half

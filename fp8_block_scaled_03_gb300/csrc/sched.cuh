@@ -3,10 +3,11 @@
 // Dense: tiles of BM x BN over D[m, n], numbered with the n-tile fastest.
 // Grouped: expert e owns rows offsets[e] .. offsets[e+1]-1 of A and D; it
 // contributes ceil(rows_e / BM) * n_tiles tiles, experts in order, so an
-// expert with no rows contributes none.  Every CTA copies the offsets into
-// shared memory and builds the tile prefix sum itself (one warp scan); tile
-// t is then found by a binary search over the prefix.  The host never
-// reads the offsets.
+// expert with no rows contributes none.  Every CTA builds the tile prefix
+// sum in shared memory itself (one warp scan over the device offsets);
+// tile t is then found by a binary search over the prefix, and its
+// expert's row range read from the offsets (L1/L2).  The host never reads
+// the offsets.
 #pragma once
 
 #include <cstdint>
@@ -23,7 +24,6 @@ struct TileInfo {
 };
 
 struct SchedShared {
-    int64_t offsets[kMaxExperts + 1];
     int64_t prefix[kMaxExperts + 1];
 };
 
@@ -33,14 +33,12 @@ template <int BM>
 __device__ __forceinline__ int64_t sched_setup(SchedShared* sh, const int64_t* __restrict__ offsets, int experts,
                                                int64_t m, int64_t n_tiles) {
     if (experts == 0) return ((m + BM - 1) / BM) * n_tiles;
-    for (int i = threadIdx.x; i <= experts; i += blockDim.x) sh->offsets[i] = offsets[i];
-    __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         const int per = (experts + 31) / 32;
         const int lo = min(experts, lane * per), hi = min(experts, lo + per);
         int64_t local = 0;
-        for (int e = lo; e < hi; ++e) local += ((sh->offsets[e + 1] - sh->offsets[e] + BM - 1) / BM) * n_tiles;
+        for (int e = lo; e < hi; ++e) local += ((__ldg(offsets + e + 1) - __ldg(offsets + e) + BM - 1) / BM) * n_tiles;
         int64_t incl = local;
         for (int o = 1; o < 32; o <<= 1) {
             const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
@@ -49,7 +47,7 @@ __device__ __forceinline__ int64_t sched_setup(SchedShared* sh, const int64_t* _
         int64_t run = incl - local;
         for (int e = lo; e < hi; ++e) {
             sh->prefix[e] = run;
-            run += ((sh->offsets[e + 1] - sh->offsets[e] + BM - 1) / BM) * n_tiles;
+            run += ((__ldg(offsets + e + 1) - __ldg(offsets + e) + BM - 1) / BM) * n_tiles;
         }
         if (lane == 31) sh->prefix[experts] = incl;
     }
@@ -58,8 +56,8 @@ __device__ __forceinline__ int64_t sched_setup(SchedShared* sh, const int64_t* _
 }
 
 template <int BM, int BN>
-__device__ __forceinline__ TileInfo sched_tile(const SchedShared* sh, int experts, int64_t m, int64_t n_tiles,
-                                               int64_t t) {
+__device__ __forceinline__ TileInfo sched_tile(const SchedShared* sh, const int64_t* __restrict__ offsets,
+                                               int experts, int64_t m, int64_t n_tiles, int64_t t) {
     TileInfo ti;
     if (experts == 0) {
         const int64_t mt = t / n_tiles, nt = t - mt * n_tiles;
@@ -78,8 +76,8 @@ __device__ __forceinline__ TileInfo sched_tile(const SchedShared* sh, int expert
     while (lo + 1 < experts && sh->prefix[lo + 1] <= t) ++lo;
     const int64_t local = t - sh->prefix[lo];
     const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
-    ti.row0 = sh->offsets[lo] + mt * BM;
-    ti.row_end = sh->offsets[lo + 1];
+    ti.row0 = __ldg(offsets + lo) + mt * BM;
+    ti.row_end = __ldg(offsets + lo + 1);
     ti.n0 = nt * BN;
     ti.expert = lo;
     return ti;
