@@ -97,10 +97,17 @@ template <int KIND>
 constexpr size_t stage_bytes() {
     return ((size_t)A_BYTES + B_BYTES + 512u * (Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS) + 1023) & ~size_t(1023);
 }
+// Per epilogue warp: 32 rows x 32 BF16 columns for a TMA store (64-byte swizzle).
+constexpr int OSTAGE_BYTES = 32 * 64;
+template <int STAGES>
+constexpr size_t shared_bytes_aligned() { return (sizeof(Shared<STAGES>) + 1023) & ~size_t(1023); }
 template <int KIND>
 constexpr size_t smem_bytes() {
-    return 1024 + Cfg<KIND>::STAGES * stage_bytes<KIND>() + sizeof(Shared<Cfg<KIND>::STAGES>);
+    return 1024 + Cfg<KIND>::STAGES * stage_bytes<KIND>() + shared_bytes_aligned<Cfg<KIND>::STAGES>() +
+           8 * OSTAGE_BYTES;
 }
+static_assert(smem_bytes<kMx>() <= 232448 && smem_bytes<kP2>() <= 232448 && smem_bytes<kNv>() <= 232448,
+              "shared memory per CTA");
 
 // Scale words of one stage for one lane: A rows r0 + 32*r1 (r1 < 4) and B rows
 // r0 + 32*r1 (r1 < 8); MXFP8 one 32-bit word per row, NVFP4 four.
@@ -272,13 +279,15 @@ __device__ __forceinline__ void drain_scale_copies(uint32_t bar, int lane, uint6
 
 template <int KIND, int SA, int SB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Params p) {
+gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_d, Params p) {
     constexpr int STAGES = Cfg<KIND>::STAGES;
     constexpr size_t STAGE_B = stage_bytes<KIND>();
     constexpr uint32_t SF_COLS = 4 * (Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS);  // TMEM columns per stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared<STAGES>* sh = reinterpret_cast<Shared<STAGES>*>(stages + STAGES * STAGE_B);
+    uint8_t* ostage = stages + STAGES * STAGE_B + shared_bytes_aligned<STAGES>();   // 1024-aligned
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = p.k / Cfg<KIND>::K_PER_STAGE;
@@ -540,7 +549,30 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 packed[j] = *reinterpret_cast<uint32_t*>(&v);
             }
             const int64_t col0 = ti.n0 + 128 * h;
-            if (row < ti.row_end) {
+            if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
+                // The warp's 32 rows all belong to the tile's row group: out by
+                // TMA, 32 columns at a time through the warp's staging buffer
+                // (64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3));
+                // the TMA clips rows and columns past the matrix.
+                uint8_t* ob = ostage + (warp - 4) * OSTAGE_BYTES;
+#pragma unroll
+                for (int qb = 0; qb < 4; ++qb) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(ob + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
+                            make_uint4(packed[16 * qb + 4 * c], packed[16 * qb + 4 * c + 1],
+                                       packed[16 * qb + 4 * c + 2], packed[16 * qb + 4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 32 * qb), (int32_t)(ti.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            } else if (row < ti.row_end) {
+                // an expert's last row block ends inside this warp's rows
                 __nv_bfloat16* drow = p.d + row * p.n + col0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -550,6 +582,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 }
             }
         }
+        if (lane == 0) bulk_wait0();   // this warp's output stores are complete
     }
 
     tc_fence_before();
@@ -561,7 +594,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 }
 
 template <int KIND, int SA = 0, int SB = 0>
-int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t st) {
+int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
+                cudaStream_t st) {
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -571,7 +605,7 @@ int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, i
         if (e != cudaSuccess) return (int)e;
         attr_set[dev] = true;
     }
-    gemm_mx_kernel<KIND, SA, SB><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, p);
+    gemm_mx_kernel<KIND, SA, SB><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, td, p);
     return (int)cudaGetLastError();
 }
 
@@ -582,9 +616,10 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     const bool nv = j.a_gran == 4;
     const uint64_t kbytes = nv ? (uint64_t)j.k / 2 : (uint64_t)j.k;
     const uint64_t b_rows = (uint64_t)j.n * (uint64_t)(j.experts > 0 ? j.experts : 1);
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (!make_tmap_u8(&ta, j.a, kbytes, (uint64_t)j.m, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_u8(&tb, j.b, kbytes, b_rows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_tmap_u8(&tb, j.b, kbytes, b_rows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return (int)cudaErrorInvalidValue;
     Params p{};
     p.m = j.m; p.n = j.n; p.k = j.k;
@@ -601,14 +636,14 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);
-    if (nv) return launch_kind<kNv>(ta, tb, p, grid, st);
-    if (j.a_gran == 3) return launch_kind<kMx>(ta, tb, p, grid, st);
+    if (nv) return launch_kind<kNv>(ta, tb, td, p, grid, st);
+    if (j.a_gran == 3) return launch_kind<kMx>(ta, tb, td, p, grid, st);
     // power-of-two block-wise: 5 = one byte per row and 128 K, 6 = per 128x128 block
     const int sa = j.a_gran == 5 ? 1 : 2, sb = j.b_gran == 5 ? 1 : 2;
-    if (sa == 1 && sb == 2) return launch_kind<kP2, 1, 2>(ta, tb, p, grid, st);
-    if (sa == 1 && sb == 1) return launch_kind<kP2, 1, 1>(ta, tb, p, grid, st);
-    if (sa == 2 && sb == 2) return launch_kind<kP2, 2, 2>(ta, tb, p, grid, st);
-    return launch_kind<kP2, 2, 1>(ta, tb, p, grid, st);
+    if (sa == 1 && sb == 2) return launch_kind<kP2, 1, 2>(ta, tb, td, p, grid, st);
+    if (sa == 1 && sb == 1) return launch_kind<kP2, 1, 1>(ta, tb, td, p, grid, st);
+    if (sa == 2 && sb == 2) return launch_kind<kP2, 2, 2>(ta, tb, td, p, grid, st);
+    return launch_kind<kP2, 2, 1>(ta, tb, td, p, grid, st);
 }
 
 }  // namespace fp8bs

@@ -59,17 +59,19 @@ inline bool make_tmap_b16(CUtensorMap* map, const void* base, uint64_t cols, uin
     return r == CUDA_SUCCESS;
 }
 
-// BF16 output matrix [rows, cols] (pitch `pitch_elems`), box {64, 32} with
-// 128-byte swizzle, for TMA stores of the GEMM epilogue.
-inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems) {
+// BF16 output matrix [rows, cols] (pitch `pitch_elems`), box {box_cols, 32}
+// (64 columns with 128-byte swizzle, or 32 with 64-byte swizzle), for TMA
+// stores of the GEMM epilogues.
+inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
+                               uint32_t box_cols = 64, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {pitch_elems * 2};
-    cuuint32_t box[2] = {64, 32};
+    cuuint32_t box[2] = {box_cols, 32};
     cuuint32_t es[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
