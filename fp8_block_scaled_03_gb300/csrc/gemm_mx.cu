@@ -16,16 +16,16 @@
 //               (128 FP8 or 256 FP4 K-elements), 128-byte swizzle.
 //   warp 1      TMEM owner + MMA issuer: per stage 4 block-scaled MMAs
 //               (M128 N256; K32 for MXFP8, K64 for NVFP4), accumulating the
-//               whole K range in TMEM (MXFP8 and power-of-two: after the
+//               whole K range in TMEM (power-of-two scales: after the
 //               tcgen05.cp of the stage's scale atoms).
 //   warps 2-3   scale loaders, taking turns by stage (power-of-two scales:
 //               by group of four stages, read with one load per row): read
 //               the row-major scale bytes of the stage's rows and write them
 //               in the 32 x 16-byte atom layout that tcgen05.cp
 //               32x128b.warpx4 replicates into all TMEM lane quarters (row
-//               r0 + 32*r1 at byte r0*16 + r1*4); for NVFP4 they also issue
-//               the tcgen05.cp of those atoms to TMEM (elsewhere the MMA
-//               thread does, before its MMAs).
+//               r0 + 32*r1 at byte r0*16 + r1*4); for NVFP4 and MXFP8 they
+//               also issue the tcgen05.cp of those atoms to TMEM (for
+//               power-of-two scales the MMA thread does, before its MMAs).
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
 //               128 columns per thread) to BF16 registers, release TMEM, store.
 // TMEM: columns 0..255 accumulator, 256.. scale factors per stage.
@@ -252,13 +252,14 @@ __device__ __forceinline__ void group_stage(ScaleRegs<KIND>& r, const WideRegs& 
 
 // Copy a stage's scale atoms from shared memory into its TMEM columns
 // (tcgen05.cp 32x128b.warpx4, one per 512-byte atom: A atoms first, then B).
-// One copy takes about 60 cycles to issue.  An NVFP4 stage has 12, more
-// than its MMAs take, so there the loader that wrote the atoms issues them
-// (copies of alternate stages go out from two threads, and the loader's
-// tcgen05.commit on the stage's full barrier arrives once they have landed).
-// MXFP8 and power-of-two stages have 3, and measured faster issued by the
-// MMA thread just before its MMAs.
-template <int KIND> constexpr bool kLoaderCopies = (KIND == kNv);
+// One copy takes about 60 cycles to issue, and the MMA thread's serial work
+// per stage bounds these kernels.  For NVFP4 (12 copies a stage) and MXFP8
+// (3) the loader that wrote the atoms issues them: copies of alternate
+// stages go out from two threads, and the loader's tcgen05.commit on the
+// stage's full barrier arrives once they have landed.  The power-of-two
+// loaders split rows and are busier; there the MMA thread issues the
+// copies just before its MMAs (measured faster).
+template <int KIND> constexpr bool kLoaderCopies = (KIND == kNv || KIND == kMx);
 
 template <int KIND>
 __device__ __forceinline__ void copy_scales_to_tmem(uint32_t sf_tmem, uint32_t sf_smem) {
