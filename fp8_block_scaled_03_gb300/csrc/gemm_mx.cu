@@ -214,6 +214,23 @@ __device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, 
         const int64_t srow = (SB == 2) ? (int64_t)ti.expert * nb_e + (n >> 7) : (int64_t)ti.expert * p.n + n;
         load_row_group(w.b[r1], p.sb + srow * sf_pitch, kb0, nkb, n < p.n, vec);
     };
+    // 128x128 blocks of B: a tile (256 rows from a multiple of 256) covers two
+    // blocks, rows 0..127 and 128..255, so one load per block serves its four
+    // row slots (rows past n read 0, and a block that starts past n is not read)
+    auto bblock = [&](int c) {
+        const int64_t nb = ti.n0 + 128 * c;
+        load_row_group(w.b[4 * c], p.sb + ((int64_t)ti.expert * nb_e + (nb >> 7)) * sf_pitch, kb0, nkb, nb < p.n, vec);
+#pragma unroll
+        for (int r1 = 1; r1 < 4; ++r1) {
+            const bool in = ti.n0 + 128 * c + lane + 32 * r1 < p.n;
+#pragma unroll
+            for (int g = 0; g < kSfGroup; ++g) w.b[4 * c + r1][g] = in ? w.b[4 * c][g] : 0u;
+        }
+        if (ti.n0 + 128 * c + lane >= p.n) {
+#pragma unroll
+            for (int g = 0; g < kSfGroup; ++g) w.b[4 * c][g] = 0u;
+        }
+    };
     if (part == 0) {
 #pragma unroll
         for (int r1 = 0; r1 < 4; ++r1) {
@@ -221,11 +238,19 @@ __device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, 
             const int64_t srow = (SA == 2) ? (row >> 7) : row;
             load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
         }
+        if constexpr (SB == 2) {
+            bblock(0);
+        } else {
 #pragma unroll
-        for (int r1 = 0; r1 < 4; ++r1) brow(r1);
+            for (int r1 = 0; r1 < 4; ++r1) brow(r1);
+        }
     } else {
+        if constexpr (SB == 2) {
+            bblock(1);
+        } else {
 #pragma unroll
-        for (int r1 = 4; r1 < 8; ++r1) brow(r1);
+            for (int r1 = 4; r1 < 8; ++r1) brow(r1);
+        }
     }
 }
 
