@@ -277,20 +277,24 @@ __device__ __forceinline__ void group_stage(ScaleRegs<KIND>& r, const WideRegs& 
 
 // Copy a stage's scale atoms from shared memory into its TMEM columns
 // (tcgen05.cp 32x128b.warpx4, one per 512-byte atom: A atoms first, then B).
-// One copy takes about 60 cycles to issue, and the MMA thread's serial work
-// per stage bounds these kernels.  For NVFP4 (12 copies a stage) and MXFP8
-// (3) the loader that wrote the atoms issues them: copies of alternate
-// stages go out from two threads, and the loader's tcgen05.commit on the
-// stage's full barrier arrives once they have landed.  The power-of-two
-// loaders split rows and are busier; there the MMA thread issues the
-// copies just before its MMAs (measured faster).
-template <int KIND> constexpr bool kLoaderCopies = (KIND == kNv || KIND == kMx);
+// One copy takes about 60 cycles to issue, and the serial work of the MMA
+// thread and of the loaders per stage bounds these kernels, so the copies
+// are split where there is slack.  The loader that wrote a stage's atoms
+// issues its share and commits it to the stage's full barrier (arrives once
+// they have landed); the MMA thread issues the rest just before its MMAs.
+//   MXFP8 (3 copies a stage): all by the loaders (idle half the time);
+//   NVFP4 (12): the 8 B atoms by the loaders, the 4 A atoms by the MMA
+//   thread (both were near saturation with all 12 on one side);
+//   power of two (3): all by the MMA thread (its row-split loaders are busy).
+template <int KIND> constexpr int kLoaderCopyFirst = (KIND == kMx) ? 0 : (KIND == kNv ? Cfg<KIND>::A_ATOMS
+                                                                                      : Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS);
+template <int KIND> constexpr bool kLoaderCopies = kLoaderCopyFirst<KIND> < Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS;
 
-template <int KIND>
+// Atoms [J0, J1) of a stage.
+template <int KIND, int J0, int J1>
 __device__ __forceinline__ void copy_scales_to_tmem(uint32_t sf_tmem, uint32_t sf_smem) {
-    constexpr int NA = Cfg<KIND>::A_ATOMS, NB = Cfg<KIND>::B_ATOMS;
 #pragma unroll
-    for (int j = 0; j < NA + NB; ++j) tmem_cp_32x128b_x4(sf_tmem + 4 * j, smem_desc(sf_smem + 512 * j, 0, 128, 0));
+    for (int j = J0; j < J1; ++j) tmem_cp_32x128b_x4(sf_tmem + 4 * j, smem_desc(sf_smem + 512 * j, 0, 128, 0));
 }
 
 // Before a loader warp exits, its last scale copies must have landed (on an
@@ -322,7 +326,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&sh->full[s]), KIND == kP2 ? 3 : 2);   // TMA bytes + scale loader(s)
+            // TMA bytes + scale loader(s); NVFP4: the loader's plain arrive (it releases the
+            // atoms the MMA thread copies) and its commit of the copies it issues
+            mbar_init(smem_u32(&sh->full[s]), (KIND == kP2 || KIND == kNv) ? 3 : 2);
             mbar_init(smem_u32(&sh->empty[s]), 1);
         }
         mbar_init(smem_u32(&sh->tfull), 1);
@@ -392,8 +398,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const uint64_t bdesc = kmajor_sw128_desc(a_addr + A_BYTES);
                     const uint32_t sfa = tmem + 256 + s * SF_COLS;
                     const uint32_t sfb = sfa + 4 * Cfg<KIND>::A_ATOMS;
-                    if constexpr (!kLoaderCopies<KIND>)
-                        copy_scales_to_tmem<KIND>(sfa, a_addr + A_BYTES + B_BYTES);
+                    copy_scales_to_tmem<KIND, 0, kLoaderCopyFirst<KIND>>(sfa, a_addr + A_BYTES + B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -520,7 +525,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     __syncwarp();
                     if (lane == 0) {
                         if constexpr (kLoaderCopies<KIND>) {
-                            copy_scales_to_tmem<KIND>(tmem + 256 + s * SF_COLS, smem_u32(sf));
+                            if constexpr (kLoaderCopyFirst<KIND> > 0) mbar_arrive(smem_u32(&sh->full[s]));
+                            copy_scales_to_tmem<KIND, kLoaderCopyFirst<KIND>, Cfg<KIND>::A_ATOMS + Cfg<KIND>::B_ATOMS>(
+                                tmem + 256 + s * SF_COLS, smem_u32(sf));
                             mma_commit(smem_u32(&sh->full[s]));
                         } else {
                             mbar_arrive(smem_u32(&sh->full[s]));
