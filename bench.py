@@ -362,10 +362,11 @@ def nvfp4_bench(torch, fp, dev, pk, flush):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def cpu_oracle_sample(rows: int = 128):
+def cpu_oracle_sample(rows: int = 4096):
     """The oracle on a bounded slice of the step: quantise `rows` token rows of
     X and dY and the whole weight W, run the three GEMMs for those rows
-    (fprop: rows x I, dgrad: rows x H, wgrad: I x H over `rows` tokens)."""
+    (fprop: rows x I, dgrad: rows x H, wgrad: I x H over `rows` tokens).
+    The default (half the step's tokens) is about 10-20 s of CPU work."""
     import numpy as np
     import synth
     from oracle import formats as OF
@@ -396,7 +397,9 @@ def cpu_oracle_sample(rows: int = 128):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    res = [cpu_oracle_sample() for _ in range(max(1, args.steps))]
+    # one bounded sample per step (about 3-7 s on a 16-core host), so that
+    # --steps K ends within a few minutes
+    res = [cpu_oracle_sample(256) for _ in range(max(1, args.steps))]
     v = statistics.mean(r["value"] for r in res)
     cb = dict(res[0])
     cb["value"] = v
