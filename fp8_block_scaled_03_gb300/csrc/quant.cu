@@ -14,6 +14,7 @@
 // in registers (16 rows x 4 columns per thread), per-column partial amaxes
 // combined through shared memory.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -45,8 +46,13 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 // Eight elements x / S -> eight E4M3 bytes.
 __device__ __forceinline__ uint2 cast8_div(const float* f, const ScaleDiv& d) {
     uint2 o;
-    o.x = e4m3x4(div_scale(f[0], d), div_scale(f[1], d), div_scale(f[2], d), div_scale(f[3], d));
-    o.y = e4m3x4(div_scale(f[4], d), div_scale(f[5], d), div_scale(f[6], d), div_scale(f[7], d));
+    if (d.fast) {   // one test per group, not per element
+        o.x = e4m3x4(div_fast(f[0], d), div_fast(f[1], d), div_fast(f[2], d), div_fast(f[3], d));
+        o.y = e4m3x4(div_fast(f[4], d), div_fast(f[5], d), div_fast(f[6], d), div_fast(f[7], d));
+    } else {
+        o.x = e4m3x4(__fdiv_rn(f[0], d.s), __fdiv_rn(f[1], d.s), __fdiv_rn(f[2], d.s), __fdiv_rn(f[3], d.s));
+        o.y = e4m3x4(__fdiv_rn(f[4], d.s), __fdiv_rn(f[5], d.s), __fdiv_rn(f[6], d.s), __fdiv_rn(f[7], d.s));
+    }
     return o;
 }
 
@@ -625,10 +631,12 @@ __device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, int* st
 
 // x / S (FP32 grans) or x * 2^-e (power-of-two grans) for two BF16 values
 // packed in `word`; d0, d1 carry S (and its reciprocal) or 2^-e in .s.
-template <int GRAN>
+// FAST: both divisors take the correction step (the caller tested .fast).
+template <int GRAN, bool FAST = false>
 __device__ __forceinline__ float2 tile_scaled2(uint32_t word, const ScaleDiv& d0, const ScaleDiv& d1) {
     const float a = bf16_lo(word), b = bf16_hi(word);
     if constexpr (kPow2<GRAN>) return make_float2(__fmul_rn(a, d0.s), __fmul_rn(b, d1.s));
+    if constexpr (FAST) return make_float2(div_fast(a, d0), div_fast(b, d1));
     return make_float2(div_scale(a, d0), div_scale(b, d1));
 }
 
@@ -713,15 +721,20 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         const ScaleDiv sd0 = kPow2<GRAN> ? ScaleDiv{d0, 0.0f, false} : scale_div(d0, true);
         const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : scale_div(d1, true);
         uint32_t c0w[8], c1w[8];
+        auto col_codes = [&](auto fast) {
+            constexpr bool F = decltype(fast)::value;
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-            const float2 a = tile_scaled2<GRAN>(colp[k * 64], sd0, sd1);
-            const float2 b = tile_scaled2<GRAN>(colp[(k + 1) * 64], sd0, sd1);
-            const float2 c = tile_scaled2<GRAN>(colp[(k + 2) * 64], sd0, sd1);
-            const float2 d = tile_scaled2<GRAN>(colp[(k + 3) * 64], sd0, sd1);
-            c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
-            c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
-        }
+            for (int k = 0; k < 32; k += 4) {
+                const float2 a = tile_scaled2<GRAN, F>(colp[k * 64], sd0, sd1);
+                const float2 b = tile_scaled2<GRAN, F>(colp[(k + 1) * 64], sd0, sd1);
+                const float2 c = tile_scaled2<GRAN, F>(colp[(k + 2) * 64], sd0, sd1);
+                const float2 d = tile_scaled2<GRAN, F>(colp[(k + 3) * 64], sd0, sd1);
+                c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
+                c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
+            }
+        };
+        if (!kPow2<GRAN> && sd0.fast && sd1.fast) col_codes(std::true_type{});
+        else col_codes(std::false_type{});
         // scales of X^T ([cols, *] grid)
         {
             const int64_t rbase = r0 + 32 * rq;
@@ -777,12 +790,16 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                 const ScaleDiv sdd = kPow2<GRAN> ? ScaleDiv{dd, 0.0f, false} : scale_div(dd, true);
                 if (r < rows) {
                     if (c < cols) {
-                        const float2 x0 = tile_scaled2<GRAN>(v.x, sdd, sdd);
-                        const float2 x1 = tile_scaled2<GRAN>(v.y, sdd, sdd);
-                        const float2 x2 = tile_scaled2<GRAN>(v.z, sdd, sdd);
-                        const float2 x3 = tile_scaled2<GRAN>(v.w, sdd, sdd);
+                        auto row_codes = [&](auto fast) {
+                            constexpr bool F = decltype(fast)::value;
+                            const float2 x0 = tile_scaled2<GRAN, F>(v.x, sdd, sdd);
+                            const float2 x1 = tile_scaled2<GRAN, F>(v.y, sdd, sdd);
+                            const float2 x2 = tile_scaled2<GRAN, F>(v.z, sdd, sdd);
+                            const float2 x3 = tile_scaled2<GRAN, F>(v.w, sdd, sdd);
+                            return make_uint2(e4m3x4(x0.x, x0.y, x1.x, x1.y), e4m3x4(x2.x, x2.y, x3.x, x3.y));
+                        };
                         *reinterpret_cast<uint2*>(q + r * cols + c) =
-                            make_uint2(e4m3x4(x0.x, x0.y, x1.x, x1.y), e4m3x4(x2.x, x2.y, x3.x, x3.y));
+                            (!kPow2<GRAN> && sdd.fast) ? row_codes(std::true_type{}) : row_codes(std::false_type{});
                     }
                     if constexpr (GRAN == kGranMx) {
                         if ((ch & 3) == 0 && c < cols) static_cast<uint8_t*>(s)[r * ncb + (c >> 5)] = (uint8_t)(ee + 127);
