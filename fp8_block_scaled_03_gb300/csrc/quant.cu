@@ -528,7 +528,9 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
 
     // ---- codes of column cc + j, rows rw .. rw+7 -> shared [column][row] tile
     // (IEEE division here: this kernel measured slower with the reciprocal
-    // and correction step of the other casts)
+    // and correction step of the other casts, with the fast-path test per
+    // element and also with it hoisted out of the loops: 41.7 against 39.3 us
+    // for the dual 128x128 form of [8192, 4096])
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float f[8];
