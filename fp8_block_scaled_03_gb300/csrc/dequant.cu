@@ -23,6 +23,14 @@
 namespace fp8bs {
 namespace {
 
+// a * b rounded to odd, for |a * b| >= 2^-100 or a * b == 0 (callers check
+// the scale once per chunk: every nonzero code value is at least 2^-10).
+__device__ __forceinline__ float round_odd_mul_normal(float a, float b) {
+    const float p = __fmul_rz(a, b);
+    const float err = __fmaf_rn(a, b, -p);
+    return err != 0.0f ? __uint_as_float(__float_as_uint(p) | 1u) : p;
+}
+
 __device__ __forceinline__ float round_odd_mul(float a, float b) {
     const float p = __fmul_rz(a, b);
     if (fabsf(p) < 0x1p-100f && p != 0.0f) {
@@ -59,11 +67,21 @@ dequant_kernel(const uint8_t* __restrict__ q, const void* __restrict__ scales, c
             const uint2 w = *reinterpret_cast<const uint2*>(q + r * (cols >> 1) + (c >> 1));
             const float sb = e4m3_value(static_cast<const uint8_t*>(scales)[r * (cols >> 4) + (c >> 4)]);
             const float sg = (GRAN == 7) ? tensor_scale[r] : *tensor_scale;
+            // E2M1 x E4M3 is exact in float32 and at least 2^-10 when nonzero
+            if (fabsf(sg) >= 0x1p-90f) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 f = e2m1x2_to_float2(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu);
-                v[2 * i] = round_odd_mul(f.x * sb, sg);          // E2M1 x E4M3 is exact in float32
-                v[2 * i + 1] = round_odd_mul(f.y * sb, sg);
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = e2m1x2_to_float2(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu);
+                    v[2 * i] = round_odd_mul_normal(f.x * sb, sg);
+                    v[2 * i + 1] = round_odd_mul_normal(f.y * sb, sg);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = e2m1x2_to_float2(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu);
+                    v[2 * i] = round_odd_mul(f.x * sb, sg);
+                    v[2 * i + 1] = round_odd_mul(f.y * sb, sg);
+                }
             }
         } else {
             uint4 w;
@@ -90,11 +108,29 @@ dequant_kernel(const uint8_t* __restrict__ q, const void* __restrict__ scales, c
                 s = exp2_neg(127 - (int)static_cast<const uint8_t*>(scales)[(r >> 7) * ((cols + 127) >> 7) + (c >> 7)]);
             }
             const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+            if (GRAN == 3 || GRAN == 5 || GRAN == 6) {
+                // power-of-two scale: code * 2^-e is exact (at worst a float32
+                // subnormal with room for the code's 4 significant bits)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 f = e4m3x2_to_float2(words[i >> 1] >> (16 * (i & 1)));
-                v[2 * i] = round_odd_mul(f.x, s);
-                v[2 * i + 1] = round_odd_mul(f.y, s);
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = e4m3x2_to_float2(words[i >> 1] >> (16 * (i & 1)));
+                    v[2 * i] = __fmul_rn(f.x, s);
+                    v[2 * i + 1] = __fmul_rn(f.y, s);
+                }
+            } else if (fabsf(s) >= 0x1p-90f) {   // every nonzero E4M3 value is at least 2^-9
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = e4m3x2_to_float2(words[i >> 1] >> (16 * (i & 1)));
+                    v[2 * i] = round_odd_mul_normal(f.x, s);
+                    v[2 * i + 1] = round_odd_mul_normal(f.y, s);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = e4m3x2_to_float2(words[i >> 1] >> (16 * (i & 1)));
+                    v[2 * i] = round_odd_mul(f.x, s);
+                    v[2 * i + 1] = round_odd_mul(f.y, s);
+                }
             }
         }
         __nv_bfloat16* dst = out + r * ld_out + c;
