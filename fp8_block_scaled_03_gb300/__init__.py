@@ -74,7 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.restype = I
-    lib.fp8bs_test_quotient_sweep.argtypes = [P, P]
+    lib.fp8bs_test_quotient_sweep.argtypes = [P, I, P]
     lib.fp8bs_test_quotient_sweep.restype = I
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
@@ -344,9 +344,10 @@ def test_stalled_gemm_nvfp4(a, a_scales, b, b_scales, a_tensor_scale, b_tensor_s
                                                         _stream(stream))
 
 
-def test_quotient_sweep(stream=None):
-    """Run fp8bs_test_quotient_sweep; returns (pairs, code mismatches, fast-path amax values)."""
+def test_quotient_sweep(nvfp4: bool = False, stream=None):
+    """Run fp8bs_test_quotient_sweep; returns (pairs, code mismatches, fast-path scales)."""
     counts = torch.zeros(3, dtype=torch.int64, device="cuda")
-    _check("fp8bs_test_quotient_sweep", load_library().fp8bs_test_quotient_sweep(_ptr(counts), _stream(stream)))
+    _check("fp8bs_test_quotient_sweep",
+           load_library().fp8bs_test_quotient_sweep(_ptr(counts), int(bool(nvfp4)), _stream(stream)))
     c = counts.cpu().tolist()
     return c[0], c[1], c[2]

@@ -321,10 +321,10 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
     return cuda_status(launch_gemm_mx(j, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int fp8bs_test_quotient_sweep(unsigned long long* counts, fp8bs_stream_t stream) {
-    if (counts == nullptr) return FP8BS_EINVAL;
+int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream) {
+    if (counts == nullptr || (nvfp4 != 0 && nvfp4 != 1)) return FP8BS_EINVAL;
     if (reinterpret_cast<uintptr_t>(counts) & 7u) return FP8BS_EALIGN;
-    return cuda_status(launch_quotient_sweep(counts, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_quotient_sweep(counts, nvfp4, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t fp8bs_workspace_size(void) { return kWorkspaceBytes; }

@@ -38,7 +38,7 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
 int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int64_t tokens, int64_t up,
                              cudaStream_t s);
 // Exhaustive check of the FP32-scale division used by the casts (test hook).
-int launch_quotient_sweep(unsigned long long* counts, cudaStream_t s);
+int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t s);
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                        float* scale, uint32_t* partials, int nparts, cudaStream_t s);
 

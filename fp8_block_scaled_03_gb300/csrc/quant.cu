@@ -296,11 +296,22 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
 // sums are then added, which is the same sum on both lanes (IEEE addition
 // commutes).  S_g is amax / (256 * 6) in that mode.
 
-__device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s) {
+// E2M1(x / S_b) for 8 elements.  S_b = E4M3value(s_b) * S_g: with S_g from
+// the tensor (or row) amax the quotient is the reciprocal-and-correction one
+// (div_fast, the test hoisted out of the loop); every E2M1 code on that
+// domain matches the IEEE quotient's, checked by enumeration
+// (fp8bs_test_quotient_sweep with nvfp4 = 1).  A supplied S_g divides exactly.
+__device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s, bool from_amax) {
     if (big_s == 0.0f) return 0u;
+    const ScaleDiv d = scale_div(big_s, from_amax);
     float t[8];
+    if (d.fast) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(f[i], big_s);
+        for (int i = 0; i < 8; ++i) t[i] = div_fast(f[i], d);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(f[i], big_s);
+    }
     return e2m1x8(t);
 }
 
@@ -321,18 +332,19 @@ __device__ __forceinline__ float half_sq_err(const float* f, uint32_t packed, fl
 // One lane's half block: packed E2M1 codes and the block's scale byte.  Every
 // lane of the warp must call this (shuffles).
 template <bool FOS>
-__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, uint32_t& packed, uint32_t& code) {
+__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, bool from_amax, uint32_t& packed,
+                                                 uint32_t& code) {
     const uint32_t m = warp_max_u32(absmax_v4(v), 2);
     const float amax_b = amax_bits_to_f32(m);
     float f[8];
     unpack8(v, f);
     code = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, kE2M1Max), s_g));
     const float s6 = __fmul_rn(e4m3_value(code), s_g);
-    packed = e2m1_quant8(f, s6);
+    packed = e2m1_quant8(f, s6, from_amax);
     if constexpr (FOS) {
         const uint32_t code4 = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, 4.0f), s_g));
         const float s4 = __fmul_rn(e4m3_value(code4), s_g);
-        const uint32_t p4 = e2m1_quant8(f, s4);
+        const uint32_t p4 = e2m1_quant8(f, s4, from_amax);
         float e6 = half_sq_err(f, packed, s6);
         float e4 = half_sq_err(f, p4, s4);
         e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, 1));
@@ -348,7 +360,7 @@ __device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, uint
 template <bool FOS>
 __device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, int64_t r, int64_t cb, int64_t cols,
                                               int64_t ldx, uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
-                                              float s_g, int lane) {
+                                              float s_g, bool from_amax, int lane) {
     const int64_t nb = cols >> 4;
     uint4 v[4];
 #pragma unroll
@@ -360,7 +372,7 @@ __device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, in
     for (int j = 0; j < 4; ++j) {
         const int64_t c = cb + j * 256 + lane * 8;
         uint32_t packed, code;
-        nvfp4_half_block<FOS>(v[j], s_g, packed, code);
+        nvfp4_half_block<FOS>(v[j], s_g, from_amax, packed, code);
         if (c < cols) {
             *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
             if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
@@ -388,7 +400,8 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     const int64_t segs = ceil_div(cols, kSeg);
     const int64_t total = rows * segs;
     TaskCursor tc(gw, nw, segs);
-    for (int64_t t = gw; t < total; t += nw, tc.advance()) nvfp4_segment<FOS>(x, tc.r, tc.si * kSeg, cols, ldx, q, sb, s_g, lane);
+    for (int64_t t = gw; t < total; t += nw, tc.advance())
+        nvfp4_segment<FOS>(x, tc.r, tc.si * kSeg, cols, ldx, q, sb, s_g, !given, lane);
 }
 
 // One outer scale per row (per token): a warp owns a row, reads it once for
@@ -420,7 +433,7 @@ quant_nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t col
             s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, FOS ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
             if (lane == 0) row_scale[r] = s_g;
         }
-        for (int64_t cb = 0; cb < cols; cb += kSeg) nvfp4_segment<FOS>(x, r, cb, cols, ldx, q, sb, s_g, lane);
+        for (int64_t cb = 0; cb < cols; cb += kSeg) nvfp4_segment<FOS>(x, r, cb, cols, ldx, q, sb, s_g, !given, lane);
     }
 }
 
@@ -953,8 +966,41 @@ __global__ void __launch_bounds__(256) quotient_sweep_kernel(unsigned long long*
     if (d.fast) atomicAdd(&counts[2], 1ull);
 }
 
-int launch_quotient_sweep(unsigned long long* counts, cudaStream_t st) {
-    quotient_sweep_kernel<<<(0x7F80 + 255) / 256, 256, 0, st>>>(counts);
+// NVFP4: every positive BF16 amax_T, S_g = amax_T / D (D = 2688, or 1536
+// for four-over-six), every nonzero block scale code s_b (1..126),
+// S_b = E4M3value(s_b) * S_g, every finite BF16 x with |x| <= amax_T; E2M1
+// code through div_scale against the IEEE quotient's.  One thread per
+// (amax_T, s_b, D).
+__global__ void __launch_bounds__(256) quotient_sweep_nvfp4_kernel(unsigned long long* __restrict__ counts) {
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t ai = t / 252u, rest = t - ai * 252u;      // 126 codes x 2 divisors
+    const uint32_t code = 1u + (rest >> 1);
+    if (ai == 0 || ai > 0x7F7Fu) return;
+    const float amax = __uint_as_float(ai << 16);
+    const float s_g = __fdiv_rn(amax, (rest & 1u) ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
+    const float big_s = __fmul_rn(e4m3_value(code), s_g);
+    if (big_s == 0.0f) return;                                // both paths give code 0
+    const ScaleDiv d = scale_div(big_s, true);
+    unsigned long long n = 0, bad = 0;
+    for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
+        if (((xb >> 7) & 0xFFu) == 0xFFu) continue;
+        const float x = __uint_as_float(xb << 16);
+        if (fabsf(x) > amax) continue;
+        ++n;
+        float a[8] = {div_scale(x, d), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float b[8] = {__fdiv_rn(x, big_s), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        bad += ((e2m1x8(a) ^ e2m1x8(b)) & 0xFu) ? 1 : 0;
+    }
+    atomicAdd(&counts[0], n);
+    atomicAdd(&counts[1], bad);
+    if (d.fast) atomicAdd(&counts[2], 1ull);
+}
+
+int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t st) {
+    if (nvfp4)
+        quotient_sweep_nvfp4_kernel<<<(0x7F80u * 252u + 255u) / 256u, 256, 0, st>>>(counts);
+    else
+        quotient_sweep_kernel<<<(0x7F80 + 255) / 256, 256, 0, st>>>(counts);
     return (int)cudaGetLastError();
 }
 

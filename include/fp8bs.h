@@ -315,21 +315,28 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
                                   size_t workspace_bytes, fp8bs_stream_t stream);
 
 /*
- * fp8bs_test_quotient_sweep -- exhaustive check of how the FP32-scale casts
- * divide.  The casts do not call IEEE division per element.  They take one
- * correctly rounded reciprocal r = RN(1/S) per group, then
- * q = RN(y + RN(x - y S) r) with y = RN(x r) (Markstein's correction step).
- * That q can differ from RN(x / S) in its last bit, but never in its E4M3
- * code, on the casts' whole domain.  This call enumerates that domain: every
- * positive finite BF16 amax, S = amax / 448, every finite BF16 x with
- * |x| <= amax.  It compares the two codes.
+ * fp8bs_test_quotient_sweep -- exhaustive check of how the casts divide by
+ * a scale derived from an amax.  They do not call IEEE division per
+ * element: they take one correctly rounded reciprocal r = RN(1/S) per
+ * group, then q = RN(y + RN(x - y S) r) with y = RN(x r) (Markstein's
+ * correction step).  q can differ from RN(x / S) in its last bit but, on
+ * the whole domain of the casts, never in its code; this call enumerates
+ * that domain and compares the codes:
+ *   nvfp4 = 0  E4M3 casts with FP32 scales: every positive finite BF16
+ *              amax, S = amax / 448, every finite BF16 x with |x| <= amax
+ *              (about 1.03e9 pairs);
+ *   nvfp4 = 1  E2M1 casts of NVFP4: every positive finite BF16 amax_T,
+ *              S_g = amax_T / 2688 and amax_T / 1536 (four-over-six), every
+ *              block scale code 1..126, S = E4M3value * S_g, every finite
+ *              BF16 x with |x| <= amax_T (about 1.3e11 pairs).
  *   counts  DEVICE uint64[3], zero-filled by the caller, 8-byte aligned;
- *           receives [0] pairs checked (about 1.03e9), [1] pairs whose codes
- *           differ (0 is the contract), [2] amax values on the fast path
- *           (amax >= 2^-80; smaller ones divide exactly).
- * Runs for about a millisecond.  No counterpart on the pages.
+ *           receives [0] pairs checked, [1] pairs whose codes differ (0 is
+ *           the contract), [2] scales on the fast path (S >= 2^-88;
+ *           smaller ones divide exactly).
+ * Runs for about a millisecond (nvfp4 = 0) or a second (nvfp4 = 1).  No
+ * counterpart on the pages.
  */
-int fp8bs_test_quotient_sweep(unsigned long long* counts, fp8bs_stream_t stream);
+int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream);
 
 /*
  * fp8_quantize_per_tensor_noalloc -- fp8_quantize(gran = PER_TENSOR) for

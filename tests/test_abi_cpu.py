@@ -169,5 +169,6 @@ def test_stalled_gemm_nvfp4_rejects_bad_arguments(lib):
 
 
 def test_quotient_sweep_rejects_bad_arguments(lib):
-    assert lib.fp8bs_test_quotient_sweep(None, None) == -1
-    assert lib.fp8bs_test_quotient_sweep(ODD4, None) == -2
+    assert lib.fp8bs_test_quotient_sweep(None, 0, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(FAKE, 2, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(ODD4, 1, None) == -2

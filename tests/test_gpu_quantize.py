@@ -260,3 +260,14 @@ def test_fp32_scale_division_matches_ieee_codes_exhaustively():
     assert bad == 0
     assert pairs > 1_000_000_000
     assert fast > 26_000          # every amax >= 2^-80 takes the fast path
+
+
+
+def test_nvfp4_block_division_matches_ieee_codes_exhaustively():
+    """NVFP4 divides each block by S_b = E4M3value * S_g the same way; over
+    every amax_T, both outer divisors, every block scale code and every BF16
+    x with |x| <= amax_T the E2M1 codes must equal the IEEE quotient's."""
+    pairs, bad, fast = fp.test_quotient_sweep(nvfp4=True)
+    assert bad == 0
+    assert pairs > 100_000_000_000
+    assert fast > 1_000_000
