@@ -33,7 +33,19 @@ template <int G> constexpr bool kPow2 = (G == kGranMx || G == kGranTokP2 || G ==
 constexpr int kSeg = 1024;       // columns per row-wise warp task
 constexpr int kThreads = 256;
 
+// max |x| of eight BF16 values as BF16 bits: packed 16-bit maxima of the
+// magnitude bits first (non-negative BF16 patterns order like their values),
+// then the larger half.
 __device__ __forceinline__ uint32_t absmax_v4(const uint4& v) {
+    const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+// The same maximum pair by pair (the plain MXFP8 row kernel measured faster
+// with it: 23.3 against 25.3 us for [8192, 4096]; its MoE gather and SwiGLU
+// forms were faster with the packed one).
+__device__ __forceinline__ uint32_t absmax_v4_pairs(const uint4& v) {
     return max(max(bf16x2_absmax_bits(v.x), bf16x2_absmax_bits(v.y)),
                max(bf16x2_absmax_bits(v.z), bf16x2_absmax_bits(v.w)));
 }
@@ -261,7 +273,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
                 o = cast8_div(f, scale_div(s, true));
                 if (ok && (lane & 15) == 0) static_cast<float*>(sout)[r * ng + (c >> 7)] = s;
             } else if constexpr (GRAN == kGranMx) {
-                const uint32_t m = warp_max_u32(absmax_v4(v[j]), 4);
+                const uint32_t m = warp_max_u32(SRC == kSrcPlain ? absmax_v4_pairs(v[j]) : absmax_v4(v[j]), 4);
                 const int e = mx_exponent_from_amax_bits(m << 16);
                 o = cast8_mul(f, exp2_neg(e));
                 if (ok && (lane & 3) == 0) static_cast<uint8_t*>(sout)[r * ng + (c >> 5)] = (uint8_t)(e + 127);
