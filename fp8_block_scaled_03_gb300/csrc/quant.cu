@@ -167,10 +167,11 @@ struct RowSrc {
 // scaling by 2^(n-1) * 2.  +inf above 89, 0 below -87 (where 1 + e^x is 1 in
 // float32 already).  Within 2 float32 ulps of e^x.
 __device__ __forceinline__ float exp_seq(float x) {
-    if (x > 0x1.64p+6f) return __int_as_float(0x7F800000);    // 89
-    if (x < -0x1.5cp+6f) return 0.0f;                           // -87
-    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));        // x / ln 2
-    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0x1.62e4p-1f)), __fmul_rn(n, 0x1.7f7d1cp-20f));
+    // computed on x clamped to [-87, 89] (which keeps n in [-126, 128]), the
+    // out-of-range results selected at the end: no branch per element
+    const float xc = fminf(fmaxf(x, -0x1.5cp+6f), 0x1.64p+6f);
+    const float n = rintf(__fmul_rn(xc, 0x1.715476p+0f));       // x / ln 2
+    const float r = __fsub_rn(__fsub_rn(xc, __fmul_rn(n, 0x1.62e4p-1f)), __fmul_rn(n, 0x1.7f7d1cp-20f));
     float p = 0x1.a01a02p-13f;                                  // 1/7!
     p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);            // 1/6!
     p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);             // 1/5!
@@ -179,9 +180,12 @@ __device__ __forceinline__ float exp_seq(float x) {
     p = __fadd_rn(__fmul_rn(p, r), 0.5f);
     p = __fadd_rn(__fmul_rn(p, r), 1.0f);
     p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    const int ni = max(min((int)n, 128), -126) - 1;             // 2^(n-1) is a float32 (>= 2^-127)
+    const int ni = (int)n - 1;                                  // 2^(n-1) is a float32 (>= 2^-127)
     const float half = ni >= -126 ? __int_as_float((ni + 127) << 23) : __int_as_float(0x00400000);
-    return __fmul_rn(__fmul_rn(p, half), 2.0f);
+    float e = __fmul_rn(__fmul_rn(p, half), 2.0f);
+    e = x > 0x1.64p+6f ? __int_as_float(0x7F800000) : e;         // 89: +inf
+    e = x < -0x1.5cp+6f ? 0.0f : e;                              // -87: 0
+    return e;
 }
 
 // Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up.
