@@ -82,6 +82,11 @@ struct Params {
     int stall_stage0;     // test hook: the producer withholds stage 0
 };
 
+// Dense tile order: NVFP4 walks groups of 16 row tiles (its 906 MB of D
+// otherwise pushes W out of L2 between waves); the FP8 kinds keep the
+// column tile fastest, which measured faster for them.
+template <int KIND> constexpr int kTileGroupM = (KIND == kNv) ? 16 : 0;
+
 template <int STAGES>
 struct alignas(16) Shared {
     uint64_t full[STAGES], empty[STAGES], tfull, tempty, drain;
@@ -360,7 +365,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
+                const TileInfo ti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
@@ -430,7 +435,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const bool vec = (sf_pitch & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.sa) | reinterpret_cast<uintptr_t>(p.sb)) & 3u) == 0;
         int64_t lt = blockIdx.x, lkb0 = 0;                // load cursor (tile, first stage of the group)
         TileInfo lti{};
-        if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+        if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
         auto load_next = [&](WideRegs& w, int64_t& kb0_out) -> bool {
             if (lt >= total) return false;
             load_scales_group<SA, SB>(w, p, lti, lkb0, nkb, lane, sf_pitch, vec, part);
@@ -439,7 +444,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             if (lkb0 >= nkb) {
                 lkb0 = 0;
                 lt += gridDim.x;
-                if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+                if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
             }
             return true;
         };
@@ -484,12 +489,12 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             ScaleRegs<KIND> ring[SF_PD];
             int64_t lt = blockIdx.x, lkb = 0;                 // load cursor
             TileInfo lti{};
-            if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+            if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
             auto step_load = [&]() {
                 if (++lkb == nkb) {
                     lkb = 0;
                     lt += gridDim.x;
-                    if (lt < total) lti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+                    if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
                 }
             };
             int64_t st_t = blockIdx.x, st_kb = 0;           // store cursor
@@ -556,7 +561,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         uint32_t tcount = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
+            const TileInfo ti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             if (KIND == kNv && p.a_ts_rows) g = (row < ti.row_end) ? __ldg(p.a_ts + row) * gb : 0.0f;
             const bool got = mbar_wait(smem_u32(&sh->tfull), tcount & 1, abort, p.status);

@@ -55,12 +55,27 @@ __device__ __forceinline__ int64_t sched_setup(SchedShared* sh, const int64_t* _
     return sh->prefix[experts];
 }
 
-template <int BM, int BN>
+// GM (dense only): 0 numbers the tiles with the column tile fastest; GM > 0
+// walks groups of GM row tiles with the row tile fastest inside a group, so
+// the tiles in flight together share a few row blocks of A and column
+// blocks of B.
+template <int BM, int BN, int GM = 0>
 __device__ __forceinline__ TileInfo sched_tile(const SchedShared* sh, const int64_t* __restrict__ offsets,
                                                int experts, int64_t m, int64_t n_tiles, int64_t t) {
     TileInfo ti;
     if (experts == 0) {
-        const int64_t mt = t / n_tiles, nt = t - mt * n_tiles;
+        int64_t mt, nt;
+        if constexpr (GM > 0) {
+            const int64_t m_tiles = (m + BM - 1) / BM;
+            const int64_t per_group = (int64_t)GM * n_tiles;
+            const int64_t g = t / per_group, r = t - g * per_group;
+            const int64_t gm = min((int64_t)GM, m_tiles - g * GM);
+            nt = r / gm;
+            mt = g * GM + (r - nt * gm);
+        } else {
+            mt = t / n_tiles;
+            nt = t - mt * n_tiles;
+        }
         ti.row0 = mt * BM;
         ti.row_end = m;
         ti.n0 = nt * BN;
