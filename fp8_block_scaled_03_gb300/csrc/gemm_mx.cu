@@ -7,8 +7,9 @@
 // scales and NVFP4 1x16 with two-level (E4M3 + FP32) scales, both Blackwell
 // formats; section "2. Unified block-wise FP8": on Blackwell the block-wise
 // recipe runs on this path with power-of-two scales (one UE8M0 byte per
-// 128-wide K block, replicated over its four 32-wide sub-blocks); section "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend is
-// chosen separately from the dense one.  Here both are one kernel: a dense
+// 128-wide K block, replicated over its four 32-wide sub-blocks); section
+// "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend is chosen separately
+// from the dense one.  Here both are one kernel: a dense
 // GEMM is the grouped GEMM with one group.
 //
 // CTA: 384 threads, one CTA per SM (persistent), tile 128 x 256.
@@ -16,19 +17,24 @@
 //               (128 FP8 or 256 FP4 K-elements), 128-byte swizzle.
 //   warp 1      TMEM owner + MMA issuer: per stage 4 block-scaled MMAs
 //               (M128 N256; K32 for MXFP8, K64 for NVFP4), accumulating the
-//               whole K range in TMEM (power-of-two scales: after the
-//               tcgen05.cp of the stage's scale atoms).
-//   warps 2-3   scale loaders, taking turns by stage (power-of-two scales:
-//               by group of four stages, read with one load per row): read
-//               the row-major scale bytes of the stage's rows and write them
-//               in the 32 x 16-byte atom layout that tcgen05.cp
-//               32x128b.warpx4 replicates into all TMEM lane quarters (row
-//               r0 + 32*r1 at byte r0*16 + r1*4); for NVFP4 and MXFP8 they
-//               also issue the tcgen05.cp of those atoms to TMEM (for
-//               power-of-two scales the MMA thread does, before its MMAs).
+//               whole K range in TMEM; before them the tcgen05.cp of the
+//               stage's A scale atoms (NVFP4) or of all its atoms (power of
+//               two).
+//   warps 2-3   scale loaders: read the row-major scale bytes of a stage's
+//               rows and write them in the 32 x 16-byte atom layout that
+//               tcgen05.cp 32x128b.warpx4 replicates into all TMEM lane
+//               quarters (row r0 + 32*r1 at byte r0*16 + r1*4).  MXFP8 and
+//               NVFP4: the two warps take turns by stage and issue the
+//               stage's copies themselves (all of them for MXFP8, the B
+//               atoms for NVFP4).  Power of two: both warps serve every
+//               stage, split by rows, four stages per load.
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
-//               128 columns per thread) to BF16 registers, release TMEM, store.
-// TMEM: columns 0..255 accumulator, 256.. scale factors per stage.
+//               128 columns per thread) with one TMEM wait, release it,
+//               convert to BF16 and store 32 x 32 boxes by TMA through a
+//               2 KB staging buffer per warp.
+// TMEM: columns 0..255 accumulator, 256.. scale factors per stage.  Dense
+// tiles are walked in groups of row tiles (sched_tile's GM).  One pass per
+// tile order and stage ring is shared by the dense and grouped forms.
 #include <algorithm>
 
 #include "common.cuh"
