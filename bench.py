@@ -203,7 +203,13 @@ def max_over_ranks(torch, dist, value: float, device) -> float:
 
 
 def flush_l2(torch, buf):
+    """Leave L2 cold and clean: write all of buf (512 MB, larger than the
+    129 MB L2), then read its first half back.  The write alone leaves L2
+    full of dirty lines, and the timed kernel would pay for writing them back
+    to HBM: a plain copy of 134 MB then reached about 0.75 of the measured
+    copy bandwidth instead of about 1.0."""
     buf.zero_()
+    buf[: buf.numel() // 2].max()
 
 
 def time_fn(torch, fn, reps, flush=None, warm=3):
@@ -246,6 +252,13 @@ def quantize_sweep(torch, fp, dev, pk, flush):
         ms, _ = time_fn(torch, lambda: fp.fp8_quantize(x, g, q=q, scales=s, tensor_scale=ts, ws=ws), 20, flush)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[g] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3)}
+    # calibration: a plain device copy of X (the same read bytes, twice the written ones) under the same flush
+    xc = torch.empty_like(x)
+    ms, _ = time_fn(torch, lambda: xc.copy_(x), 20, flush)
+    gbs = 4 * e / (ms * 1e-3) / 1e9
+    out["copy_calibration"] = {"gbs": round(gbs, 1), "us": round(ms * 1e3, 2), "frac": round(gbs / pk["hbm_gbs"], 3),
+                               "what": "torch copy of the same [8192,4096] BF16 input, read + write bytes"}
+    del xc
     xd = torch.empty((r, c), dtype=torch.bfloat16, device=dev)
     for g in ("1x128", "mxfp8"):
         q, s, _ = bufs[g]
@@ -417,7 +430,7 @@ def workload_config(args):
                         "intermediate 9728); X,dY 1x128 FP32 scales (dual row+transposed), W 128x128 FP32 scales",
             "tokens": M3, "hidden": H3, "intermediate": I3, "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs 250 MB and step working set ~630 MB, both > 129 MB L2; sub-benchmarks flush L2 "
-                  "(512 MB write) before each timed call"}
+                  "before each timed call (512 MB written, then 256 MB of it read back, so L2 starts cold and clean)"}
 
 
 # ---------------------------------------------------------------- main

@@ -59,8 +59,9 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 __device__ __forceinline__ uint2 cast8_div(const float* f, const ScaleDiv& d) {
     uint2 o;
     if (d.fast) {   // one test per group, not per element
-        o.x = e4m3x4(div_fast(f[0], d), div_fast(f[1], d), div_fast(f[2], d), div_fast(f[3], d));
-        o.y = e4m3x4(div_fast(f[4], d), div_fast(f[5], d), div_fast(f[6], d), div_fast(f[7], d));
+        const ScaleDiv2 d2 = scale_div2(d);
+        o.x = e4m3x4_div_fast2(pair_f32(f[0], f[1]), pair_f32(f[2], f[3]), d2);
+        o.y = e4m3x4_div_fast2(pair_f32(f[4], f[5]), pair_f32(f[6], f[7]), d2);
     } else {
         o.x = e4m3x4(__fdiv_rn(f[0], d.s), __fdiv_rn(f[1], d.s), __fdiv_rn(f[2], d.s), __fdiv_rn(f[3], d.s));
         o.y = e4m3x4(__fdiv_rn(f[4], d.s), __fdiv_rn(f[5], d.s), __fdiv_rn(f[6], d.s), __fdiv_rn(f[7], d.s));
@@ -754,6 +755,17 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         uint32_t c0w[8], c1w[8];
         auto col_codes = [&](auto fast) {
             constexpr bool F = decltype(fast)::value;
+            if constexpr (F) {   // four rows of each of the two columns as two pairs each
+                const ScaleDiv2 e0 = scale_div2(sd0), e1 = scale_div2(sd1);
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    const uint32_t wa = colp[k * 64], wb = colp[(k + 1) * 64];
+                    const uint32_t wc = colp[(k + 2) * 64], wd = colp[(k + 3) * 64];
+                    c0w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), e0);
+                    c1w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), e1);
+                }
+                return;
+            }
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
                 const float2 a = tile_scaled2<GRAN, F>(colp[k * 64], sd0, sd1);
@@ -823,6 +835,11 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                     if (c < cols) {
                         auto row_codes = [&](auto fast) {
                             constexpr bool F = decltype(fast)::value;
+                            if constexpr (F) {
+                                const ScaleDiv2 e2 = scale_div2(sdd);
+                                return make_uint2(e4m3x4_div_fast2(pair_bf16(v.x), pair_bf16(v.y), e2),
+                                                  e4m3x4_div_fast2(pair_bf16(v.z), pair_bf16(v.w), e2));
+                            }
                             const float2 x0 = tile_scaled2<GRAN, F>(v.x, sdd, sdd);
                             const float2 x1 = tile_scaled2<GRAN, F>(v.y, sdd, sdd);
                             const float2 x2 = tile_scaled2<GRAN, F>(v.z, sdd, sdd);
@@ -969,13 +986,22 @@ __global__ void __launch_bounds__(256) quotient_sweep_kernel(unsigned long long*
     const float amax = __uint_as_float(ai << 16);
     const float sc = fp32_scale_from_amax(amax);
     const ScaleDiv d = scale_div(sc, true);
+    const ScaleDiv2 d2 = scale_div2(d);
     unsigned long long n = 0, bad = 0;
     for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
         if (((xb >> 7) & 0xFFu) == 0xFFu) continue;
         const float x = __uint_as_float(xb << 16);
         if (fabsf(x) > amax) continue;
         ++n;
-        bad += (e4m3_byte(div_scale(x, d)) != e4m3_byte(__fdiv_rn(x, sc))) ? 1 : 0;
+        // the code as the quantisers take it: packed pairs on the fast path
+        // (both byte positions of a pair checked), IEEE division otherwise
+        const uint32_t want = e4m3_byte(__fdiv_rn(x, sc));
+        if (d.fast) {
+            const uint32_t c4 = e4m3x4_div_fast2(pair_f32(x, x), pair_f32(x, x), d2);
+            bad += ((c4 & 0xFFu) != want || (c4 >> 24) != want) ? 1 : 0;
+        } else {
+            bad += (e4m3_byte(__fdiv_rn(x, d.s)) != want) ? 1 : 0;
+        }
     }
     atomicAdd(&counts[0], n);
     atomicAdd(&counts[1], bad);
