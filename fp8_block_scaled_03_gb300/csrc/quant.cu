@@ -321,14 +321,10 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
 __device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s, bool from_amax) {
     if (big_s == 0.0f) return 0u;
     const ScaleDiv d = scale_div(big_s, from_amax);
+    if (d.fast) return e2m1x8_div_fast2(f, scale_div2(d));
     float t[8];
-    if (d.fast) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = div_fast(f[i], d);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(f[i], big_s);
-    }
+    for (int i = 0; i < 8; ++i) t[i] = __fdiv_rn(f[i], big_s);
     return e2m1x8(t);
 }
 
@@ -556,29 +552,33 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
         }
     }
 
+    // Four codes of x / S (FP32 scales: the packed correction-step quotient
+    // when S came from an amax, the test taken once per thread; IEEE division
+    // for a supplied per-tensor S) or of x * 2^-e.
+    const ScaleDiv sd = kPow2<GRAN> ? ScaleDiv{sc, 0.0f, false} : scale_div(sc, given == nullptr);
+    const ScaleDiv2 sd2 = scale_div2(sd);
+    auto codes4 = [&](float a0, float a1, float a2, float a3, auto fast) -> uint32_t {
+        if constexpr (kPow2<GRAN>) return e4m3x4(__fmul_rn(a0, sc), __fmul_rn(a1, sc), __fmul_rn(a2, sc), __fmul_rn(a3, sc));
+        else if constexpr (decltype(fast)::value) return e4m3x4_div_fast2(pair_f32(a0, a1), pair_f32(a2, a3), sd2);
+        else return e4m3x4(__fdiv_rn(a0, sc), __fdiv_rn(a1, sc), __fdiv_rn(a2, sc), __fdiv_rn(a3, sc));
+    };
+
     // ---- codes of column cc + j, rows rw .. rw+7 -> shared [column][row] tile
-    // (IEEE division here: this kernel measured slower with the reciprocal
-    // and correction step of the other casts, with the fast-path test per
-    // element and also with it hoisted out of the loops: 41.7 against 39.3 us
-    // for the dual 128x128 form of [8192, 4096])
+    auto col_pass = [&](auto fast) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float f[8];
+        for (int j = 0; j < 4; ++j) {
+            float f[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t word = (j < 2) ? v[i].x : v[i].y;
-            f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t word = (j < 2) ? v[i].x : v[i].y;
+                f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+            }
+            const uint2 o = make_uint2(codes4(f[0], f[1], f[2], f[3], fast), codes4(f[4], f[5], f[6], f[7], fast));
+            *reinterpret_cast<uint2*>(tq + (lane * 4 + j) * kTPitch + 8 * w) = o;
         }
-        uint2 o;
-        if constexpr (kPow2<GRAN>) {
-            o.x = e4m3x4(__fmul_rn(f[0], sc), __fmul_rn(f[1], sc), __fmul_rn(f[2], sc), __fmul_rn(f[3], sc));
-            o.y = e4m3x4(__fmul_rn(f[4], sc), __fmul_rn(f[5], sc), __fmul_rn(f[6], sc), __fmul_rn(f[7], sc));
-        } else {
-            o.x = e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc));
-            o.y = e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc));
-        }
-        *reinterpret_cast<uint2*>(tq + (lane * 4 + j) * kTPitch + 8 * w) = o;
-    }
+    };
+    if (sd.fast) col_pass(std::true_type{});
+    else col_pass(std::false_type{});
     __syncthreads();
     // ---- whole rows of X^T: 128 columns x 128 bytes, 16 bytes per thread and pass
 #pragma unroll
@@ -601,13 +601,15 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
 
     // ---- row-wise codes of X from the same registers
     if constexpr (DUAL) {
+        auto row_pass = [&](auto fast) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float f0 = bf16_lo(v[i].x), f1 = bf16_hi(v[i].x), f2 = bf16_lo(v[i].y), f3 = bf16_hi(v[i].y);
-            const uint32_t o = kPow2<GRAN> ? e4m3x4(__fmul_rn(f0, sc), __fmul_rn(f1, sc), __fmul_rn(f2, sc), __fmul_rn(f3, sc))
-                                           : e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc), __fdiv_rn(f3, sc));
-            if (cok && wok) *reinterpret_cast<uint32_t*>(q + (rw + i) * cols + cc) = o;
-        }
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t o = codes4(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y), fast);
+                if (cok && wok) *reinterpret_cast<uint32_t*>(q + (rw + i) * cols + cc) = o;
+            }
+        };
+        if (sd.fast) row_pass(std::true_type{});
+        else row_pass(std::false_type{});
         if constexpr (GRAN == kGranBlk) {
             if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = sc;
         } else if constexpr (GRAN == kGranBlkP2) {
@@ -1023,15 +1025,25 @@ __global__ void __launch_bounds__(256) quotient_sweep_nvfp4_kernel(unsigned long
     const float big_s = __fmul_rn(e4m3_value(code), s_g);
     if (big_s == 0.0f) return;                                // both paths give code 0
     const ScaleDiv d = scale_div(big_s, true);
+    const ScaleDiv2 d2 = scale_div2(d);
     unsigned long long n = 0, bad = 0;
     for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
         if (((xb >> 7) & 0xFFu) == 0xFFu) continue;
         const float x = __uint_as_float(xb << 16);
         if (fabsf(x) > amax) continue;
         ++n;
-        float a[8] = {div_scale(x, d), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float b[8] = {__fdiv_rn(x, big_s), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        bad += ((e2m1x8(a) ^ e2m1x8(b)) & 0xFu) ? 1 : 0;
+        // the codes as the quantisers take them (packed pairs on the fast
+        // path; the first and last positions checked) against IEEE division
+        const float b[8] = {__fdiv_rn(x, big_s), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint32_t want = e2m1x8(b) & 0xFu;
+        if (d.fast) {
+            const float a[8] = {x, x, x, x, x, x, x, x};
+            const uint32_t c8 = e2m1x8_div_fast2(a, d2);
+            bad += ((c8 & 0xFu) != want || (c8 >> 28) != want) ? 1 : 0;
+        } else {
+            const float a[8] = {__fdiv_rn(x, d.s), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            bad += ((e2m1x8(a) & 0xFu) != want) ? 1 : 0;
+        }
     }
     atomicAdd(&counts[0], n);
     atomicAdd(&counts[1], bad);
