@@ -71,9 +71,10 @@ __device__ __forceinline__ uint2 cast8_div(const float* f, const ScaleDiv& d) {
 
 // Eight elements x * 2^-e (exact power-of-two division) -> eight E4M3 bytes.
 __device__ __forceinline__ uint2 cast8_mul(const float* f, float m) {
+    const uint64_t m2 = pair_f32(m, m);
     uint2 o;
-    o.x = e4m3x4(__fmul_rn(f[0], m), __fmul_rn(f[1], m), __fmul_rn(f[2], m), __fmul_rn(f[3], m));
-    o.y = e4m3x4(__fmul_rn(f[4], m), __fmul_rn(f[5], m), __fmul_rn(f[6], m), __fmul_rn(f[7], m));
+    o.x = e4m3x4_mul2(pair_f32(f[0], f[1]), pair_f32(f[2], f[3]), m2);
+    o.y = e4m3x4_mul2(pair_f32(f[4], f[5]), pair_f32(f[6], f[7]), m2);
     return o;
 }
 
@@ -558,7 +559,7 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
     const ScaleDiv sd = kPow2<GRAN> ? ScaleDiv{sc, 0.0f, false} : scale_div(sc, given == nullptr);
     const ScaleDiv2 sd2 = scale_div2(sd);
     auto codes4 = [&](float a0, float a1, float a2, float a3, auto fast) -> uint32_t {
-        if constexpr (kPow2<GRAN>) return e4m3x4(__fmul_rn(a0, sc), __fmul_rn(a1, sc), __fmul_rn(a2, sc), __fmul_rn(a3, sc));
+        if constexpr (kPow2<GRAN>) return e4m3x4_mul2(pair_f32(a0, a1), pair_f32(a2, a3), pair_f32(sc, sc));
         else if constexpr (decltype(fast)::value) return e4m3x4_div_fast2(pair_f32(a0, a1), pair_f32(a2, a3), sd2);
         else return e4m3x4(__fdiv_rn(a0, sc), __fdiv_rn(a1, sc), __fdiv_rn(a2, sc), __fdiv_rn(a3, sc));
     };
@@ -757,7 +758,17 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         uint32_t c0w[8], c1w[8];
         auto col_codes = [&](auto fast) {
             constexpr bool F = decltype(fast)::value;
-            if constexpr (F) {   // four rows of each of the two columns as two pairs each
+            if constexpr (kPow2<GRAN>) {   // x * 2^-e, four rows of each column as two pairs
+                const uint64_t m0 = pair_f32(sd0.s, sd0.s), m1 = pair_f32(sd1.s, sd1.s);
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    const uint32_t wa = colp[k * 64], wb = colp[(k + 1) * 64];
+                    const uint32_t wc = colp[(k + 2) * 64], wd = colp[(k + 3) * 64];
+                    c0w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), m0);
+                    c1w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), m1);
+                }
+                return;
+            } else if constexpr (F) {   // four rows of each of the two columns as two pairs each
                 const ScaleDiv2 e0 = scale_div2(sd0), e1 = scale_div2(sd1);
 #pragma unroll
                 for (int k = 0; k < 32; k += 4) {
@@ -837,7 +848,11 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                     if (c < cols) {
                         auto row_codes = [&](auto fast) {
                             constexpr bool F = decltype(fast)::value;
-                            if constexpr (F) {
+                            if constexpr (kPow2<GRAN>) {
+                                const uint64_t m2 = pair_f32(sdd.s, sdd.s);
+                                return make_uint2(e4m3x4_mul2(pair_bf16(v.x), pair_bf16(v.y), m2),
+                                                  e4m3x4_mul2(pair_bf16(v.z), pair_bf16(v.w), m2));
+                            } else if constexpr (F) {
                                 const ScaleDiv2 e2 = scale_div2(sdd);
                                 return make_uint2(e4m3x4_div_fast2(pair_bf16(v.x), pair_bf16(v.y), e2),
                                                   e4m3x4_div_fast2(pair_bf16(v.z), pair_bf16(v.w), e2));
