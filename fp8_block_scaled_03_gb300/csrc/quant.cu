@@ -162,41 +162,75 @@ struct RowSrc {
     int* status;          // gather: sticky status word for an index out of range
 };
 
-// e^x in float32 by one fixed sequence (each operation one IEEE rounding,
-// no fused multiply-add): Cody and Waite's reduction x = n ln2 + r ("Software
+// Float32 pair arithmetic, each half rounded on its own (round to nearest).
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ void unpair(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t splat2(float c) { return pair_f32(c, c); }
+
+// e^x of two elements in float32 by one fixed sequence (each operation one
+// IEEE rounding, no fused multiply-add; two elements per instruction where
+// the operation allows): Cody and Waite's reduction x = n ln2 + r ("Software
 // Manual for the Elementary Functions", 1980) with ln 2 split into a 16-bit
 // head and a tail, the Taylor series of e^r to r^7 in Horner form, and the
 // scaling by 2^(n-1) * 2.  +inf above 89, 0 below -87 (where 1 + e^x is 1 in
-// float32 already).  Within 2 float32 ulps of e^x.
-__device__ __forceinline__ float exp_seq(float x) {
-    // computed on x clamped to [-87, 89] (which keeps n in [-126, 128]), the
-    // out-of-range results selected at the end: no branch per element
-    const float xc = fminf(fmaxf(x, -0x1.5cp+6f), 0x1.64p+6f);
-    const float n = rintf(__fmul_rn(xc, 0x1.715476p+0f));       // x / ln 2
-    const float r = __fsub_rn(__fsub_rn(xc, __fmul_rn(n, 0x1.62e4p-1f)), __fmul_rn(n, 0x1.7f7d1cp-20f));
-    float p = 0x1.a01a02p-13f;                                  // 1/7!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);            // 1/6!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);             // 1/5!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);             // 1/4!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);             // 1/3!
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    const int ni = (int)n - 1;                                  // 2^(n-1) is a float32 (>= 2^-127)
-    const float half = ni >= -126 ? __int_as_float((ni + 127) << 23) : __int_as_float(0x00400000);
-    float e = __fmul_rn(__fmul_rn(p, half), 2.0f);
-    e = x > 0x1.64p+6f ? __int_as_float(0x7F800000) : e;         // 89: +inf
-    e = x < -0x1.5cp+6f ? 0.0f : e;                              // -87: 0
-    return e;
+// float32 already).  Within 2 float32 ulps of e^x.  The sequence runs on x
+// clamped to [-87, 89] (which keeps n in [-126, 128]); the out-of-range
+// results are selected at the end, with no branch per element.
+__device__ __forceinline__ uint64_t exp_seq2(float x0, float x1) {
+    const uint64_t xc = pair_f32(fminf(fmaxf(x0, -0x1.5cp+6f), 0x1.64p+6f), fminf(fmaxf(x1, -0x1.5cp+6f), 0x1.64p+6f));
+    float t0, t1;
+    unpair(fmul2(xc, splat2(0x1.715476p+0f)), t0, t1);
+    const float n0 = rintf(t0), n1 = rintf(t1);
+    const uint64_t n = pair_f32(n0, n1);
+    const uint64_t r = fsub2(fsub2(xc, fmul2(n, splat2(0x1.62e4p-1f))), fmul2(n, splat2(0x1.7f7d1cp-20f)));
+    uint64_t p = splat2(0x1.a01a02p-13f);
+    p = fadd2(fmul2(p, r), splat2(0x1.6c16c2p-10f));
+    p = fadd2(fmul2(p, r), splat2(0x1.111112p-7f));
+    p = fadd2(fmul2(p, r), splat2(0x1.555556p-5f));
+    p = fadd2(fmul2(p, r), splat2(0x1.555556p-3f));
+    p = fadd2(fmul2(p, r), splat2(0.5f));
+    p = fadd2(fmul2(p, r), splat2(1.0f));
+    p = fadd2(fmul2(p, r), splat2(1.0f));
+    const int ni0 = (int)n0 - 1, ni1 = (int)n1 - 1;
+    const float h0 = ni0 >= -126 ? __int_as_float((ni0 + 127) << 23) : __int_as_float(0x00400000);
+    const float h1 = ni1 >= -126 ? __int_as_float((ni1 + 127) << 23) : __int_as_float(0x00400000);
+    float e0, e1;
+    unpair(fmul2(fmul2(p, pair_f32(h0, h1)), splat2(2.0f)), e0, e1);
+    e0 = x0 > 0x1.64p+6f ? __int_as_float(0x7F800000) : e0;
+    e0 = x0 < -0x1.5cp+6f ? 0.0f : e0;
+    e1 = x1 > 0x1.64p+6f ? __int_as_float(0x7F800000) : e1;
+    e1 = x1 < -0x1.5cp+6f ? 0.0f : e1;
+    return pair_f32(e0, e1);
 }
 
-// Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up.
+// Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up; the
+// exponential, the sum and the product on element pairs.
 __device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
     float g[8], u[8], y[8];
     unpack8(gv, g);
     unpack8(uv, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(__fdiv_rn(g[i], __fadd_rn(1.0f, exp_seq(-g[i]))), u[i]);
+    for (int i = 0; i < 8; i += 2) {
+        float d0, d1;
+        unpair(fadd2(splat2(1.0f), exp_seq2(-g[i], -g[i + 1])), d0, d1);
+        unpair(fmul2(pair_f32(__fdiv_rn(g[i], d0), __fdiv_rn(g[i + 1], d1)), pair_f32(u[i], u[i + 1])), y[i], y[i + 1]);
+    }
     uint4 o;
     uint32_t* ow = &o.x;
 #pragma unroll
@@ -757,7 +791,7 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : scale_div(d1, true);
         uint32_t c0w[8], c1w[8];
         auto col_codes = [&](auto fast) {
-            constexpr bool F = decltype(fast)::value;
+            [[maybe_unused]] constexpr bool F = decltype(fast)::value;
             if constexpr (kPow2<GRAN>) {   // x * 2^-e, four rows of each column as two pairs
                 const uint64_t m0 = pair_f32(sd0.s, sd0.s), m1 = pair_f32(sd1.s, sd1.s);
 #pragma unroll
@@ -767,7 +801,6 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                     c0w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), m0);
                     c1w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), m1);
                 }
-                return;
             } else if constexpr (F) {   // four rows of each of the two columns as two pairs each
                 const ScaleDiv2 e0 = scale_div2(sd0), e1 = scale_div2(sd1);
 #pragma unroll
@@ -777,16 +810,16 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                     c0w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), e0);
                     c1w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), e1);
                 }
-                return;
-            }
+            } else {
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-                const float2 a = tile_scaled2<GRAN, F>(colp[k * 64], sd0, sd1);
-                const float2 b = tile_scaled2<GRAN, F>(colp[(k + 1) * 64], sd0, sd1);
-                const float2 c = tile_scaled2<GRAN, F>(colp[(k + 2) * 64], sd0, sd1);
-                const float2 d = tile_scaled2<GRAN, F>(colp[(k + 3) * 64], sd0, sd1);
-                c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
-                c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
+                for (int k = 0; k < 32; k += 4) {
+                    const float2 a = tile_scaled2<GRAN, F>(colp[k * 64], sd0, sd1);
+                    const float2 b = tile_scaled2<GRAN, F>(colp[(k + 1) * 64], sd0, sd1);
+                    const float2 c = tile_scaled2<GRAN, F>(colp[(k + 2) * 64], sd0, sd1);
+                    const float2 d = tile_scaled2<GRAN, F>(colp[(k + 3) * 64], sd0, sd1);
+                    c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
+                    c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
+                }
             }
         };
         if (!kPow2<GRAN> && sd0.fast && sd1.fast) col_codes(std::true_type{});
