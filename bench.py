@@ -317,9 +317,22 @@ def moe_bench(torch, fp, dev, pk, flush):
     run_sw = lambda: fp.fp8_swiglu_quantize(d_gu, "mxfp8", q=qy, scales=sy)  # noqa: E731
     run_dn = lambda: fp.fp8_grouped_gemm(qy, sy, qdn, sdn, off, "mxfp8", out=d_dn, ws=ws)  # noqa: E731
 
+    # the same dispatch as two launches: the token matrix quantised once, then
+    # its code rows gathered into expert order (bit-identical to run_ga)
+    qx_t, sx_t, _ = fp.fp8_quantize(x, "mxfp8", ws=ws)
+
+    def run_qg():
+        fp.fp8_quantize(x, "mxfp8", q=qx_t, scales=sx_t, ws=ws)
+        fp.fp8_gather_rows(qx_t, sx_t, idx, "mxfp8", q=qa, scales=sa, ws=ws)
+
     def layer():
         run_ga(); run_gu(); run_sw(); run_dn()  # noqa: E702
 
+    def layer_qg():
+        run_qg(); run_gu(); run_sw(); run_dn()  # noqa: E702
+
+    ms_qg, _ = time_fn(torch, run_qg, 10, flush)
+    ms_layer_qg, _ = time_fn(torch, layer_qg, 10, flush)
     ms_ga, _ = time_fn(torch, run_ga, 10, flush)
     ms_gu, _ = time_fn(torch, run_gu, 10, flush)
     ms_sw, _ = time_fn(torch, run_sw, 10, flush)
@@ -336,6 +349,11 @@ def moe_bench(torch, fp, dev, pk, flush):
             "down": {"tflops": round(t_dn, 1), "ms": round(ms_dn, 3), "frac": round(t_dn / peak, 3)},
             "gather_quantize": {"gbs": round(g_ga, 1), "us": round(ms_ga * 1e3, 2),
                                 "frac": round(g_ga / pk["hbm_gbs"], 3), "bytes": b_ga},
+            "quantize_then_gather": {"gbs": round(b_ga / (ms_qg * 1e-3) / 1e9, 1), "us": round(ms_qg * 1e3, 2),
+                                     "frac": round(b_ga / (ms_qg * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes": b_ga,
+                                     "launches": 2},
+            "layer_quantize_then_gather": {"ms": round(ms_layer_qg, 3),
+                                           "tflops": round((f_gu + f_dn) / ms_layer_qg / 1e9, 1), "kernels": 5},
             "swiglu_quantize": {"gbs": round(g_sw, 1), "us": round(ms_sw * 1e3, 2),
                                 "frac": round(g_sw / pk["hbm_gbs"], 3), "bytes": b_sw},
             "layer": {"ms": round(ms_layer, 3), "tflops": round((f_gu + f_dn) / ms_layer / 1e9, 1),

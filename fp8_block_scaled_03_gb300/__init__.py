@@ -40,7 +40,7 @@ STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNS
           -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE", -7: "FP8BS_EINDEX"}
 EINDEX = -7
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
-           "fp8_quantize_gathered", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
+           "fp8_quantize_gathered", "fp8_gather_rows", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
            "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
            "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4",
            "fp8bs_test_quotient_sweep")
@@ -70,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
     lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.fp8_quantize_gathered.argtypes = [P, I64, I64, I64, P, I64, I, P, P, P, SZ, P]
+    lib.fp8_gather_rows.argtypes = [P, P, I64, I64, I, P, I64, P, P, P, SZ, P]
     lib.fp8_swiglu_quantize.argtypes = [P, I64, I64, I64, I, P, P, P]
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
@@ -290,6 +291,36 @@ def fp8_quantize_gathered(x: torch.Tensor, token_index: torch.Tensor, gran, *, q
     rc = load_library().fp8_quantize_gathered(_ptr(x), tokens, cols, x.stride(0), _ptr(token_index), rows, g,
                                               _ptr(q), _ptr(scales), _ptr(ws), ws.numel(), _stream(stream))
     _check("fp8_quantize_gathered", rc)
+    return q, scales
+
+
+def fp8_gather_rows(q_src: torch.Tensor, scales_src: torch.Tensor, token_index: torch.Tensor, gran, *, q=None,
+                    scales=None, ws=None, stream=None):
+    """Rows token_index[r] of already quantised (q_src, scales_src) in expert order; returns
+    (q, scales).  Equals fp8_quantize_gathered on the BF16 rows those codes came from.  An
+    index outside [0, tokens) gives an all-zero row and sets FP8BS_EINDEX (read_status)."""
+    g = _gran(gran)
+    if q_src.dtype != torch.uint8 or q_src.dim() != 2 or not q_src.is_contiguous():
+        raise ValueError("q_src must be a contiguous 2-D uint8 tensor of codes")
+    tokens, cols = q_src.shape
+    shp, dt = scale_shape(g, tokens, cols)
+    if scales_src.dtype != dt or tuple(scales_src.shape) != tuple(shp) or not scales_src.is_contiguous():
+        raise ValueError(f"scales_src must be a contiguous {dt} tensor of shape {tuple(shp)}")
+    if token_index.dtype != torch.int64 or not token_index.is_cuda or token_index.dim() != 1:
+        raise ValueError("token_index must be a 1-D CUDA int64 tensor")
+    if not token_index.is_contiguous():
+        raise ValueError("token_index must be contiguous")
+    rows = token_index.numel()
+    dev = q_src.device
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        shp, dt = scale_shape(g, rows, cols)
+        scales = torch.empty(shp, dtype=dt, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    rc = load_library().fp8_gather_rows(_ptr(q_src), _ptr(scales_src), tokens, cols, g, _ptr(token_index), rows,
+                                        _ptr(q), _ptr(scales), _ptr(ws), ws.numel(), _stream(stream))
+    _check("fp8_gather_rows", rc)
     return q, scales
 
 

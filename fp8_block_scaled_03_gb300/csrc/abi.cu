@@ -178,6 +178,33 @@ int fp8_quantize_gathered(const void* x, int64_t tokens, int64_t cols, int64_t l
     return cuda_status(launch_quantize_rows_src(j, token_index, tokens, 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, int64_t cols, int gran,
+                    const int64_t* token_index, int64_t rows, void* q, void* scales, void* workspace,
+                    size_t workspace_bytes, fp8bs_stream_t stream) {
+    if (tokens < 0 || rows < 0 || cols < 0) return FP8BS_EINVAL;
+    if (gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
+    if (!is_moe_rowwise(gran)) return FP8BS_EUNSUPPORTED;
+    if (cols % 8 != 0) return FP8BS_EINVAL;
+    if (rows == 0 || cols == 0) return FP8BS_OK;
+    // with no tokens the sources are never read (every index is out of range) and may be NULL
+    if (((q_src == nullptr || scales_src == nullptr) && tokens > 0) || token_index == nullptr || q == nullptr ||
+        scales == nullptr)
+        return FP8BS_EINVAL;
+    if (!aligned16(q_src) || !aligned16(q) || !scales_aligned(scales, gran) || !scales_aligned(scales_src, gran) ||
+        (reinterpret_cast<uintptr_t>(token_index) & 7u))
+        return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    GatherJob j{};
+    j.q_src = static_cast<const uint8_t*>(q_src);
+    j.s_src = scales_src;
+    j.tokens = tokens; j.cols = cols; j.rows = rows;
+    j.idx = token_index;
+    j.q = static_cast<uint8_t*>(q); j.s = scales;
+    j.gran = gran;
+    j.status = static_cast<int*>(workspace);
+    return cuda_status(launch_gather_rows(j, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h, int gran, void* q, void* scales,
                         fp8bs_stream_t stream) {
     if (rows < 0 || inter < 0) return FP8BS_EINVAL;

@@ -37,6 +37,19 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t s);
 // row r is silu(x[r, 0:cols]) * x[r, up:up+cols]).
 int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int64_t tokens, int64_t up,
                              cudaStream_t s);
+// Gather of already quantised rows (1x128, MXFP8, 1x128 power-of-two):
+// row r of q / s is row idx[r] of q_src / s_src ([tokens, cols] layouts).
+struct GatherJob {
+    const uint8_t* q_src;
+    const void* s_src;
+    int64_t tokens, cols, rows;
+    const int64_t* idx;
+    uint8_t* q;
+    void* s;
+    int gran;
+    int* status;
+};
+int launch_gather_rows(const GatherJob& j, cudaStream_t s);
 // Exhaustive check of the FP32-scale division used by the casts (test hook).
 int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t s);
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,

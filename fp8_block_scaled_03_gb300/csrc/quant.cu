@@ -1106,6 +1106,65 @@ int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t st
     return (int)cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- gather of quantised rows
+// q[r] = q_src[idx[r]] and the scale row likewise, for the row-wise layouts
+// of 1x128 (FP32 scales), MXFP8 and 1x128 power-of-two (byte scales).  The
+// codes and scales of a row depend on that row alone, so this equals the
+// gathered quantiser on the same tokens.  An index outside [0, tokens)
+// gives the all-zero row (zero codes, the scale of an all-zero group: 1.0,
+// or the byte 0 of exponent -127) and sets kStatusIndex.  One warp per row;
+// V16: 16-byte code chunks (cols % 16 == 0), else 8-byte ones.
+template <int GRAN, bool V16>
+__global__ void __launch_bounds__(kThreads)
+gather_rows_kernel(const uint8_t* __restrict__ q_src, const void* __restrict__ s_src, int64_t tokens, int64_t cols,
+                   const int64_t* __restrict__ idx, int64_t rows, uint8_t* __restrict__ q, void* __restrict__ s,
+                   int* status) {
+    constexpr int CH = V16 ? 16 : 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t ng = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
+    for (int64_t r = gw; r < rows; r += nw) {
+        const int64_t t = __ldg(idx + r);
+        const bool valid = t >= 0 && t < tokens;
+        if (!valid && lane == 0 && status != nullptr) atomicExch(status, kStatusIndex);
+        const uint8_t* src = q_src + (valid ? t : 0) * cols;
+        uint8_t* dst = q + r * cols;
+        for (int64_t c = (int64_t)CH * lane; c < cols; c += 32 * CH) {
+            if constexpr (V16) stg_cs_v4(dst + c, valid ? ldg_v4(src + c) : make_uint4(0, 0, 0, 0));
+            else stg_cs_v2(dst + c, valid ? ldg_v2(src + c) : make_uint2(0, 0));
+        }
+        for (int64_t g = lane; g < ng; g += 32) {
+            if constexpr (GRAN == kGranTok)
+                static_cast<float*>(s)[r * ng + g] = valid ? __ldg(static_cast<const float*>(s_src) + t * ng + g) : 1.0f;
+            else
+                static_cast<uint8_t*>(s)[r * ng + g] = valid ? __ldg(static_cast<const uint8_t*>(s_src) + t * ng + g)
+                                                             : (uint8_t)0;
+        }
+    }
+}
+
+template <int GRAN>
+static int launch_gather_g(const GatherJob& j, cudaStream_t st) {
+    const int nb = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(j.rows, kThreads / 32), sm_count() * 8));
+    if (j.cols % 16 == 0)
+        gather_rows_kernel<GRAN, true><<<nb, kThreads, 0, st>>>(j.q_src, j.s_src, j.tokens, j.cols, j.idx, j.rows,
+                                                               j.q, j.s, j.status);
+    else
+        gather_rows_kernel<GRAN, false><<<nb, kThreads, 0, st>>>(j.q_src, j.s_src, j.tokens, j.cols, j.idx, j.rows,
+                                                                j.q, j.s, j.status);
+    return (int)cudaGetLastError();
+}
+
+int launch_gather_rows(const GatherJob& j, cudaStream_t st) {
+    switch (j.gran) {
+    case kGranTok: return launch_gather_g<kGranTok>(j, st);
+    case kGranMx: return launch_gather_g<kGranMx>(j, st);
+    case kGranTokP2: return launch_gather_g<kGranTokP2>(j, st);
+    default: return (int)cudaErrorInvalidValue;
+    }
+}
+
 template <int SRC>
 static int launch_rows_src(const QuantJob& j, const RowSrc& src, int nb, cudaStream_t st) {
     switch (j.gran) {

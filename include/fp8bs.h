@@ -206,6 +206,34 @@ int fp8_quantize_gathered(const void* x, int64_t tokens, int64_t cols, int64_t l
                           void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
 
 /*
+ * fp8_gather_rows -- the MoE dispatch of rows that are already quantised:
+ * row r of (q, scales) is row token_index[r] of (q_src, scales_src).  A
+ * row's codes and scales depend on that row alone, so fp8_quantize of x
+ * followed by this call gives exactly what fp8_quantize_gathered gives from
+ * x; the token matrix is then quantised once, not once per routed copy
+ * (the same MoE step, "Low Precision RL", section "3. Unified MXFP8
+ * (Blackwell)"; the pages do not describe it).
+ *
+ *   q_src, scales_src  codes [tokens, cols] (pitch cols) and scales of
+ *                fp8_quantize at `gran`, 16-byte aligned codes, scales
+ *                aligned as fp8_quantize's; cols % 8 == 0
+ *   gran         TOKEN_1x128, MXFP8_1x32 or TOKEN_1x128_POW2 (the other
+ *                valid granularities return FP8BS_EUNSUPPORTED)
+ *   token_index  DEVICE int64 [rows], 8-byte aligned (repeats allowed)
+ *   q, scales    [rows, cols] in the same layouts, written
+ *   workspace    required (FP8BS_WORKSPACE_BYTES): its status word receives
+ *                FP8BS_EINDEX when an index is outside [0, tokens); that row
+ *                gets zero codes and the scale of an all-zero group (1.0f
+ *                for TOKEN_1x128, the byte 0 otherwise), as in
+ *                fp8_quantize_gathered; the other rows are unaffected.
+ * rows or cols == 0 is a no-op.  tokens may be 0 (then q_src and scales_src
+ * may be NULL).
+ */
+int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, int64_t cols, int gran,
+                    const int64_t* token_index, int64_t rows, void* q, void* scales, void* workspace,
+                    size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
  * fp8_swiglu_quantize -- the SwiGLU activation between the gate+up and the
  * down projection of an expert MLP, quantised row-wise for the down GEMM
  * (Qwen3 MoE experts, "Low Precision RL", section "3. Unified MXFP8

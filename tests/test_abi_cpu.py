@@ -143,6 +143,29 @@ def test_gathered_quantize_rejects_bad_arguments(lib):
     assert g(None, 0, 128, 128, None, 0, 3, None, None, None, 0, None) == 0         # empty: no-op
 
 
+def test_gather_rows_rejects_bad_arguments(lib):
+    # every call fails a host check before any launch (the pointers are fake)
+    g = lib.fp8_gather_rows
+    WS = 16384
+    assert g(None, FAKE, 8, 128, 3, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -1       # null codes source
+    assert g(FAKE, None, 8, 128, 3, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -1       # null scales source
+    assert g(FAKE, FAKE, 8, 128, 3, None, 4, FAKE, FAKE, FAKE, WS, None) == -1       # null index
+    assert g(FAKE, FAKE, 8, 128, 3, FAKE, 4, None, FAKE, FAKE, WS, None) == -1       # null output
+    assert g(FAKE, FAKE, 8, 124, 3, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -1       # cols % 8
+    assert g(FAKE, FAKE, -1, 128, 3, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -1      # negative tokens
+    assert g(FAKE, FAKE, 8, 128, 9, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -1       # bad gran
+    for unsupported in (0, 2, 4, 6, 7):
+        assert g(FAKE, FAKE, 8, 128, unsupported, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -3
+    assert g(FAKE, FAKE, 8, 128, 3, ODD4, 4, FAKE, FAKE, FAKE, WS, None) == -2       # index 8-byte aligned
+    assert g(MISALIGNED, FAKE, 8, 128, 3, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -2
+    assert g(FAKE, FAKE, 8, 128, 3, FAKE, 4, MISALIGNED, FAKE, FAKE, WS, None) == -2
+    assert g(FAKE, ODD4, 8, 128, 1, FAKE, 4, FAKE, FAKE, FAKE, WS, None) == -2       # FP32 source scales
+    assert g(FAKE, FAKE, 8, 128, 1, FAKE, 4, FAKE, ODD4, FAKE, WS, None) == -2       # FP32 scales
+    assert g(FAKE, FAKE, 8, 128, 3, FAKE, 4, FAKE, FAKE, None, 0, None) == -6        # status word needed
+    assert g(FAKE, FAKE, 8, 128, 3, FAKE, 4, FAKE, FAKE, FAKE, 1024, None) == -6
+    assert g(None, None, 0, 128, 3, None, 0, None, None, None, 0, None) == 0         # empty: no-op
+
+
 def test_swiglu_quantize_rejects_bad_arguments(lib):
     s = lib.fp8_swiglu_quantize
     assert s(None, 4, 128, 256, 3, FAKE, FAKE, None) == -1          # null h

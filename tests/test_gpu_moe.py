@@ -105,6 +105,70 @@ def test_gathered_empty_and_no_tokens():
     assert int(q.count_nonzero()) == 0 and int(s.count_nonzero()) == 0
 
 
+# ---------------------------------------------------------------- gather of quantised rows
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("cols", (1000, 264, 2048))
+def test_gather_rows_after_quantise_matches_oracle(gran, cols):
+    """fp8_quantize of the token matrix, then fp8_gather_rows, against the
+    oracle's gathered quantisation: ragged last groups and 8-byte code
+    chunks (1000, 264 columns), 16-byte chunks (2048), repeated indices."""
+    tokens = 301
+    bits = synth.activations((tokens, cols), seed=81 + cols, outlier_frac=0.01, outlier_mult=60.0)
+    idx = synth.rng(82).integers(0, tokens, size=777).astype(np.int64)
+    idx[:3] = [0, tokens - 1, 0]
+    qt, st, _ = fp.fp8_quantize(to_dev_bf16(bits), gran)
+    ws = torch.zeros(fp.load_library().fp8bs_workspace_size(), dtype=torch.uint8, device="cuda")
+    q, s = fp.fp8_gather_rows(qt, st, torch.from_numpy(idx).cuda(), gran, ws=ws)
+    torch.cuda.synchronize()
+    pq, ps = OM.quantize_gathered(to_f32(bits), idx, gran)
+    assert_same(q, s, pq, ps, gran, "gather of quantised rows")
+    assert fp.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("gran", GRANS)
+def test_gather_rows_out_of_range_like_gathered_quantise(gran):
+    """Out-of-range indices: the same all-zero rows and status as the
+    gathered quantiser; no tokens at all; no rows."""
+    tokens, cols = 40, 256
+    bits = synth.activations((tokens, cols), seed=74)
+    idx = torch.tensor([5, -1, 39, 40, 7, 2**40, 0], dtype=torch.int64, device="cuda")
+    ws = torch.zeros(fp.load_library().fp8bs_workspace_size(), dtype=torch.uint8, device="cuda")
+    qt, st, _ = fp.fp8_quantize(to_dev_bf16(bits), gran)
+    q, s = fp.fp8_gather_rows(qt, st, idx, gran, ws=ws)
+    assert fp.read_status(ws) == fp.EINDEX
+    q2, s2 = fp.fp8_quantize_gathered(to_dev_bf16(bits), idx, gran, ws=ws)
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.uint8), s2.view(torch.uint8))
+    fp.clear_status(ws)
+    none_q = torch.zeros((0, cols), dtype=torch.uint8, device="cuda")
+    shp, dt = fp.scale_shape(gran, 0, cols)
+    none_s = torch.zeros(shp, dtype=dt, device="cuda")
+    q, s = fp.fp8_gather_rows(none_q, none_s, idx[:4], gran, ws=ws)
+    assert fp.read_status(ws) == fp.EINDEX           # no token exists: every row is out of range
+    zq, zs = OM.ROWWISE[gran](np.zeros((1, cols), np.float32))
+    assert np.array_equal(np_u8(q), np.repeat(zq, 4, axis=0))
+    assert np.array_equal(scales_np(s, gran), np.repeat(zs, 4, axis=0))
+    q, s = fp.fp8_gather_rows(qt, st, torch.zeros(0, dtype=torch.int64, device="cuda"), gran)
+    assert q.shape == (0, cols)
+
+
+@pytest.mark.parametrize("gran", ("mxfp8", "1x128"))
+def test_gather_rows_full_moe_layer_equals_gathered_quantise(gran):
+    """MoE layer size (16384 tokens x 2048, top-8 of 128 experts): the two
+    paths give the same bytes, compared on the device in full."""
+    tokens, hidden, experts, topk = 16384, 2048, 128, 8
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x = (torch.randn((tokens, hidden), generator=g, device="cuda")).to(torch.bfloat16)
+    order, _ = synth.moe_routing(tokens, experts, topk, seed=0)
+    idx = torch.from_numpy(np.asarray(order, dtype=np.int64)).cuda()
+    ws = torch.zeros(fp.load_library().fp8bs_workspace_size(), dtype=torch.uint8, device="cuda")
+    qt, st, _ = fp.fp8_quantize(x, gran, ws=ws)
+    q, s = fp.fp8_gather_rows(qt, st, idx, gran, ws=ws)
+    q2, s2 = fp.fp8_quantize_gathered(x, idx, gran, ws=ws)
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.uint8), s2.view(torch.uint8))
+    assert fp.read_status(ws) == 0
+
+
 @pytest.mark.parametrize("gran", ("mxfp8", "1x128"))
 def test_gathered_full_moe_layer_sampled(gran):
     """Routed tokens of the MoE layer (16384 tokens x 2048, 128 experts, top 8:
