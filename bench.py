@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--kernel", default=None,
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
                              "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "moe_gather_quant",
-                             "moe_swiglu_quant", "moe_layer", "nvfp4"],
+                             "moe_swiglu_quant", "moe_quant_then_gather", "moe_layer", "nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
@@ -608,11 +608,20 @@ def single_kernel(args, torch, fp, dev):
             fp.fp8_swiglu_quantize(h, "mxfp8", q=qy, scales=sy)
             fp.fp8_grouped_gemm(qy, sy, qdn, sdn, off, "mxfp8", out=out, ws=ws)
         work = 2 * rows * 1536 * 2048 + 2 * rows * 2048 * 768
-    elif name in ("moe_gather_quant", "moe_swiglu_quant"):
+    elif name in ("moe_gather_quant", "moe_swiglu_quant", "moe_quant_then_gather"):
         import synth
         token_index, offsets = synth.moe_routing(16384, 128, 8, seed=0)
         rows = int(offsets[-1])
-        if name == "moe_gather_quant":
+        if name == "moe_quant_then_gather":
+            x = act((16384, 2048), 0.001, 100.0)
+            idx = torch.from_numpy(token_index).to(dev)
+            qt, st, _ = fp.fp8_quantize(x, "mxfp8", ws=ws)
+            q, s_ = fp.fp8_gather_rows(qt, st, idx, "mxfp8", ws=ws)
+
+            def fn():
+                fp.fp8_quantize(x, "mxfp8", q=qt, scales=st, ws=ws)
+                fp.fp8_gather_rows(qt, st, idx, "mxfp8", q=q, scales=s_, ws=ws)
+        elif name == "moe_gather_quant":
             x = act((16384, 2048), 0.001, 100.0)
             idx = torch.from_numpy(token_index).to(dev)
             q, s_ = fp.fp8_quantize_gathered(x, idx, "mxfp8", ws=ws)
