@@ -37,13 +37,15 @@ NVFP4_GRANS = (4, 7)
 FLAG_GIVEN_TENSOR_SCALE = 1
 FLAG_NVFP4_4OVER6 = 2
 STATUS = {0: "FP8BS_OK", -1: "FP8BS_EINVAL", -2: "FP8BS_EALIGN", -3: "FP8BS_EUNSUPPORTED",
-          -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE", -7: "FP8BS_EINDEX"}
+          -4: "FP8BS_ECUDA", -5: "FP8BS_ETIMEOUT", -6: "FP8BS_EWORKSPACE", -7: "FP8BS_EINDEX", -8: "FP8BS_EOFFSETS"}
 EINDEX = -7
+EOFFSETS = -8
 EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_block_gemm", "fp8_grouped_gemm",
            "fp8_quantize_gathered", "fp8_gather_rows", "fp8_swiglu_quantize", "fp8_quantize_per_tensor_noalloc",
-           "fp8bs_workspace_size", "fp8bs_read_status", "fp8bs_clear_status",
+           "fp8bs_workspace_size", "fp8bs_workspace_size_for", "fp8bs_read_status", "fp8bs_clear_status",
            "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4",
-           "fp8bs_test_quotient_sweep")
+           "fp8bs_test_stalled_gemm_blockwise",
+           "fp8bs_test_quotient_sweep", "fp8bs_mma_peak")
 
 _lib = None
 
@@ -68,17 +70,23 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_quantize_transposed.argtypes = [P, I64, I64, I64, I, P, P, P, P, P, U, P, SZ, P]
     lib.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, P, I64, P]
     lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
-    lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
+    lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.fp8_quantize_gathered.argtypes = [P, I64, I64, I64, P, I64, I, P, P, P, SZ, P]
     lib.fp8_gather_rows.argtypes = [P, P, I64, I64, I, P, I64, P, P, P, SZ, P]
     lib.fp8_swiglu_quantize.argtypes = [P, I64, I64, I64, I, P, P, P]
     lib.fp8bs_test_stalled_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
     lib.fp8bs_test_stalled_gemm_nvfp4.restype = I
+    lib.fp8bs_test_stalled_gemm_blockwise.argtypes = [P, P, I, P, P, I, I64, I64, I64, P, ctypes.c_uint64, P, SZ, P]
+    lib.fp8bs_test_stalled_gemm_blockwise.restype = I
     lib.fp8bs_test_quotient_sweep.argtypes = [P, I, P]
     lib.fp8bs_test_quotient_sweep.restype = I
+    lib.fp8bs_mma_peak.argtypes = [I, I, I, I, P, P, SZ, P]
+    lib.fp8bs_mma_peak.restype = I
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
+    lib.fp8bs_workspace_size_for.restype = SZ
+    lib.fp8bs_workspace_size_for.argtypes = [I, I64, I64, I, U]
     lib.fp8bs_read_status.argtypes = [P, P]
     lib.fp8bs_clear_status.argtypes = [P, P]
     lib.fp8bs_status_string.restype = ctypes.c_char_p
@@ -251,19 +259,24 @@ def fp8_block_gemm(a, a_scales, a_gran, b, b_scales, b_gran, a_tensor_scale=None
     return out
 
 
-def fp8_grouped_gemm(a, a_scales, b, b_scales, offsets, gran, *, out=None, ws=None, stream=None):
-    """MoE grouped GEMM: rows offsets[e]..offsets[e+1] of A times B[e]^T; D BF16 [rows, n]."""
+def fp8_grouped_gemm(a, a_scales, b, b_scales, offsets, gran, *, a_tensor_scale=None, b_tensor_scale=None,
+                     k: Optional[int] = None, out=None, ws=None, stream=None):
+    """MoE grouped GEMM: rows offsets[e]..offsets[e+1] of A times B[e]^T; D BF16 [rows, n].
+    NVFP4: a, b packed codes ([rows, k/2], [experts, n, k/2]); a_tensor_scale [1] or
+    [rows] ("nvfp4_row"), b_tensor_scale [experts]."""
     g = _gran(gran)
-    experts, n, k = b.shape
+    experts, n = b.shape[0], b.shape[1]
     rows = a.shape[0]
+    if k is None:
+        k = a.shape[1] * (2 if g in NVFP4_GRANS else 1)
     if offsets.dtype != torch.int64 or not offsets.is_cuda or offsets.numel() != experts + 1:
         raise ValueError("offsets must be a CUDA int64 tensor of experts+1 entries")
     if out is None:
         out = torch.empty((rows, n), dtype=torch.bfloat16, device=a.device)
     ws = ws if ws is not None else workspace(a.device)
-    rc = load_library().fp8_grouped_gemm(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(offsets),
-                                         experts, rows, n, k, g, _ptr(out), _ptr(ws), ws.numel(),
-                                         _stream(stream))
+    rc = load_library().fp8_grouped_gemm(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(a_tensor_scale),
+                                         _ptr(b_tensor_scale), _ptr(offsets), experts, rows, n, k, g, _ptr(out),
+                                         _ptr(ws), ws.numel(), _stream(stream))
     _check("fp8_grouped_gemm", rc)
     return out
 
@@ -361,6 +374,20 @@ def test_stalled_gemm(a, a_scales, b, b_scales, wait_limit_ns: int, *, out=None,
                                                   _stream(stream))
 
 
+def test_stalled_gemm_blockwise(a, a_scales, a_gran, b, b_scales, b_gran, wait_limit_ns: int, *, out=None, ws=None,
+                                stream=None) -> int:
+    """As test_stalled_gemm, for the FP32-scale blockwise GEMM."""
+    m, k = a.shape
+    n = b.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    ws = ws if ws is not None else workspace(a.device)
+    return load_library().fp8bs_test_stalled_gemm_blockwise(_ptr(a), _ptr(a_scales), _gran(a_gran), _ptr(b),
+                                                            _ptr(b_scales), _gran(b_gran), m, n, k, _ptr(out),
+                                                            int(wait_limit_ns), _ptr(ws), ws.numel(),
+                                                            _stream(stream))
+
+
 def test_stalled_gemm_nvfp4(a, a_scales, b, b_scales, a_tensor_scale, b_tensor_scale, wait_limit_ns: int, *, k=None,
                             out=None, ws=None, stream=None) -> int:
     """As test_stalled_gemm, for the NVFP4 GEMM (packed codes [rows, k/2])."""
@@ -382,3 +409,16 @@ def test_quotient_sweep(nvfp4: bool = False, stream=None):
            load_library().fp8bs_test_quotient_sweep(_ptr(counts), int(bool(nvfp4)), _stream(stream)))
     c = counts.cpu().tolist()
     return c[0], c[1], c[2]
+
+
+MMA_PEAK_K = {0: 32, 1: 32, 2: 64}      # K per instruction: E4M3, MXFP8, NVFP4
+
+
+def mma_peak(kind: int, n: int = 256, iters: int = 1024, pattern: int = 0, *, out=None, ws=None, stream=None) -> int:
+    """Launch the tensor-core throughput loop (fp8bs_mma_peak) on the current
+    stream; returns the FLOPs the launch performs (time it with CUDA events)."""
+    ws = ws if ws is not None else workspace()
+    _check("fp8bs_mma_peak", load_library().fp8bs_mma_peak(int(kind), int(n), int(iters), int(pattern), _ptr(out),
+                                                           _ptr(ws), ws.numel(), _stream(stream)))
+    sms = torch.cuda.get_device_properties(ws.device).multi_processor_count
+    return sms * iters * 4 * 2 * 128 * n * MMA_PEAK_K[int(kind)]

@@ -268,16 +268,24 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
 
 int fp8_grouped_gemm(const void* a, const void* a_scales,
                      const void* b, const void* b_scales,
+                     const float* a_tensor_scale, const float* b_tensor_scale,
                      const int64_t* offsets, int experts, int64_t total_rows,
                      int64_t n, int64_t k, int gran, void* d,
                      void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr ||
         offsets == nullptr)
         return FP8BS_EINVAL;
-    if (experts <= 0 || experts > 1024 || total_rows < 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 128 != 0)
+    if (gran < 0 || gran > FP8BS_NVFP4_ROW_1x16) return FP8BS_EINVAL;
+    const bool nv = is_nvfp4(gran);
+    if (experts <= 0 || experts > 1024 || total_rows < 0 || n <= 0 || k <= 0 || n % 8 != 0 ||
+        k % (nv ? 256 : 128) != 0)
         return FP8BS_EINVAL;
+    if (nv && (a_tensor_scale == nullptr || b_tensor_scale == nullptr)) return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
     if (!aligned4(a_scales) || !aligned4(b_scales) || (reinterpret_cast<uintptr_t>(offsets) & 7u)) return FP8BS_EALIGN;
+    if (nv && (!aligned16(a_scales) || !aligned16(b_scales) || !aligned4(a_tensor_scale) ||
+               !aligned4(b_tensor_scale)))
+        return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
     if (total_rows == 0) return FP8BS_OK;
     GemmJob j{};
@@ -298,7 +306,12 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
         j.a_gran = FP8BS_TOKEN_1x128_POW2; j.b_gran = FP8BS_BLOCK_128x128_POW2;
         return cuda_status(launch_gemm_mx(j, st));
     }
-    if (gran < 0 || gran > FP8BS_BLOCK_128x128_POW2) return FP8BS_EINVAL;
+    if (nv) {
+        j.a_gran = j.b_gran = FP8BS_NVFP4_1x16;
+        j.a_ts = a_tensor_scale; j.b_ts = b_tensor_scale;
+        j.a_ts_rows = gran == FP8BS_NVFP4_ROW_1x16;
+        return cuda_status(launch_gemm_mx(j, st));
+    }
     return FP8BS_EUNSUPPORTED;
 }
 
@@ -321,6 +334,31 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
     j.wait_ns = wait_limit_ns;
     j.stall_stage0 = 1;
     return cuda_status(launch_gemm_mx(j, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_test_stalled_gemm_blockwise(const void* a, const void* a_scales, int a_gran, const void* b,
+                                      const void* b_scales, int b_gran, int64_t m, int64_t n, int64_t k, void* d,
+                                      uint64_t wait_limit_ns, void* workspace, size_t workspace_bytes,
+                                      fp8bs_stream_t stream) {
+    if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
+        return FP8BS_EINVAL;
+    if (a_gran < FP8BS_PER_TENSOR || a_gran > FP8BS_BLOCK_128x128 || b_gran < FP8BS_PER_TENSOR ||
+        b_gran > FP8BS_BLOCK_128x128)
+        return FP8BS_EINVAL;
+    if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 128 != 0) return FP8BS_EINVAL;
+    if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return FP8BS_EINVAL;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned4(a_scales) || !aligned4(b_scales))
+        return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    GemmJob j{};
+    j.a = a; j.sa = a_scales; j.a_gran = a_gran;
+    j.b = b; j.sb = b_scales; j.b_gran = b_gran;
+    j.m = m; j.n = n; j.k = k; j.d = d;
+    j.status = static_cast<int*>(workspace);
+    j.offsets = nullptr; j.experts = 0;
+    j.wait_ns = wait_limit_ns;
+    j.stall_stage0 = 1;
+    return cuda_status(launch_gemm_blockwise(j, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const void* b, const void* b_scales,
@@ -354,7 +392,38 @@ int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_strea
     return cuda_status(launch_quotient_sweep(counts, nvfp4, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_mma_peak(int kind, int n, int iters, int pattern, float* out, void* workspace, size_t workspace_bytes,
+                   fp8bs_stream_t stream) {
+    if (kind < 0 || kind > 2 || (n != 64 && n != 128 && n != 256) || (kind != 0 && n == 64) || iters < 1 ||
+        iters > (1 << 24) ||
+        (pattern != 0 && pattern != 1))
+        return FP8BS_EINVAL;
+    if (out != nullptr && !aligned4(out)) return FP8BS_EALIGN;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    return cuda_status(launch_mma_peak(kind, sm_count(), iters, n, pattern, out, static_cast<int*>(workspace),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t fp8bs_workspace_size(void) { return kWorkspaceBytes; }
+
+size_t fp8bs_workspace_size_for(int op, int64_t rows, int64_t cols, int gran, unsigned flags) {
+    if (rows < 0 || cols < 0 || gran < FP8BS_PER_TENSOR || gran > FP8BS_NVFP4_ROW_1x16) return (size_t)-1;
+    switch (op) {
+    case FP8BS_OP_QUANTIZE:
+    case FP8BS_OP_QUANTIZE_TRANSPOSED:
+        return needs_partials(gran, flags) ? kWorkspaceBytes : 0;
+    case FP8BS_OP_DEQUANTIZE:
+    case FP8BS_OP_SWIGLU_QUANTIZE:
+        return 0;
+    case FP8BS_OP_BLOCK_GEMM:
+    case FP8BS_OP_GROUPED_GEMM:
+    case FP8BS_OP_QUANTIZE_GATHERED:
+    case FP8BS_OP_GATHER_ROWS:
+        return kWorkspaceBytes;
+    default:
+        return (size_t)-1;
+    }
+}
 
 int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream) {
     if (workspace == nullptr) return FP8BS_EINVAL;
@@ -380,10 +449,11 @@ const char* fp8bs_status_string(int status) {
     case FP8BS_ETIMEOUT: return "a bounded device wait timed out";
     case FP8BS_EWORKSPACE: return "workspace missing or too small";
     case FP8BS_EINDEX: return "a token index was out of range (its row was zeroed)";
+    case FP8BS_EOFFSETS: return "expert offsets out of range or decreasing (clamped; malformed experts skipped)";
     default: return "unknown status";
     }
 }
 
-int fp8bs_version(void) { return 100; }
+int fp8bs_version(void) { return 101; }
 
 }  // extern "C"

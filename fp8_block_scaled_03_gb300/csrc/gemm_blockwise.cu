@@ -144,7 +144,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         tmem_alloc(smem_u32(&sh->tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
-    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles);  // has __syncthreads
+    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, p.status);  // has __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

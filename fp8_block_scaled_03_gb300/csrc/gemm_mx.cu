@@ -78,7 +78,7 @@ struct Params {
     const uint8_t* sa;   // row-major scale bytes [m, k / vec]
     const uint8_t* sb;   // [experts * n, k / vec]
     const float* a_ts;   // NVFP4 outer scales: [1], or [m] when a_ts_rows
-    const float* b_ts;   // [1]
+    const float* b_ts;   // [1], or [experts] for a grouped GEMM
     int a_ts_rows;
     __nv_bfloat16* d;
     int* status;
@@ -359,7 +359,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         tmem_alloc(smem_u32(&sh->tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
-    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles);
+    const int64_t total = sched_setup<BM>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, p.status);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -561,16 +561,18 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // ------------------------------------------------------------ epilogue (8 warps)
         const int q = warp & 3, h = (warp - 4) >> 2;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        float g = 1.0f, gb = 1.0f;
-        if (KIND == kNv) {
-            gb = __ldg(p.b_ts);
-            if (!p.a_ts_rows) g = __ldg(p.a_ts) * gb;
-        }
+        // NVFP4: D = acc * S_g(A) * S_g(B), with S_g(A) per tensor or per row and
+        // S_g(B) per expert (one value for a dense GEMM)
+        float g = 1.0f;
         uint32_t tcount = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
             const TileInfo ti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
-            if (KIND == kNv && p.a_ts_rows) g = (row < ti.row_end) ? __ldg(p.a_ts + row) * gb : 0.0f;
+            if (KIND == kNv) {
+                const float gb = __ldg(p.b_ts + ti.expert);
+                if (p.a_ts_rows) g = (row < ti.row_end) ? __ldg(p.a_ts + row) * gb : 0.0f;
+                else g = __ldg(p.a_ts) * gb;
+            }
             const bool got = mbar_wait(smem_u32(&sh->tfull), tcount & 1, abort, p.status);
             if (!__all_sync(0xFFFFFFFFu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
             tc_fence_after();

@@ -76,4 +76,7 @@ struct GemmJob {
 int launch_gemm_blockwise(const GemmJob& j, cudaStream_t s);
 int launch_gemm_mx(const GemmJob& j, cudaStream_t s);
 
+// ---- tensor-core throughput loop (peak.cu)
+int launch_mma_peak(int kind, int ctas, int iters, int n, int pattern, float* out, int* status, cudaStream_t s);
+
 }  // namespace fp8bs

@@ -219,11 +219,23 @@ __device__ __forceinline__ uint64_t exp_seq2(float x0, float x1) {
     return pair_f32(e0, e1);
 }
 
+// Round a float64 value once to nearest-even BF16 (bits).  The value is
+// scaled by a power of two so that its BF16 quantum becomes 1 (2^-133 below
+// the normal range), rounded to an integer, and scaled back: every step but
+// the rounding is exact.
+__device__ __forceinline__ uint32_t bf16_bits_rne_f64(double v) {
+    int e = 0;
+    (void)frexp(v, &e);
+    const int qe = max(e - 8, -133);
+    const float f = (float)ldexp(rint(ldexp(v, -qe)), qe);   // a BF16 value, or +-inf past the largest
+    return __float_as_uint(f) >> 16;
+}
+
 // Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up; the
-// exponential, the sum and the product on element pairs.
-__device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
-    float g[8], u[8], y[8];
-    unpack8(gv, g);
+// exponential, the sum and the product on element pairs, in float32 (a few
+// float32 ulps from the exact value before the BF16 rounding).
+__device__ __forceinline__ uint4 swiglu8_f32(const float* g, const uint4& uv) {
+    float u[8], y[8];
     unpack8(uv, u);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
@@ -241,9 +253,46 @@ __device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
     return o;
 }
 
+// The eight outputs when some gate is below -80: the float32 form for the
+// others, the float64 form for those (a separate function, so that the
+// common path keeps its registers).
+__device__ __noinline__ uint4 swiglu8_with_far_negative(uint4 gv, uint4 uv) {
+    float g[8], u[8];
+    unpack8(gv, g);
+    unpack8(uv, u);
+    uint4 o = swiglu8_f32(g, uv);
+    uint32_t* ow = &o.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (g[i] < -80.0f) {
+            const uint32_t b = bf16_bits_rne_f64((double)g[i] * exp((double)g[i]) * (double)u[i]);
+            ow[i >> 1] = (i & 1) ? ((ow[i >> 1] & 0xFFFFu) | (b << 16)) : ((ow[i >> 1] & 0xFFFF0000u) | b);
+        }
+    }
+    return o;
+}
+
+// SwiGLU of eight elements.  Gates below -80 never occur in activations of
+// ordinary size; for them e^-g is at or beyond the float32 range (it
+// overflows above 88.7), while y = silu(g) * up = g e^g up / (1 + e^g) can
+// still be a small normal or subnormal BF16 number.  1 + e^g equals 1 there
+// to far below float64 precision, so such an element is evaluated as
+// g e^g up in float64 and rounded once.
+__device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
+    float g[8];
+    unpack8(gv, g);
+    bool far = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) far |= g[i] < -80.0f;
+    if (far) return swiglu8_with_far_negative(gv, uv);
+    return swiglu8_f32(g, uv);
+}
+
 // ---------------------------------------------------------------- row-wise 1x128 / 1x32 / per-tensor
+// The SwiGLU source is held to 64 registers (four CTAs per SM): its rare
+// float64 path would otherwise raise the whole kernel's register count.
 template <int GRAN, int SRC = kSrcPlain>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, SRC == kSrcSwiglu ? 4 : 1)
 quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                   uint8_t* __restrict__ q, void* __restrict__ sout,
                   const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given,

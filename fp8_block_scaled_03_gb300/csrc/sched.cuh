@@ -8,6 +8,14 @@
 // tile t is then found by a binary search over the prefix, and its
 // expert's row range read from the offsets (L1/L2).  The host never reads
 // the offsets.
+//
+// Offsets are checked on the device: expert e's rows are taken as
+// [lo_e, hi_e) with lo_e = offsets[e] clamped to [0, m] and hi_e =
+// offsets[e+1] clamped to [lo_e, m], so no tile ever addresses a row of A, D
+// or their scales outside [0, m), whatever the offsets hold.  Offsets that
+// break the contract (offsets[0] == 0, non-decreasing, offsets[E] == m) set
+// the sticky status FP8BS_EOFFSETS; the rows of the well-formed experts are
+// still computed.
 #pragma once
 
 #include <cstdint>
@@ -15,6 +23,14 @@
 namespace fp8bs {
 
 constexpr int kMaxExperts = 1024;
+constexpr int kStatusOffsets = -8;   // FP8BS_EOFFSETS
+
+// Row range of expert e, clamped as described above.
+__device__ __forceinline__ void expert_rows(const int64_t* __restrict__ offsets, int e, int64_t m, int64_t& lo,
+                                            int64_t& hi) {
+    lo = min(max(__ldg(offsets + e), (int64_t)0), m);
+    hi = min(max(__ldg(offsets + e + 1), lo), m);
+}
 
 struct TileInfo {
     int64_t row0;     // first row of A / D
@@ -31,25 +47,37 @@ struct SchedShared {
 // total number of tiles.
 template <int BM>
 __device__ __forceinline__ int64_t sched_setup(SchedShared* sh, const int64_t* __restrict__ offsets, int experts,
-                                               int64_t m, int64_t n_tiles) {
+                                               int64_t m, int64_t n_tiles, int* status) {
     if (experts == 0) return ((m + BM - 1) / BM) * n_tiles;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         const int per = (experts + 31) / 32;
-        const int lo = min(experts, lane * per), hi = min(experts, lo + per);
+        const int lo_e = min(experts, lane * per), hi_e = min(experts, lo_e + per);
         int64_t local = 0;
-        for (int e = lo; e < hi; ++e) local += ((__ldg(offsets + e + 1) - __ldg(offsets + e) + BM - 1) / BM) * n_tiles;
+        bool bad = false;
+        for (int e = lo_e; e < hi_e; ++e) {
+            int64_t lo, hi;
+            expert_rows(offsets, e, m, lo, hi);
+            bad |= lo != __ldg(offsets + e) || hi != __ldg(offsets + e + 1);
+            local += ((hi - lo + BM - 1) / BM) * n_tiles;
+        }
+        if (lane == 0) bad |= __ldg(offsets) != 0;
+        if (lane == 31) bad |= __ldg(offsets + experts) != m;
         int64_t incl = local;
         for (int o = 1; o < 32; o <<= 1) {
             const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
             if (lane >= o) incl += v;
         }
         int64_t run = incl - local;
-        for (int e = lo; e < hi; ++e) {
+        for (int e = lo_e; e < hi_e; ++e) {
             sh->prefix[e] = run;
-            run += ((__ldg(offsets + e + 1) - __ldg(offsets + e) + BM - 1) / BM) * n_tiles;
+            int64_t lo, hi;
+            expert_rows(offsets, e, m, lo, hi);
+            run += ((hi - lo + BM - 1) / BM) * n_tiles;
         }
         if (lane == 31) sh->prefix[experts] = incl;
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && blockIdx.x == 0 && status != nullptr)
+            atomicExch(status, kStatusOffsets);
     }
     __syncthreads();
     return sh->prefix[experts];
@@ -91,8 +119,10 @@ __device__ __forceinline__ TileInfo sched_tile(const SchedShared* sh, const int6
     while (lo + 1 < experts && sh->prefix[lo + 1] <= t) ++lo;
     const int64_t local = t - sh->prefix[lo];
     const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
-    ti.row0 = __ldg(offsets + lo) + mt * BM;
-    ti.row_end = __ldg(offsets + lo + 1);
+    int64_t r_lo, r_hi;
+    expert_rows(offsets, lo, m, r_lo, r_hi);
+    ti.row0 = r_lo + mt * BM;
+    ti.row_end = r_hi;
     ti.n0 = nt * BN;
     ti.expert = lo;
     return ti;

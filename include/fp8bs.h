@@ -36,8 +36,8 @@
  *   - `workspace` is a caller-owned device buffer of at least
  *     FP8BS_WORKSPACE_BYTES bytes, zero-filled once by the caller before its
  *     first use.  Its first 4 bytes are a sticky device status word that
- *     kernels set (never clear) when a bounded wait gives up or a gathered
- *     token index is out of range; read it with
+ *     kernels set (never clear) when a bounded wait gives up, a gathered
+ *     token index is out of range or expert offsets are malformed; read it with
  *     fp8bs_read_status and clear it with fp8bs_clear_status.  The rest is
  *     scratch for the per-tensor / NVFP4 amax reduction.  Calls that share a
  *     workspace must be ordered on the GPU (same stream or events).
@@ -63,7 +63,8 @@ typedef enum {
     FP8BS_ECUDA = -4,         /* a CUDA runtime call or launch failed */
     FP8BS_ETIMEOUT = -5,      /* (status word) a bounded device wait gave up */
     FP8BS_EWORKSPACE = -6,    /* workspace NULL or smaller than required */
-    FP8BS_EINDEX = -7         /* (status word) a gathered token index was out of range */
+    FP8BS_EINDEX = -7,        /* (status word) a gathered token index was out of range */
+    FP8BS_EOFFSETS = -8       /* (status word) grouped-GEMM expert offsets broke their contract */
 } fp8bs_status;
 
 typedef enum {
@@ -242,13 +243,16 @@ int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, i
  *   h       BF16 [rows, 2 * inter] = [gate | up] (gate in columns 0 ..
  *           inter-1, up in inter .. 2*inter-1), pitch ld_h >= 2 * inter,
  *           ld_h % 8 == 0, 16-byte aligned; inter % 8 == 0
- *   y[r,c]  = BF16_RNE(silu(g) * u), g = h[r,c], u = h[r,inter+c],
- *           silu(g) = g / (1 + e^-g), all in IEEE float32 without fused
- *           multiply-add; e^t is evaluated by one fixed sequence: n =
- *           rint(t * RN(log2 e)), r = (t - n * L_hi) - n * L_lo with ln 2 =
- *           L_hi + L_lo (L_hi = 0x1.62e4p-1), Taylor series of e^r to r^7 by
- *           Horner's rule, times 2^(n-1), times 2; +inf for t > 89, 0 for
- *           t < -87 (within 2 float32 ulps of e^t)
+ *   y[r,c]  = BF16(silu(g) * u), g = h[r,c], u = h[r,inter+c],
+ *           silu(g) = g / (1 + e^-g): the exact value rounded once to
+ *           nearest-even BF16, except where the exact value lies within 8
+ *           float32 ulps (or 2^-146) of a BF16 rounding boundary, where
+ *           either neighbouring BF16 value may result.  (The kernel
+ *           evaluates y in float32 without fused multiply-add: e^t by
+ *           Cody-Waite reduction with ln 2 split in two and the Taylor
+ *           series of e^r to r^7, within a few float32 ulps; gates below -80,
+ *           where e^-g leaves the float32 range, in float64.)  y must be
+ *           finite.
  *   gran    TOKEN_1x128, MXFP8_1x32 or TOKEN_1x128_POW2 (other valid
  *           granularities return FP8BS_EUNSUPPORTED)
  *   q, scales  as fp8_quantize of y [rows, inter] at `gran`
@@ -299,17 +303,38 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
  *   D[r, j] = sum_k deq(A)[r, k] * deq(B[e])[j, k]   for offsets[e] <= r < offsets[e+1]
  * ("Low Precision RL", "3. Unified MXFP8 (Blackwell)": the MoE GEMM backend
  * chosen separately from the dense one).  offsets: DEVICE int64 [experts+1],
- * non-decreasing, offsets[0] == 0, offsets[experts] == total_rows (not
- * checked on the host; the host never reads it).  Experts with no rows
- * cost nothing.  gran: MXFP8_1x32 (k % 128 == 0), TOKEN_1x128 for A with
- * BLOCK_128x128 for B (k % 128 == 0, FP32 scales), or TOKEN_1x128_POW2 for A
- * with BLOCK_128x128_POW2 for B (k % 128 == 0).  a: [total_rows, k],
- * a_scales as fp8_quantize for [total_rows, k]; b: [experts, n, k] codes,
- * b_scales: per-expert scale grids stacked along the expert axis.
- * D: BF16 [total_rows, n].  n % 8 == 0.  workspace required.
+ * non-decreasing, offsets[0] == 0, offsets[experts] == total_rows.  The host
+ * never reads it; the kernel checks it: expert e's rows are taken as
+ * [lo, hi) with lo = offsets[e] clamped to [0, total_rows] and hi =
+ * offsets[e+1] clamped to [lo, total_rows], so no offsets can make the GEMM
+ * read or write outside A, D or their scales, and offsets that break the
+ * contract set the status word to FP8BS_EOFFSETS (the well-formed experts'
+ * rows are still computed; D rows no expert covers are not written).
+ * Experts with no rows cost nothing.
+ *
+ *   gran                 A                      B[e]                 k
+ *   MXFP8_1x32           MXFP8                  MXFP8                % 128
+ *   TOKEN_1x128          1x128 FP32 scales      128x128 FP32 scales  % 128
+ *   TOKEN_1x128_POW2     1x128 power of two     128x128 power of two % 128
+ *   NVFP4_1x16           NVFP4, S_g per tensor  NVFP4                % 256
+ *   NVFP4_ROW_1x16       NVFP4, S_g per row     NVFP4                % 256
+ * ("Low Precision RL", table "Choose a precision": the NVFP4 recipe on the
+ * Qwen3-30B-A3B MoE; "4. NVFP4 (Blackwell)": per-token activation scales,
+ * gate and up sharing one outer weight scale.)  a: [total_rows, k] codes
+ * (NVFP4: packed [total_rows, k/2]), a_scales as fp8_quantize for
+ * [total_rows, k]; b: [experts, n, k] codes (NVFP4: [experts, n, k/2]),
+ * b_scales: the per-expert scale grids stacked along the expert axis.
+ * a_tensor_scale: NVFP4 only, DEVICE float32[1] (NVFP4_1x16) or
+ * float32[total_rows] (NVFP4_ROW_1x16); b_tensor_scale: NVFP4 only, DEVICE
+ * float32[experts], the outer scale S_g of each expert's weight; row r of
+ * expert e is multiplied by a_tensor_scale[0 or r] * b_tensor_scale[e].  Both
+ * are ignored (may be NULL) for the other granularities.  NVFP4 block scales
+ * 16-byte aligned.  D: BF16 [total_rows, n].  n % 8 == 0.  workspace
+ * required.
  */
 int fp8_grouped_gemm(const void* a, const void* a_scales,
                      const void* b, const void* b_scales,
+                     const float* a_tensor_scale, const float* b_tensor_scale,
                      const int64_t* offsets, int experts, int64_t total_rows,
                      int64_t n, int64_t k, int gran, void* d,
                      void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
@@ -329,6 +354,20 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
 int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, const void* b_scales,
                             int64_t m, int64_t n, int64_t k, void* d, uint64_t wait_limit_ns,
                             void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
+
+/*
+ * fp8bs_test_stalled_gemm_blockwise -- as fp8bs_test_stalled_gemm for the
+ * FP32-scale blockwise GEMM (fp8_block_gemm with a_gran, b_gran in
+ * {PER_TENSOR, TOKEN_1x128, BLOCK_128x128}; same arguments and
+ * requirements, k % 128 == 0).  Its epilogue warps, which promote every
+ * K block out of two TMEM buffers, and its scale-loader warp must all give
+ * up on the abort, and the CTA must still free its tensor memory.  No
+ * counterpart on the pages.  The contents of d are unspecified afterwards.
+ */
+int fp8bs_test_stalled_gemm_blockwise(const void* a, const void* a_scales, int a_gran, const void* b,
+                                      const void* b_scales, int b_gran, int64_t m, int64_t n, int64_t k, void* d,
+                                      uint64_t wait_limit_ns, void* workspace, size_t workspace_bytes,
+                                      fp8bs_stream_t stream);
 
 /*
  * fp8bs_test_stalled_gemm_nvfp4 -- as fp8bs_test_stalled_gemm for the
@@ -367,6 +406,32 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
 int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream);
 
 /*
+ * fp8bs_mma_peak -- dense tensor-core throughput loop, to measure the FP8
+ * and FP4 MMA rates that the GEMM rooflines divide by.  The pages compare
+ * FP8 with BF16 tensor throughput ("Unified FP8 ...", section "Tensor
+ * Cores": FP8 at twice the BF16 rate on H100); this measures the rate on
+ * the GPU at hand instead of assuming a ratio.
+ *
+ * One CTA per SM; each keeps its operands in shared memory (no memory
+ * traffic) and one thread issues `iters` K blocks of four tcgen05.mma
+ * instructions (M = 128 rows, N = n columns) into a TMEM accumulator:
+ *   kind 0  E4M3 x E4M3, FP32 accumulate (kind::f8f6f4), K = 32 per instruction
+ *   kind 1  MXFP8: E4M3 with UE8M0 scales per 32 (block_scale, scale_vec::1X), K = 32
+ *   kind 2  NVFP4: E2M1 with E4M3 scales per 16 (block_scale, scale_vec::4X), K = 64
+ * FLOPs per call = SMs * iters * 4 * 2 * 128 * n * K; the caller times the
+ * call (CUDA events on `stream`).  n: 64 (kind 0 only), 128 or 256;
+ * iters: 1 .. 2^24.
+ * pattern 0: pseudo-random finite operands; pattern 1: every operand and
+ * scale 1.0, so every accumulator element ends at iters * 4 * K.
+ * out: NULL, or DEVICE float32[128] receiving column 0 of the first CTA's
+ * accumulator (rows 0..127).  workspace: required (status word; the final
+ * wait is bounded like the GEMMs').  No counterpart on the pages beyond the
+ * comparison above.
+ */
+int fp8bs_mma_peak(int kind, int n, int iters, int pattern, float* out, void* workspace, size_t workspace_bytes,
+                   fp8bs_stream_t stream);
+
+/*
  * fp8_quantize_per_tensor_noalloc -- fp8_quantize(gran = PER_TENSOR) for
  * callers that cannot allocate device memory.  The pages have no
  * counterpart: this is an interface variant, not a different computation.
@@ -402,9 +467,32 @@ int fp8_quantize_per_tensor_noalloc(const void* x, int64_t rows, int64_t cols, i
 /* Bytes of workspace every entry point accepts (FP8BS_WORKSPACE_BYTES). */
 size_t fp8bs_workspace_size(void);
 
+/* Operations, for fp8bs_workspace_size_for. */
+typedef enum {
+    FP8BS_OP_QUANTIZE = 0,
+    FP8BS_OP_QUANTIZE_TRANSPOSED = 1,
+    FP8BS_OP_DEQUANTIZE = 2,
+    FP8BS_OP_BLOCK_GEMM = 3,
+    FP8BS_OP_GROUPED_GEMM = 4,
+    FP8BS_OP_QUANTIZE_GATHERED = 5,
+    FP8BS_OP_GATHER_ROWS = 6,
+    FP8BS_OP_SWIGLU_QUANTIZE = 7
+} fp8bs_op;
+
+/* Bytes of workspace one call of `op` on a [rows, cols] operand at
+ * granularity `gran` (and `flags`, as passed to the quantisers) requires:
+ * 0 when the call takes none (it may then be NULL), else
+ * FP8BS_WORKSPACE_BYTES.  The size does not grow with the operand: the
+ * status word is 4 bytes, and the tensor-amax reduction of PER_TENSOR and
+ * NVFP4_1x16 quantisation uses at most 4032 partial maxima whatever the
+ * size.  Returns (size_t)-1 for an unknown op or granularity or negative
+ * sizes. */
+size_t fp8bs_workspace_size_for(int op, int64_t rows, int64_t cols, int gran, unsigned flags);
+
 /* Synchronises `stream`, then returns the sticky device status word of
- * `workspace` (FP8BS_OK, FP8BS_ETIMEOUT if a bounded wait gave up, or
- * FP8BS_EINDEX if fp8_quantize_gathered met an index out of range), or
+ * `workspace` (FP8BS_OK, FP8BS_ETIMEOUT if a bounded wait gave up,
+ * FP8BS_EINDEX if a gathered token index was out of range, or
+ * FP8BS_EOFFSETS if grouped-GEMM offsets broke their contract), or
  * FP8BS_ECUDA if the copy failed. */
 int fp8bs_read_status(const void* workspace, fp8bs_stream_t stream);
 

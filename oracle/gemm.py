@@ -116,8 +116,3 @@ def grouped_gemm(a64: np.ndarray, b64_per_expert, offsets) -> np.ndarray:
         if hi > lo:
             out[lo:hi] = gemm_bf16(a64[lo:hi], b64_per_expert[e])
     return out
-
-
-def gemm_rows(a64: np.ndarray, b64: np.ndarray, rows) -> np.ndarray:
-    """Reference output for a subset of rows only (sampled parity at full size)."""
-    return gemm_bf16(np.asarray(a64)[np.asarray(rows)], b64)

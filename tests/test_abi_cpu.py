@@ -33,8 +33,15 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_sizes(lib):
     assert lib.fp8bs_workspace_size() == 16384
-    assert lib.fp8bs_version() == 100
-    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+    ws = lib.fp8bs_workspace_size_for
+    big = 1 << 40
+    assert ws(0, big, 8192, 0, 0) == 16384 and ws(0, 4, 128, 4, 0) == 16384     # per-tensor / NVFP4 amax partials
+    assert ws(0, 4, 128, 0, 1) == 0 and ws(0, 4, 128, 1, 0) == 0               # given scale / 1x128: none
+    assert ws(2, 4, 128, 1, 0) == 0 and ws(7, 4, 128, 3, 0) == 0               # dequantise, SwiGLU: none
+    assert all(ws(op, 4, 128, 3, 0) == 16384 for op in (3, 4, 5, 6))          # GEMMs, gathers: status word
+    assert ws(8, 4, 128, 1, 0) == 2 ** 64 - 1 and ws(0, -1, 128, 1, 0) == 2 ** 64 - 1
+    assert lib.fp8bs_version() == 101
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert fp.status_string(code) != "unknown status"
     assert fp.status_string(7) == "unknown status"
 
@@ -79,11 +86,17 @@ def test_gemm_rejects_bad_arguments(lib):
 
 def test_grouped_gemm_rejects_bad_arguments(lib):
     g = lib.fp8_grouped_gemm
-    assert g(FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 256, 3, FAKE, FAKE, 16384, None) == -1   # offsets
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, 128, 256, 3, FAKE, FAKE, 16384, None) == -1   # experts
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 200, 3, FAKE, FAKE, 16384, None) == -1   # k
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 256, 3, FAKE, None, 0, None) == -6
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 0, 128, 256, 3, FAKE, FAKE, 16384, None) == 0     # empty: no-op
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, None, 8, 64, 128, 256, 3, FAKE, FAKE, 16384, None) == -1  # offsets
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 0, 64, 128, 256, 3, FAKE, FAKE, 16384, None) == -1  # experts
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 64, 128, 200, 3, FAKE, FAKE, 16384, None) == -1  # k
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 64, 128, 256, 3, FAKE, None, 0, None) == -6
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 0, 128, 256, 3, FAKE, FAKE, 16384, None) == 0  # empty
+    # NVFP4: both tensor scales required, k % 256, 16-byte block scales
+    assert g(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 8, 64, 128, 256, 4, FAKE, FAKE, 16384, None) == -1
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 384, 7, FAKE, FAKE, 16384, None) == -1
+    assert g(FAKE, ctypes.c_void_p(0x10004), FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 256, 4, FAKE, FAKE, 16384,
+             None) == -2
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 64, 128, 256, 9, FAKE, FAKE, 16384, None) == -1  # gran
 
 
 ODD4 = ctypes.c_void_p(0x10002)        # not 4-byte aligned
