@@ -44,7 +44,7 @@ METRIC = "block-scaled FP8 GEMM TFLOPS and quantize GB/s at 1 GB300 (% of roofli
 # on `bench.py --no-extras`), together with the SHA-256 (first 16 hex digits)
 # of the kernel source it was taken on: once that source changes the figure
 # no longer describes the kernel and the bench reports null.
-GEMM_TRAFFIC = {"bytes": 138438400, "source_sha16": None}
+GEMM_TRAFFIC = {"bytes": 138411093, "source_sha16": "5a38cf66990a2a72"}
 L2_FLUSH_BYTES = 512 << 20
 TIMED_CALLS = 50                                # sub-benchmarks: median of this many calls
 
@@ -58,7 +58,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the sub-benchmarks")
     ap.add_argument("--kernel", default=None,
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
-                             "quant_nvfp4_row_4over6", "dequant_1x128", "moe_gate_up", "moe_gather_quant",
+                             "quant_per_tensor", "quant_nvfp4", "quant_nvfp4_row_4over6", "dequant_1x128",
+                             "moe_gate_up", "moe_gather_quant",
                              "moe_swiglu_quant", "moe_quant_then_gather", "moe_layer", "nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
@@ -388,6 +389,51 @@ def moe_bench(torch, fp, dev, pk, flush):
             "peak_tflops": round(peak, 1), "peak_note": "measured bf16 burst x nominal fp8/bf16 ratio 2"}
 
 
+def moe_nvfp4_bench(torch, fp, dev, pk, flush):
+    """The MoE expert GEMMs in NVFP4 (Qwen3-30B-A3B shapes, the NVFP4 recipe's
+    MoE): routed activations with per-token outer scales, each expert's
+    weight with its own outer scale (gate and up sharing one)."""
+    import synth
+    tokens, experts, hidden, inter = 16384, 128, 2048, 768
+    _, offsets = synth.moe_routing(tokens, experts, 8, seed=0)
+    rows = int(offsets[-1])
+    act, wt = device_inputs(torch, 400, dev)
+    ws = fp.workspace(dev)
+    off = torch.from_numpy(offsets).to(dev)
+
+    def expert_weights(n, k):
+        w = wt((experts, n, k))
+        q = torch.empty((experts, n, k // 2), dtype=torch.uint8, device=dev)
+        s = torch.empty((experts, n, k // 16), dtype=torch.uint8, device=dev)
+        t = torch.empty((experts,), dtype=torch.float32, device=dev)
+        for e in range(experts):
+            fp.fp8_quantize(w[e], "nvfp4", q=q[e], scales=s[e], tensor_scale=t[e:e + 1], ws=ws)
+        return q, s, t
+    qgu, sgu, tgu = expert_weights(2 * inter, hidden)
+    qdn, sdn, tdn = expert_weights(hidden, inter)
+    qa, sa, ta = fp.fp8_quantize(act((rows, hidden), 0.001, 100.0), "nvfp4_row", ws=ws)
+    qh, sh_, th = fp.fp8_quantize(act((rows, inter), 0.0, 1.0), "nvfp4_row", ws=ws)
+    d_gu = torch.empty((rows, 2 * inter), dtype=torch.bfloat16, device=dev)
+    d_dn = torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev)
+    run_gu = lambda: fp.fp8_grouped_gemm(qa, sa, qgu, sgu, off, "nvfp4_row", a_tensor_scale=ta,  # noqa: E731
+                                         b_tensor_scale=tgu, k=hidden, out=d_gu, ws=ws)
+    run_dn = lambda: fp.fp8_grouped_gemm(qh, sh_, qdn, sdn, off, "nvfp4_row", a_tensor_scale=th,  # noqa: E731
+                                         b_tensor_scale=tdn, k=inter, out=d_dn, ws=ws)
+    ms_gu, _ = time_fn(torch, run_gu, flush=flush)
+    ms_dn, _ = time_fn(torch, run_dn, flush=flush)
+    f_gu, f_dn = 2 * rows * 2 * inter * hidden, 2 * rows * hidden * inter
+    peak = pk["bf16_tflops"] * FP4_PER_BF16
+    lp = pk.get("loop", {}).get("nvfp4")
+    out = {}
+    for name, f, ms in (("gate_up", f_gu, ms_gu), ("down", f_dn, ms_dn)):
+        t = f / ms / 1e9
+        out[name] = {"tflops": round(t, 1), "ms": round(ms, 3), "frac": round(t / peak, 3),
+                     "frac_of_nvfp4_loop_peak": round(t / lp, 3) if lp else None}
+    out["note"] = "A per-token NVFP4 (nvfp4_row), B NVFP4 with one outer scale per expert"
+    out["peak_note"] = "measured bf16 burst x nominal fp4/bf16 ratio 6"
+    return out
+
+
 def nvfp4_bench(torch, fp, dev, pk, flush):
     """NVFP4 linear, Qwen2.5-32B MLP shape X [16384,5120] x W [27648,5120]^T."""
     m, n, k = 16384, 27648, 5120
@@ -596,6 +642,7 @@ def main():
         line["quantize"] = quantize_sweep(torch, fp, dev, pk, flush)
         line["moe_mxfp8"] = moe_bench(torch, fp, dev, pk, flush)
         line["nvfp4"] = nvfp4_bench(torch, fp, dev, pk, flush)
+        line["moe_nvfp4"] = moe_nvfp4_bench(torch, fp, dev, pk, flush)
         line["e2e"] = e2e_bench(torch, fp, dev, step)
         line["cpu_baseline"] = cpu_oracle_sample()
     if rank == 0:
@@ -627,6 +674,12 @@ def single_kernel(args, torch, fp, dev):
             q, s_, t_ = fp.fp8_quantize(x, "nvfp4_row", flags=fos, ws=ws)
             fn = lambda: fp.fp8_quantize(x, "nvfp4_row", q=q, scales=s_, tensor_scale=t_, flags=fos,  # noqa: E731
                                          ws=ws)
+        elif name == "quant_nvfp4":
+            q, s_, t_ = fp.fp8_quantize(x, "nvfp4", ws=ws)
+            fn = lambda: fp.fp8_quantize(x, "nvfp4", q=q, scales=s_, tensor_scale=t_, ws=ws)  # noqa: E731
+        elif name == "quant_per_tensor":
+            q, s_, _ = fp.fp8_quantize(x, "per_tensor", ws=ws)
+            fn = lambda: fp.fp8_quantize(x, "per_tensor", q=q, scales=s_, ws=ws)  # noqa: E731
         elif name == "dequant_1x128":
             q, s_, _ = fp.fp8_quantize(x, "1x128", ws=ws)
             xd = torch.empty_like(x)
