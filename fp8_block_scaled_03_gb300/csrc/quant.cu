@@ -183,12 +183,13 @@ __device__ __forceinline__ void unpair(uint64_t v, float& lo, float& hi) {
 }
 __device__ __forceinline__ uint64_t splat2(float c) { return pair_f32(c, c); }
 
-// e^x of two elements in float32 by one fixed sequence (each operation one
-// IEEE rounding, no fused multiply-add; two elements per instruction where
-// the operation allows): Cody and Waite's reduction x = n ln2 + r ("Software
+// e^x of two elements in float32, two elements per instruction where the
+// operation allows: Cody and Waite's reduction x = n ln2 + r ("Software
 // Manual for the Elementary Functions", 1980) with ln 2 split into a 16-bit
 // head and a tail, the Taylor series of e^r to r^7 in Horner form, and the
-// scaling by 2^(n-1) * 2.  +inf above 89, 0 below -87 (where 1 + e^x is 1 in
+// scaling by 2^(n-1) * 2.  The compiler may fuse a pair multiplication with
+// the pair addition that follows it (it does so for mul/sub.rn.f32x2), which
+// only removes a rounding; the SwiGLU contract allows for a few float32 ulps.  +inf above 89, 0 below -87 (where 1 + e^x is 1 in
 // float32 already).  Within 2 float32 ulps of e^x.  The sequence runs on x
 // clamped to [-87, 89] (which keeps n in [-126, 128]); the out-of-range
 // results are selected at the end, with no branch per element.
@@ -289,10 +290,14 @@ __device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
 }
 
 // ---------------------------------------------------------------- row-wise 1x128 / 1x32 / per-tensor
-// The SwiGLU source is held to 64 registers (four CTAs per SM): its rare
-// float64 path would otherwise raise the whole kernel's register count.
+// Plain and SwiGLU rows are held to 64 registers, four CTAs (32 warps) per
+// SM: the 1x128 form measured 26.6 -> 23.5 us on [8192, 4096] against its
+// unconstrained 66 registers (three CTAs), with the same codes; the MXFP8 and
+// per-tensor forms did not move, and five or more CTAs per SM were slower.
+// The SwiGLU source's rare float64 path would otherwise raise its count too.
+// The gathered source keeps its own count (capped, its MXFP8 form spills).
 template <int GRAN, int SRC = kSrcPlain>
-__global__ void __launch_bounds__(kThreads, SRC == kSrcSwiglu ? 4 : 1)
+__global__ void __launch_bounds__(kThreads, SRC == kSrcGather ? 1 : 4)
 quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                   uint8_t* __restrict__ q, void* __restrict__ sout,
                   const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given,
@@ -413,6 +418,10 @@ __device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s, boo
 }
 
 // sum_i (x_i - E2M1(q_i) * S_b)^2 over this lane's 8 elements, in order.
+// Scalar on purpose: written with mul.rn.f32x2 and sub.rn.f32x2 on element
+// pairs, the difference came out as one fused multiply-add (x - e S rounded
+// once), which changed 2627 code bytes of a [8192, 4096] four-over-six
+// quantisation; the scalar intrinsics keep the product rounded on its own.
 __device__ __forceinline__ float half_sq_err(const float* f, uint32_t packed, float big_s) {
     float acc = 0.0f;
 #pragma unroll
