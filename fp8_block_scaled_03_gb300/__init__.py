@@ -45,7 +45,8 @@ EXPORTS = ("fp8_quantize", "fp8_quantize_transposed", "fp8_dequantize", "fp8_blo
            "fp8bs_workspace_size", "fp8bs_workspace_size_for", "fp8bs_read_status", "fp8bs_clear_status",
            "fp8bs_status_string", "fp8bs_version", "fp8bs_test_stalled_gemm", "fp8bs_test_stalled_gemm_nvfp4",
            "fp8bs_test_stalled_gemm_blockwise",
-           "fp8bs_test_quotient_sweep", "fp8bs_mma_peak")
+           "fp8bs_test_quotient_sweep", "fp8bs_mma_peak", "fp8bs_test_noalloc_scratch",
+           "fp8bs_test_encoder_breakpoints")
 
 _lib = None
 
@@ -82,6 +83,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8bs_test_quotient_sweep.argtypes = [P, I, P]
     lib.fp8bs_test_quotient_sweep.restype = I
     lib.fp8bs_mma_peak.argtypes = [I, I, I, I, P, P, SZ, P]
+    lib.fp8bs_test_encoder_breakpoints.argtypes = [P, P]
+    lib.fp8bs_test_encoder_breakpoints.restype = I
+    lib.fp8bs_test_noalloc_scratch.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P)]
+    lib.fp8bs_test_noalloc_scratch.restype = I
     lib.fp8bs_mma_peak.restype = I
     lib.fp8bs_workspace_size.restype = SZ
     lib.fp8bs_workspace_size.argtypes = []
@@ -402,13 +407,24 @@ def test_stalled_gemm_nvfp4(a, a_scales, b, b_scales, a_tensor_scale, b_tensor_s
                                                         _stream(stream))
 
 
-def test_quotient_sweep(nvfp4: bool = False, stream=None):
-    """Run fp8bs_test_quotient_sweep; returns (pairs, code mismatches, fast-path scales)."""
+def test_quotient_sweep(nvfp4=False, stream=None):
+    """Run fp8bs_test_quotient_sweep (mode 0: FP32-scale E4M3 casts, 1 or
+    True: NVFP4 element casts, 2: NVFP4 block scale codes); returns (pairs,
+    code mismatches, fast-path scales)."""
     counts = torch.zeros(3, dtype=torch.int64, device="cuda")
     _check("fp8bs_test_quotient_sweep",
-           load_library().fp8bs_test_quotient_sweep(_ptr(counts), int(bool(nvfp4)), _stream(stream)))
+           load_library().fp8bs_test_quotient_sweep(_ptr(counts), int(nvfp4), _stream(stream)))
     c = counts.cpu().tolist()
     return c[0], c[1], c[2]
+
+
+def test_encoder_breakpoints(stream=None):
+    """Run fp8bs_test_encoder_breakpoints; returns the 266 breakpoint bit
+    patterns as a list (E4M3 positive, E4M3 negative, E2M1 positive, E2M1
+    negative)."""
+    out = torch.zeros(266, dtype=torch.int32, device="cuda")
+    _check("fp8bs_test_encoder_breakpoints", load_library().fp8bs_test_encoder_breakpoints(_ptr(out), _stream(stream)))
+    return [v & 0xFFFFFFFF for v in out.cpu().tolist()]
 
 
 MMA_PEAK_K = {0: 32, 1: 32, 2: 64}      # K per instruction: E4M3, MXFP8, NVFP4

@@ -51,6 +51,7 @@ struct GatherJob {
 };
 int launch_gather_rows(const GatherJob& j, cudaStream_t s);
 // Exhaustive check of the FP32-scale division used by the casts (test hook).
+int launch_encoder_breakpoints(uint32_t* out, cudaStream_t st);
 int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t s);
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                        float* scale, uint32_t* partials, int nparts, cudaStream_t s);

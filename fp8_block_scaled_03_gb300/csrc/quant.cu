@@ -124,9 +124,30 @@ struct TaskCursor {
 };
 
 // ---------------------------------------------------------------- pass 1: amax partials
+// The cast pass that follows reads X again.  When X fits in L2 (the host
+// decides: `keep`), the pass's loads of X mark their lines evict-last, and
+// the cast pass then finds X in L2 instead of HBM.  Without the mark the
+// second pass over a tensor of about L2's size found little of it: the
+// lines it wants first are the ones the first pass evicted first.  For a
+// larger X, marking a share of it only crowded the cast pass's own traffic
+// out of L2, so X is then loaded plainly.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ldg_v4_policy(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 __global__ void __launch_bounds__(kThreads)
 amax_partials_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-                     uint32_t* __restrict__ partials) {
+                     uint32_t* __restrict__ partials, bool keep) {
+    const uint64_t pol = l2_policy_evict_last();
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -140,7 +161,8 @@ amax_partials_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t c = cb + j * 256 + lane * 8;
-            v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+            v[j] = (c < cols) ? (keep ? ldg_v4_policy(x + r * ldx + c, pol) : ldg_v4(x + r * ldx + c))
+                              : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) m = max(m, absmax_v4(v[j]));
@@ -402,14 +424,27 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
 // sums are then added, which is the same sum on both lanes (IEEE addition
 // commutes).  S_g is amax / (256 * 6) in that mode.
 
+// tab[c] = RN(1/S_b) for S_b = RN(E4M3value(c) * S_g), c = 0..127 (entries
+// for c = 0 and the NaN code 127 are never read), written by `n` threads
+// starting at thread `t`: the reciprocal each block would otherwise take,
+// computed once per outer scale.
+__device__ __forceinline__ void nvfp4_fill_rcp(float* tab, float s_g, int t, int n) {
+    for (int c = t; c < 128; c += n) tab[c] = __frcp_rn(__fmul_rn(e4m3_value((uint32_t)c), s_g));
+}
+
 // E2M1(x / S_b) for 8 elements.  S_b = E4M3value(s_b) * S_g: with S_g from
 // the tensor (or row) amax the quotient is the reciprocal-and-correction one
 // (div_fast, the test hoisted out of the loop); every E2M1 code on that
 // domain matches the IEEE quotient's, checked by enumeration
 // (fp8bs_test_quotient_sweep with nvfp4 = 1).  A supplied S_g divides exactly.
-__device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s, bool from_amax) {
+// r is RN(1/S_b), read from the kernel's table of the 127 possible S_b of
+// its S_g (nvfp4_fill_rcp) instead of one reciprocal per block and lane.
+__device__ __forceinline__ uint32_t e2m1_quant8(const float* f, float big_s, float r, bool from_amax) {
     if (big_s == 0.0f) return 0u;
-    const ScaleDiv d = scale_div(big_s, from_amax);
+    ScaleDiv d;
+    d.s = big_s;
+    d.fast = from_amax && big_s >= kFastDivMinScale;
+    d.r = r;
     if (d.fast) return e2m1x8_div_fast2(f, scale_div2(d));
     float t[8];
 #pragma unroll
@@ -435,22 +470,45 @@ __device__ __forceinline__ float half_sq_err(const float* f, uint32_t packed, fl
     return acc;
 }
 
+// The block scale code E4M3(RN(RN(a / 6) / S_g)) of a block amax a (a
+// BF16 value), and with four = true the four-over-six alternative
+// E4M3(RN(RN(a / 4) / S_g)).  On the fast path (S_g derived from a tensor
+// or row amax, S_g >= 2^-88) both divisions take the correction step of
+// div_fast: RN(a / 6) with r = RN(1/6), which equals the IEEE quotient for
+// every BF16 a; RN(a / 4) is the exact product a * 0.25; the division by
+// S_g with dg's reciprocal, whose E4M3 code equals that of the IEEE
+// quotient for every BF16 amax_T and every BF16 a <= amax_T, for both outer
+// divisors.  Both facts were checked by enumeration on the device
+// (fp8bs_test_quotient_sweep with mode 2).  Otherwise: IEEE division.
+constexpr float kRecip6 = 0x1.555556p-3f;   // RN(1/6)
+
+__device__ __forceinline__ float div6_fast(float a) {
+    const float y = __fmul_rn(a, kRecip6);
+    const float e = __fmaf_rn(-y, kE2M1Max, a);
+    return __fmaf_rn(e, kRecip6, y);
+}
+
+__device__ __forceinline__ uint32_t nvfp4_block_code(float amax_b, float s_g, const ScaleDiv& dg, bool four) {
+    if (dg.fast) return e4m3_byte(div_fast(four ? __fmul_rn(amax_b, 0.25f) : div6_fast(amax_b), dg));
+    return e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, four ? 4.0f : kE2M1Max), s_g));
+}
+
 // One lane's half block: packed E2M1 codes and the block's scale byte.  Every
 // lane of the warp must call this (shuffles).
 template <bool FOS>
-__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, bool from_amax, uint32_t& packed,
-                                                 uint32_t& code) {
+__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, const ScaleDiv& dg, const float* rcp,
+                                                 bool from_amax, uint32_t& packed, uint32_t& code) {
     const uint32_t m = warp_max_u32(absmax_v4(v), 2);
     const float amax_b = amax_bits_to_f32(m);
     float f[8];
     unpack8(v, f);
-    code = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, kE2M1Max), s_g));
+    code = nvfp4_block_code(amax_b, s_g, dg, false);
     const float s6 = __fmul_rn(e4m3_value(code), s_g);
-    packed = e2m1_quant8(f, s6, from_amax);
+    packed = e2m1_quant8(f, s6, rcp[code], from_amax);
     if constexpr (FOS) {
-        const uint32_t code4 = e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, 4.0f), s_g));
+        const uint32_t code4 = nvfp4_block_code(amax_b, s_g, dg, true);
         const float s4 = __fmul_rn(e4m3_value(code4), s_g);
-        const uint32_t p4 = e2m1_quant8(f, s4, from_amax);
+        const uint32_t p4 = e2m1_quant8(f, s4, rcp[code4], from_amax);
         float e6 = half_sq_err(f, packed, s6);
         float e4 = half_sq_err(f, p4, s4);
         e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, 1));
@@ -466,7 +524,8 @@ __device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, bool
 template <bool FOS>
 __device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, int64_t r, int64_t cb, int64_t cols,
                                               int64_t ldx, uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
-                                              float s_g, bool from_amax, int lane) {
+                                              float s_g, const ScaleDiv& dg, const float* rcp, bool from_amax,
+                                              int lane) {
     const int64_t nb = cols >> 4;
     uint4 v[4];
 #pragma unroll
@@ -478,7 +537,7 @@ __device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, in
     for (int j = 0; j < 4; ++j) {
         const int64_t c = cb + j * 256 + lane * 8;
         uint32_t packed, code;
-        nvfp4_half_block<FOS>(v[j], s_g, from_amax, packed, code);
+        nvfp4_half_block<FOS>(v[j], s_g, dg, rcp, from_amax, packed, code);
         if (c < cols) {
             *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
             if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
@@ -506,8 +565,12 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     const int64_t segs = ceil_div(cols, kSeg);
     const int64_t total = rows * segs;
     TaskCursor tc(gw, nw, segs);
+    const ScaleDiv dg = scale_div(s_g, !given);
+    __shared__ float rcp[128];
+    nvfp4_fill_rcp(rcp, s_g, threadIdx.x, blockDim.x);
+    __syncthreads();
     for (int64_t t = gw; t < total; t += nw, tc.advance())
-        nvfp4_segment<FOS>(x, tc.r, tc.si * kSeg, cols, ldx, q, sb, s_g, !given, lane);
+        nvfp4_segment<FOS>(x, tc.r, tc.si * kSeg, cols, ldx, q, sb, s_g, dg, rcp, !given, lane);
 }
 
 // One outer scale per row (per token): a warp owns a row, reads it once for
@@ -516,6 +579,7 @@ template <bool FOS>
 __global__ void __launch_bounds__(kThreads)
 quant_nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
                        uint8_t* __restrict__ q, uint8_t* __restrict__ sb, float* __restrict__ row_scale, bool given) {
+    __shared__ float rcp_rows[kThreads / 32][128];   // per warp: RN(1/S_b) of its row's S_g
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -539,7 +603,13 @@ quant_nvfp4_row_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t col
             s_g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, FOS ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
             if (lane == 0) row_scale[r] = s_g;
         }
-        for (int64_t cb = 0; cb < cols; cb += kSeg) nvfp4_segment<FOS>(x, r, cb, cols, ldx, q, sb, s_g, !given, lane);
+        const ScaleDiv dg = scale_div(s_g, !given);
+        float* rcp = rcp_rows[threadIdx.x >> 5];
+        __syncwarp();                       // the previous row's table is no longer read
+        nvfp4_fill_rcp(rcp, s_g, lane, 32);
+        __syncwarp();
+        for (int64_t cb = 0; cb < cols; cb += kSeg)
+            nvfp4_segment<FOS>(x, r, cb, cols, ldx, q, sb, s_g, dg, rcp, !given, lane);
     }
 }
 
@@ -1014,9 +1084,16 @@ static int rowwise_blocks(int64_t rows, int64_t cols, int cap) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
 }
 
+// Whether the amax pass keeps X in L2 for the cast pass: X up to 96 MB,
+// three quarters of GB300's 126 MB L2.
+static bool l2_keep_x(int64_t rows, int64_t ldx) {
+    return 2.0 * (double)rows * (double)ldx <= 96.0 * 1024 * 1024;
+}
+
 static int launch_amax(const QuantJob& j, cudaStream_t st, int* nparts) {
     const int n = rowwise_blocks(j.rows, j.cols, std::min(kMaxPartials, sm_count() * 4));
-    amax_partials_kernel<<<n, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.partials);
+    amax_partials_kernel<<<n, kThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.partials,
+                                                 l2_keep_x(j.rows, j.ldx));
     *nparts = n;
     return (int)cudaGetLastError();
 }
@@ -1156,8 +1233,97 @@ __global__ void __launch_bounds__(256) quotient_sweep_nvfp4_kernel(unsigned long
     if (d.fast) atomicAdd(&counts[2], 1ull);
 }
 
+// Breakpoints of the product's casts.  Both casts are monotone in the
+// magnitude of their float32 input, so for each nonzero code magnitude c
+// there is a smallest float32 magnitude whose code has magnitude >= c; a
+// binary search over the (ordered) bit patterns of the positive floats finds
+// it.  Thread t < 252: E4M3, sign t / 126, c = 1 + t % 126, through the
+// packed pair cast the quantisers use (all four bytes must agree); thread
+// 252 <= t < 266: E2M1, sign (t - 252) / 7, c = 1 + (t - 252) % 7, through
+// the eight-wide cast (all eight nibbles must agree).  out[t] receives the
+// breakpoint's bits; a disagreement between lanes, or a code of the wrong
+// sign, writes 0xFFFFFFFF instead.
+__global__ void __launch_bounds__(288) encoder_breakpoints_kernel(uint32_t* __restrict__ out) {
+    const int t = threadIdx.x;
+    if (t >= 266) return;
+    const bool fp4 = t >= 252;
+    const int u = fp4 ? t - 252 : t;
+    const int per_sign = fp4 ? 7 : 126;
+    const bool neg = u >= per_sign;
+    const uint32_t c = 1u + (uint32_t)(u % per_sign);
+    bool ok = true;
+    // magnitude of the code of (sign) * bits, checking every lane agrees
+    auto mag = [&](uint32_t bits) -> uint32_t {
+        const float x = __uint_as_float(bits | (neg ? 0x80000000u : 0u));
+        if (!fp4) {
+            const uint32_t r = e4m3x4_pairs(pair_f32(x, x), pair_f32(x, x));
+            const uint32_t b = r & 0xFFu;
+            if (r != b * 0x01010101u) ok = false;
+            if (neg && b != 0u && (b & 0x80u) == 0u) ok = false;
+            if (!neg && (b & 0x80u) != 0u) ok = false;
+            return b & 0x7Fu;
+        }
+        const float a[8] = {x, x, x, x, x, x, x, x};
+        const uint32_t r = e2m1x8(a);
+        const uint32_t b = r & 0xFu;
+        if (r != b * 0x11111111u) ok = false;
+        if (neg && b != 0u && (b & 0x8u) == 0u) ok = false;
+        if (!neg && (b & 0x8u) != 0u) ok = false;
+        return b & 0x7u;
+    };
+    uint32_t lo = 0u, hi = 0x7F7FFFFFu;          // mag(0) = 0 < c; FLT_MAX saturates to the largest code
+    if (mag(hi) < c) ok = false;
+    while (lo + 1u < hi) {                       // invariant: mag(lo) < c <= mag(hi)
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        if (mag(mid) >= c) hi = mid; else lo = mid;
+    }
+    out[t] = ok ? hi : 0xFFFFFFFFu;
+}
+
+int launch_encoder_breakpoints(uint32_t* out, cudaStream_t st) {
+    encoder_breakpoints_kernel<<<1, 288, 0, st>>>(out);
+    return (int)cudaGetLastError();
+}
+
+// NVFP4 block scale codes: every positive BF16 amax_T with S_g =
+// RN(amax_T / D) on the fast path, for D = 2688 and D = 1536, and every BF16
+// a <= amax_T: the code through nvfp4_block_code against
+// E4M3(RN(RN(a / 6) / S_g)) by IEEE division, and for D = 1536 (the
+// four-over-six divisor) also the a / 4 form.  Each thread also compares
+// div6_fast(amax_T) with RN(amax_T / 6), bit for bit, for every BF16
+// amax_T including zero and the subnormals.  One thread per amax_T.
+__global__ void __launch_bounds__(256) quotient_sweep_block_code_kernel(unsigned long long* __restrict__ counts) {
+    const uint32_t ai = blockIdx.x * blockDim.x + threadIdx.x;
+    if (ai > 0x7F7Fu) return;
+    const float amax = __uint_as_float(ai << 16);
+    unsigned long long n = 1, bad = 0, fast = 0;
+    bad += __float_as_uint(div6_fast(amax)) != __float_as_uint(__fdiv_rn(amax, kE2M1Max)) ? 1 : 0;
+    if (ai != 0) {
+        for (int v = 0; v < 2; ++v) {
+            const float s_g = __fdiv_rn(amax, v ? kNvfp4GlobalDiv4over6 : kNvfp4GlobalDiv);
+            const ScaleDiv dg = scale_div(s_g, true);
+            if (!dg.fast) continue;
+            ++fast;
+            for (uint32_t bi = 0; bi <= ai; ++bi) {
+                const float a = __uint_as_float(bi << 16);
+                ++n;
+                bad += nvfp4_block_code(a, s_g, dg, false) != e4m3_byte(__fdiv_rn(__fdiv_rn(a, kE2M1Max), s_g)) ? 1 : 0;
+                if (v) {
+                    ++n;
+                    bad += nvfp4_block_code(a, s_g, dg, true) != e4m3_byte(__fdiv_rn(__fdiv_rn(a, 4.0f), s_g)) ? 1 : 0;
+                }
+            }
+        }
+    }
+    atomicAdd(&counts[0], n);
+    atomicAdd(&counts[1], bad);
+    atomicAdd(&counts[2], fast);
+}
+
 int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t st) {
-    if (nvfp4)
+    if (nvfp4 == 2)
+        quotient_sweep_block_code_kernel<<<(0x7F80u + 255u) / 256u, 256, 0, st>>>(counts);
+    else if (nvfp4)
         quotient_sweep_nvfp4_kernel<<<(0x7F80u * 252u + 255u) / 256u, 256, 0, st>>>(counts);
     else
         quotient_sweep_kernel<<<(0x7F80 + 255) / 256, 256, 0, st>>>(counts);
@@ -1323,7 +1489,7 @@ namespace fp8bs {
 // pass 2 reduces those `nparts` partials, so no slot needs clearing first.
 int launch_quantize_per_tensor_scratch(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
                                        float* scale, uint32_t* partials, int nparts, cudaStream_t st) {
-    amax_partials_kernel<<<nparts, kThreads, 0, st>>>(x, rows, cols, ldx, partials);
+    amax_partials_kernel<<<nparts, kThreads, 0, st>>>(x, rows, cols, ldx, partials, l2_keep_x(rows, ldx));
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     const int nb = rowwise_blocks(rows, cols, sm_count() * 8);

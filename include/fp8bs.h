@@ -394,15 +394,42 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
  *   nvfp4 = 1  E2M1 casts of NVFP4: every positive finite BF16 amax_T,
  *              S_g = amax_T / 2688 and amax_T / 1536 (four-over-six), every
  *              block scale code 1..126, S = E4M3value * S_g, every finite
- *              BF16 x with |x| <= amax_T (about 1.3e11 pairs).
+ *              BF16 x with |x| <= amax_T (about 1.3e11 pairs);
+ *   nvfp4 = 2  NVFP4 block scale codes E4M3(RN(RN(a / 6) / S_g)), and
+ *              E4M3(RN(RN(a / 4) / S_g)) for the four-over-six divisor,
+ *              which the quantisers take as RN(a / 6) by the same
+ *              correction step with r = RN(1/6), the exact a * 0.25, then
+ *              the correction step with r = RN(1/S_g): every positive
+ *              finite BF16 amax_T, both outer divisors, every BF16 block
+ *              amax a <= amax_T (about 1.6e9 codes); also RN(a / 6) itself,
+ *              bit for bit, for every finite BF16 a >= 0.
  *   counts  DEVICE uint64[3], zero-filled by the caller, 8-byte aligned;
  *           receives [0] pairs checked, [1] pairs whose codes differ (0 is
- *           the contract), [2] scales on the fast path (S >= 2^-88;
- *           smaller ones divide exactly).
- * Runs for about a millisecond (nvfp4 = 0) or a second (nvfp4 = 1).  No
- * counterpart on the pages.
+ *           the contract; mode 2 also counts RN(a / 6) mismatches here),
+ *           [2] scales on the fast path (S >= 2^-88; smaller ones divide
+ *           exactly).
+ * Runs for about a millisecond (nvfp4 = 0 and 2) or a second (nvfp4 = 1).
+ * No counterpart on the pages.
  */
 int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream);
+
+/*
+ * fp8bs_test_encoder_breakpoints -- where the device casts change code.
+ * The saturating round-to-nearest-even casts to E4M3 and E2M1 ("Low
+ * Precision RL", table "Choose a precision": FP8 E4M3 and NVFP4 E2M1
+ * elements) are monotone in |x|, so each is fixed by its breakpoints: for
+ * every nonzero code magnitude c, the smallest float32 magnitude whose code
+ * has magnitude >= c.  A one-CTA kernel finds them by binary search over
+ * the float32 bit patterns, through the same packed casts the quantisers
+ * use, for both signs.
+ *   out  DEVICE uint32[266]: out[s*126 + c-1] (s = 0 positive, 1 negative,
+ *        c = 1..126) the E4M3 breakpoints' float32 bits (magnitude);
+ *        out[252 + s*7 + c-1] (c = 1..7) the E2M1 ones.  An entry is
+ *        0xFFFFFFFF if the lanes of a packed cast disagreed or a code had
+ *        the wrong sign.
+ * FP8BS_EINVAL for NULL, FP8BS_EALIGN if out is not 4-byte aligned.
+ */
+int fp8bs_test_encoder_breakpoints(uint32_t* out, fp8bs_stream_t stream);
 
 /*
  * fp8bs_mma_peak -- dense tensor-core throughput loop, to measure the FP8
@@ -441,9 +468,13 @@ int fp8bs_mma_peak(int kind, int n, int iters, int pattern, float* out, void* wo
  * input and output buffers (a framework allocator owns all device memory, a
  * plugin interface passes tensors but no scratch, a real-time caller forbids
  * allocation while running) use this entry point instead: the partials live
- * in a fixed array inside the library (FP8BS_NOALLOC_MAX_PARTIALS 32-bit
- * words, 16 KB, held on every GPU that loads the library until exit).  It
- * never calls an allocating routine.
+ * in a fixed array inside the library's device module
+ * (FP8BS_NOALLOC_MAX_PARTIALS 32-bit words, 16 KB).  It never calls an
+ * allocating routine itself, but the array is committed when the module is
+ * loaded on a device, and under CUDA's default lazy module loading that
+ * happens at the first call on that device (in that context).  A caller
+ * with a strict no-allocation phase makes one warm-up call on each device
+ * before that phase (and before any stream capture).
  *
  *   x      BF16 [rows, cols], pitch ld_x (as fp8_quantize)
  *   q      E4M3 codes [rows, cols], written
@@ -453,15 +484,27 @@ int fp8bs_mma_peak(int kind, int n, int iters, int pattern, float* out, void* wo
  * Limit: rows * ceil(cols / 1024) <= 64 * FP8BS_NOALLOC_MAX_PARTIALS
  * (262144; e.g. 268,435,456 elements when cols is a multiple of 1024);
  * larger inputs return FP8BS_EINVAL and launch nothing.  Other checks and
- * codes as fp8_quantize.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Every call uses the same array: calls that
- * overlap on the GPU (different streams without ordering) race and give
- * wrong scales.
+ * codes as fp8_quantize.  The first call in each context looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it under the
+ * context's unique id, so a context destroyed and created again
+ * (cudaDeviceReset) is looked up afresh rather than served a stale address.
+ * Every call uses the same array: calls that overlap on the GPU (different
+ * streams without ordering) race and give wrong scales.
  */
 #define FP8BS_NOALLOC_MAX_PARTIALS 4096
 int fp8_quantize_per_tensor_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
                                     float* scale, fp8bs_stream_t stream);
+
+/*
+ * fp8bs_test_noalloc_scratch -- test hook for the entry point above.
+ * Writes to *cached the device address of its partials array that the
+ * entry point would use in the calling thread's current context (through
+ * its per-context cache, looking it up if needed) and to *looked_up the
+ * address a fresh cudaGetSymbolAddress returns.  They are equal unless the
+ * cache is stale.  Launches nothing.  FP8BS_EINVAL for NULL arguments,
+ * FP8BS_ECUDA if a lookup fails.
+ */
+int fp8bs_test_noalloc_scratch(void** cached, void** looked_up);
 
 /* Bytes of workspace every entry point accepts (FP8BS_WORKSPACE_BYTES). */
 size_t fp8bs_workspace_size(void);

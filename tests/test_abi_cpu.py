@@ -206,5 +206,14 @@ def test_stalled_gemm_nvfp4_rejects_bad_arguments(lib):
 
 def test_quotient_sweep_rejects_bad_arguments(lib):
     assert lib.fp8bs_test_quotient_sweep(None, 0, None) == -1
-    assert lib.fp8bs_test_quotient_sweep(FAKE, 2, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(FAKE, 3, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(FAKE, -1, None) == -1
     assert lib.fp8bs_test_quotient_sweep(ODD4, 1, None) == -2
+
+
+def test_encoder_breakpoints_and_scratch_hook_reject_bad_arguments(lib):
+    assert lib.fp8bs_test_encoder_breakpoints(None, None) == -1
+    assert lib.fp8bs_test_encoder_breakpoints(ctypes.c_void_p(0x1002), None) == -2
+    p = ctypes.c_void_p()
+    assert lib.fp8bs_test_noalloc_scratch(None, ctypes.byref(p)) == -1
+    assert lib.fp8bs_test_noalloc_scratch(ctypes.byref(p), None) == -1

@@ -263,6 +263,18 @@ def test_fp32_scale_division_matches_ieee_codes_exhaustively():
 
 
 
+def test_nvfp4_block_scale_codes_match_ieee_exhaustively():
+    """The NVFP4 block scale code E4M3(RN(RN(a / 6) / S_g)) (and the
+    four-over-six a / 4 form) is taken without IEEE division on the fast
+    path.  Over every BF16 tensor amax, both outer divisors and every BF16
+    block amax a <= amax_T the codes must equal the IEEE ones, and RN(a / 6)
+    itself must be bit-exact for every BF16 a."""
+    pairs, bad, fast = fp.test_quotient_sweep(nvfp4=2)
+    assert bad == 0
+    assert pairs > 1_000_000_000
+    assert fast > 50_000          # both divisors, every amax_T down to about 2^-76
+
+
 def test_nvfp4_block_division_matches_ieee_codes_exhaustively():
     """NVFP4 divides each block by S_b = E4M3value * S_g the same way; over
     every amax_T, both outer divisors, every block scale code and every BF16
@@ -271,3 +283,32 @@ def test_nvfp4_block_division_matches_ieee_codes_exhaustively():
     assert bad == 0
     assert pairs > 100_000_000_000
     assert fast > 1_000_000
+
+
+def test_encoder_breakpoints_match_the_oracle():
+    """Both casts are monotone in |x|, so they are fixed by where they change
+    code.  The device finds, through the quantisers' own packed casts and for
+    both signs, the smallest float32 magnitude giving each nonzero code
+    magnitude (E4M3: 126, E2M1: 7); the oracle's encoder must give exactly
+    that code there and the code below it one float32 step lower.  Together
+    that is the comparison over all float32 inputs, code by code."""
+    bp = fp.test_encoder_breakpoints()
+    assert 0xFFFFFFFF not in bp                  # lanes agreed, signs right
+    sections = ((0, 126, OF.e4m3_encode, 0x7F, 1.0), (126, 126, OF.e4m3_encode, 0x7F, -1.0),
+                (252, 7, OF.e2m1_encode, 0x7, 1.0), (259, 7, OF.e2m1_encode, 0x7, -1.0))
+    for start, count, enc, mask, sign in sections:
+        bits = np.array(bp[start:start + count], dtype=np.uint32)
+        assert np.all(np.diff(bits.astype(np.int64)) > 0)          # strictly increasing breakpoints
+        at = bits.view(np.float32) * np.float32(sign)
+        below = (bits - 1).view(np.float32) * np.float32(sign)
+        c = np.arange(1, count + 1)
+        assert np.array_equal(enc(at) & mask, c), (start, bits)
+        assert np.array_equal(enc(below) & mask, c - 1), (start, bits)
+    # spot values from the formats: just above 2^-10 (half of E4M3's
+    # smallest subnormal, a tie to the even code 0); 432 (the midpoint of
+    # 416 and 448) goes up to the even 448; E2M1 0.25 -> 0, 0.75 -> 1.0
+    f = lambda b: float(np.uint32(b).view(np.float32))
+    assert f(bp[0]) == float(np.nextafter(np.float32(2.0 ** -10), np.float32(1)))
+    assert f(bp[125]) == 432.0
+    assert f(bp[252]) == float(np.nextafter(np.float32(0.25), np.float32(1)))
+    assert f(bp[253]) == 0.75
