@@ -218,7 +218,10 @@ def flush_l2(torch, buf):
     buf[: buf.numel() // 2].max()
 
 
-def time_fn(torch, fn, reps=TIMED_CALLS, flush=None, warm=3):
+WARM_CALLS = 10                                 # sub-benchmarks: untimed calls first
+
+
+def time_fn(torch, fn, reps=TIMED_CALLS, flush=None, warm=WARM_CALLS):
     """Median CUDA-event time (ms) of fn() on the current stream over `reps`
     calls, L2 flushed before each call; returns (median, samples)."""
     for _ in range(warm):
@@ -240,7 +243,7 @@ BATCH_SETS = 4                                  # rotating buffer sets for short
 BATCH_CALLS = 16                                # calls per timed sample (BATCH_SETS rounds)
 
 
-def time_batched(torch, fns, reps=TIMED_CALLS, flush=None, warm=1):
+def time_batched(torch, fns, reps=TIMED_CALLS, flush=None, warm=3):
     """Per-call CUDA-event time (ms) of short kernels: each of `reps` samples
     times BATCH_CALLS back-to-back calls that cycle through `fns` (one
     callable per buffer set, inputs and outputs distinct), after an L2
@@ -251,7 +254,7 @@ def time_batched(torch, fns, reps=TIMED_CALLS, flush=None, warm=1):
     last touched three calls (over 300 MB of traffic) earlier, more than the
     129 MB L2 holds, so every call still reads its input from HBM and its
     writes still reach HBM."""
-    for _ in range(warm):
+    for _ in range(warm):            # warm rounds over every set (12 calls for 4 sets)
         for f in fns:
             f()
     ts = []
@@ -333,6 +336,11 @@ def quantize_sweep(torch, fp, dev, pk, flush):
                for xi, o in zip(xs, sets)]
         ms, _ = time_batched(torch, fns, flush=flush)
         out[g] = row(nbytes, ms)
+        if g in ("per_tensor", "nvfp4"):
+            # the same time against one read of X, the ideal if X could stay
+            # on chip between the amax pass and the cast
+            once = nbytes - 2 * e
+            out[g]["frac_single_read_ideal"] = round(once / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)
         if g in ("1x128", "mxfp8"):
             sbytes = {"1x128": 4 * e // 128, "mxfp8": e // 32}[g]
             xds = [torch.empty((r, c), dtype=torch.bfloat16, device=dev) for _ in xs]
@@ -530,6 +538,19 @@ def nvfp4_bench(torch, fp, dev, pk, flush):
 
 
 # ---------------------------------------------------------------- CPU oracle
+def cpu_model() -> str:
+    """The host CPU's model name (Linux /proc/cpuinfo), else the platform's."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_oracle_sample(rows: int = 4096):
     """The oracle on a bounded slice of the step: quantise `rows` token rows of
     X and dY and the whole weight W, run the three GEMMs for those rows
@@ -557,7 +578,7 @@ def cpu_oracle_sample(rows: int = 4096):
     flop = 3 * 2 * rows * H3 * I3
     threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or (os.cpu_count() or 1)
     return {"value": flop / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "seconds": round(dt, 2),
+            "cpu": cpu_model(), "seconds": round(dt, 2),
             "sample": f"{rows} of {M3} token rows of the step (all three GEMMs, weight quantised in full); "
                       f"FLOPs counted for the sample only"}
 

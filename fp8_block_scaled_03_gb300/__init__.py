@@ -10,7 +10,8 @@ Entry points (same names as the C ABI):
     fp8_quantize_transposed(x, gran, also_rowwise=False)
                                           -> (q_t, scales_t, q, scales)
     fp8_dequantize(q, scales, gran)       -> BF16 values (exact, rounded once)
-    fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16)
+    fp8_block_gemm(a, sa, a_gran, b, sb, b_gran, a_ts=None, b_ts=None) -> d (bf16, or float32 with
+                                          out_dtype=torch.float32)
     fp8_grouped_gemm(a, sa, b, sb, offsets, gran)                      -> d (bf16)
     fp8_quantize_gathered(x, token_index, gran) -> (q, scales)   rows x[token_index]
     fp8_swiglu_quantize(h, gran)          -> (q, scales)   of BF16(silu(gate) * up)
@@ -70,7 +71,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_quantize.argtypes = [P, I64, I64, I64, I, P, P, P, U, P, SZ, P]
     lib.fp8_quantize_transposed.argtypes = [P, I64, I64, I64, I, P, P, P, P, P, U, P, SZ, P]
     lib.fp8_dequantize.argtypes = [P, P, P, I64, I64, I, P, I64, P]
-    lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, P, SZ, P]
+    lib.fp8_block_gemm.argtypes = [P, P, I, P, P, I, P, P, I64, I64, I64, P, I, P, SZ, P]
     lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.fp8_quantize_gathered.argtypes = [P, I64, I64, I64, P, I64, I, P, P, P, SZ, P]
     lib.fp8_gather_rows.argtypes = [P, P, I64, I64, I, P, I64, P, P, P, SZ, P]
@@ -247,19 +248,29 @@ def fp8_dequantize(q, scales, gran, cols: Optional[int] = None, tensor_scale=Non
     return out
 
 
+OUT_DTYPES = {torch.bfloat16: 0, torch.float32: 1}     # FP8BS_OUT_BF16, FP8BS_OUT_F32
+
+
 def fp8_block_gemm(a, a_scales, a_gran, b, b_scales, b_gran, a_tensor_scale=None, b_tensor_scale=None, *,
-                   k: Optional[int] = None, out=None, ws=None, stream=None):
-    """D = deq(A) . deq(B)^T in BF16.  A [m, k] and B [n, k] codes (NVFP4: packed [., k/2])."""
+                   k: Optional[int] = None, out=None, out_dtype=None, ws=None, stream=None):
+    """D = deq(A) . deq(B)^T in BF16 (or float32: out_dtype=torch.float32, or
+    an `out` of that dtype).  A [m, k] and B [n, k] codes (NVFP4: packed [., k/2])."""
     ga, gb = _gran(a_gran), _gran(b_gran)
     m, n = a.shape[0], b.shape[0]
     if k is None:
         k = a.shape[1] * (2 if ga in NVFP4_GRANS else 1)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if out_dtype not in OUT_DTYPES:
+        raise ValueError(f"fp8_block_gemm: out_dtype must be bfloat16 or float32, not {out_dtype}")
     if out is None:
-        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+        out = torch.empty((m, n), dtype=out_dtype, device=a.device)
+    elif out.dtype != out_dtype:
+        raise ValueError("fp8_block_gemm: out.dtype differs from out_dtype")
     ws = ws if ws is not None else workspace(a.device)
     rc = load_library().fp8_block_gemm(_ptr(a), _ptr(a_scales), ga, _ptr(b), _ptr(b_scales), gb,
                                        _ptr(a_tensor_scale), _ptr(b_tensor_scale), m, n, k, _ptr(out),
-                                       _ptr(ws), ws.numel(), _stream(stream))
+                                       OUT_DTYPES[out_dtype], _ptr(ws), ws.numel(), _stream(stream))
     _check("fp8_block_gemm", rc)
     return out
 

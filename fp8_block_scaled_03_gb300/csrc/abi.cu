@@ -224,11 +224,12 @@ int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h
 int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
                    const void* b, const void* b_scales, int b_gran,
                    const float* a_tensor_scale, const float* b_tensor_scale,
-                   int64_t m, int64_t n, int64_t k, void* d,
+                   int64_t m, int64_t n, int64_t k, void* d, int d_dtype,
                    void* workspace, size_t workspace_bytes, fp8bs_stream_t stream) {
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0) return FP8BS_EINVAL;
+    if (d_dtype != FP8BS_OUT_BF16 && d_dtype != FP8BS_OUT_F32) return FP8BS_EINVAL;
     if (a_gran < 0 || a_gran > FP8BS_NVFP4_ROW_1x16 || b_gran < 0 || b_gran > FP8BS_NVFP4_ROW_1x16)
         return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
@@ -240,6 +241,7 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
     j.b = b; j.sb = b_scales; j.b_gran = b_gran;
     j.a_ts = a_tensor_scale; j.b_ts = b_tensor_scale;
     j.m = m; j.n = n; j.k = k; j.d = d;
+    j.d_f32 = d_dtype == FP8BS_OUT_F32;
     j.status = static_cast<int*>(workspace);
     j.offsets = nullptr; j.experts = 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -460,6 +462,6 @@ const char* fp8bs_status_string(int status) {
     }
 }
 
-int fp8bs_version(void) { return 101; }
+int fp8bs_version(void) { return 102; }
 
 }  // extern "C"

@@ -34,9 +34,10 @@
 //               thread) and columns 128*((w-4)/4).. (one 128-column half);
 //               acc += partial * sa * sb with both scales read from the
 //               ring.  At the end of the tile each warp writes its 32 rows as
-//               BF16 into a 4 KB staging buffer, 64 columns at a time, and a
-//               TMA store takes them out, so the warp is back to promoting
-//               while the store drains (its stores used to hold the MMA up).
+//               BF16 into a 4 KB staging buffer, 64 columns at a time (float32
+//               output: 32 at a time), and a TMA store takes them out, so the
+//               warp is back to promoting while the store drains (its stores
+//               used to hold the MMA up).
 // Scale modes (template): 0 per-tensor, 1 per row (1x128), 2 per 128-row block.
 #include <algorithm>
 
@@ -68,6 +69,7 @@ struct Params {
     int experts;
     uint64_t wait_ns;     // bound of every pipeline wait
     int stall_stage0;     // test hook: the producer withholds stage 0
+    int out_f32;          // D is float32 (tm_d then maps float32 32 x 32 boxes)
 };
 
 struct alignas(16) Shared {
@@ -350,7 +352,29 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             // tile's row group (always for a dense GEMM; an expert's last,
             // partial row block may end inside them, and the rows after it
             // belong to the next expert).
-            if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
+            if ((p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) && p.out_f32) {
+                // float32 output: the same staging buffer holds 32 rows x 32
+                // floats (128-byte rows, same swizzle); four boxes per warp
+                uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float a0, a1, a2, a3;
+                        f2_unpack(acc[16 * qq + 2 * c], a0, a1);
+                        f2_unpack(acc[16 * qq + 2 * c + 1], a2, a3);
+                        *reinterpret_cast<float4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_float4(a0, a1, a2, a3);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 32 * qq), (int32_t)(ti.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            } else if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
                 // BF16 tile rows through this warp's staging buffer (128-byte
                 // swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)), then a
                 // TMA store of the 32 x 64 box; the TMA clips rows and columns
@@ -377,6 +401,17 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     if (lane == 0) {
                         tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 64 * half), (int32_t)(ti.row0 + 32 * q));
                         bulk_commit();
+                    }
+                }
+            } else if (row < ti.row_end && p.out_f32) {
+                float* drow = reinterpret_cast<float*>(p.d) + row * p.n + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4) {
+                    if (col0 + j < p.n) {
+                        float a0, a1, a2, a3;
+                        f2_unpack(acc[j / 2], a0, a1);
+                        f2_unpack(acc[j / 2 + 1], a2, a3);
+                        *reinterpret_cast<float4*>(drow + j) = make_float4(a0, a1, a2, a3);
                     }
                 }
             } else if (row < ti.row_end) {
@@ -442,7 +477,10 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
         !make_tmap_u8(&tb, j.b, (uint64_t)j.k, b_rows, (uint64_t)j.k, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return (int)cudaErrorInvalidValue;
     CUtensorMap td;
-    if (!make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n)) return (int)cudaErrorInvalidValue;
+    const bool td_ok = j.d_f32 ? make_tmap_out_f32(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n, 32,
+                                                   CU_TENSOR_MAP_SWIZZLE_128B)
+                               : make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n);
+    if (!td_ok) return (int)cudaErrorInvalidValue;
     Params p{};
     p.m = j.m; p.n = j.n; p.k = j.k;
     p.sa = static_cast<const float*>(j.sa);
@@ -453,6 +491,7 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
     p.experts = j.experts;
     p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
     p.stall_stage0 = j.stall_stage0;
+    p.out_f32 = j.d_f32 ? 1 : 0;
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) {

@@ -31,7 +31,7 @@
 //   warps 4-11  epilogue: drain the 128 x 256 FP32 accumulator (one row and
 //               128 columns per thread) with one TMEM wait, release it,
 //               convert to BF16 and store 32 x 32 boxes by TMA through a
-//               2 KB staging buffer per warp.
+//               2 KB staging buffer per warp (float32 output: 32 x 16 boxes).
 // TMEM: columns 0..255 accumulator, 256.. scale factors per stage.  Dense
 // tiles are walked in groups of row tiles (sched_tile's GM).  One pass per
 // tile order and stage ring is shared by the dense and grouped forms.
@@ -86,6 +86,7 @@ struct Params {
     int experts;
     uint64_t wait_ns;     // bound of every pipeline wait
     int stall_stage0;     // test hook: the producer withholds stage 0
+    int out_f32;          // D is float32 (tm_d then maps float32 32 x 16 boxes)
 };
 
 // Dense tile order: groups of row tiles, row tile fastest inside a group.
@@ -589,13 +590,47 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
+            const int64_t col0 = ti.n0 + 128 * h;
+            if (p.out_f32) {
+                // float32 output: 32 rows x 16 floats per box (64-byte rows,
+                // the same swizzle and staging buffer as the BF16 boxes)
+#pragma unroll
+                for (int j = 0; j < 128; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * g);
+                if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
+                    uint8_t* ob = ostage + (warp - 4) * OSTAGE_BYTES;
+#pragma unroll
+                    for (int qb = 0; qb < 8; ++qb) {
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(ob + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
+                                make_uint4(r[16 * qb + 4 * c], r[16 * qb + 4 * c + 1], r[16 * qb + 4 * c + 2],
+                                           r[16 * qb + 4 * c + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 16 * qb), (int32_t)(ti.row0 + 32 * q));
+                            bulk_commit();
+                        }
+                    }
+                } else if (row < ti.row_end) {
+                    float* drow = reinterpret_cast<float*>(p.d) + row * p.n + col0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (col0 + 4 * j < p.n)
+                            *reinterpret_cast<uint4*>(drow + 4 * j) =
+                                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    }
+                }
+                continue;
+            }
             uint32_t packed[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
                 __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * g, __uint_as_float(r[2 * j + 1]) * g);
                 packed[j] = *reinterpret_cast<uint32_t*>(&v);
             }
-            const int64_t col0 = ti.n0 + 128 * h;
             if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
                 // The warp's 32 rows all belong to the tile's row group: out by
                 // TMA, 32 columns at a time through the warp's staging buffer
@@ -664,9 +699,12 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     const uint64_t kbytes = nv ? (uint64_t)j.k / 2 : (uint64_t)j.k;
     const uint64_t b_rows = (uint64_t)j.n * (uint64_t)(j.experts > 0 ? j.experts : 1);
     CUtensorMap ta, tb, td;
+    const bool td_ok = j.d_f32 ? make_tmap_out_f32(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n, 16,
+                                                   CU_TENSOR_MAP_SWIZZLE_64B)
+                               : make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n, 32,
+                                                    CU_TENSOR_MAP_SWIZZLE_64B);
     if (!make_tmap_u8(&ta, j.a, kbytes, (uint64_t)j.m, kbytes, BKB, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_u8(&tb, j.b, kbytes, b_rows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_out_bf16(&td, j.d, (uint64_t)j.n, (uint64_t)j.m, (uint64_t)j.n, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_tmap_u8(&tb, j.b, kbytes, b_rows, kbytes, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B) || !td_ok)
         return (int)cudaErrorInvalidValue;
     Params p{};
     p.m = j.m; p.n = j.n; p.k = j.k;
@@ -680,6 +718,7 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     p.experts = j.experts;
     p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
     p.stall_stage0 = j.stall_stage0;
+    p.out_f32 = j.d_f32 ? 1 : 0;
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);

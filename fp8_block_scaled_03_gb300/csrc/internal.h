@@ -68,6 +68,7 @@ struct GemmJob {
     bool a_ts_rows = false;               // NVFP4: a_ts holds one outer scale per row of A
     int64_t m, n, k;
     void* d;
+    bool d_f32 = false;                   // D is float32 (fp8_block_gemm's FP8BS_OUT_F32), else BF16
     int* status;
     // grouped
     const int64_t* offsets; int experts;  // experts == 0 -> dense

@@ -76,4 +76,21 @@ inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols
     return r == CUDA_SUCCESS;
 }
 
+// float32 output matrix [rows, cols] (pitch `pitch_elems`), box {box_cols,
+// 32}: 32 columns (128-byte rows) with 128-byte swizzle, or 16 (64-byte
+// rows) with 64-byte swizzle, for the GEMM epilogues' FP32 output.
+inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
+                              uint32_t box_cols, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch_elems * 4};
+    cuuint32_t box[2] = {box_cols, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace fp8bs

@@ -260,13 +260,25 @@ int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, i
 int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h, int gran, void* q, void* scales,
                         fp8bs_stream_t stream);
 
+/* Output types of fp8_block_gemm's D. */
+typedef enum {
+    FP8BS_OUT_BF16 = 0,
+    FP8BS_OUT_F32 = 1
+} fp8bs_out_dtype;
+
 /*
- * fp8_block_gemm -- D[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], D in BF16.
+ * fp8_block_gemm -- D[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], D in BF16
+ * or float32.
  *
  * The matching low-precision GEMM of "Low Precision RL" ("Unified training
  * recipe"), on operands quantised as above, with FP32 accumulation on the
  * tensor cores.  A is [m, k], B is [n, k]; both K-major (row-major with k
- * contiguous); D is row-major [m, n] BF16 (round-to-nearest-even).
+ * contiguous); D is row-major [m, n]: d_dtype FP8BS_OUT_BF16 rounds the FP32
+ * accumulator to BF16 (round-to-nearest-even), FP8BS_OUT_F32 writes the
+ * accumulator itself (for a caller that accumulates in float32, e.g. weight
+ * gradients into float32 main gradients).  Both come from the same
+ * accumulator: the BF16 output is the float32 output rounded.  Other
+ * d_dtype values return FP8BS_EINVAL.
  *
  *   (a_gran, b_gran)                          scale handling
  *   {PER_TENSOR,TOKEN_1x128,BLOCK_128x128}^2  FP32 scales applied per
@@ -291,7 +303,7 @@ int fp8_swiglu_quantize(const void* h, int64_t rows, int64_t inter, int64_t ld_h
 int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
                    const void* b, const void* b_scales, int b_gran,
                    const float* a_tensor_scale, const float* b_tensor_scale,
-                   int64_t m, int64_t n, int64_t k, void* d,
+                   int64_t m, int64_t n, int64_t k, void* d, int d_dtype,
                    void* workspace, size_t workspace_bytes, fp8bs_stream_t stream);
 
 /*

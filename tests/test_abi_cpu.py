@@ -40,7 +40,7 @@ def test_status_strings_and_sizes(lib):
     assert ws(2, 4, 128, 1, 0) == 0 and ws(7, 4, 128, 3, 0) == 0               # dequantise, SwiGLU: none
     assert all(ws(op, 4, 128, 3, 0) == 16384 for op in (3, 4, 5, 6))          # GEMMs, gathers: status word
     assert ws(8, 4, 128, 1, 0) == 2 ** 64 - 1 and ws(0, -1, 128, 1, 0) == 2 ** 64 - 1
-    assert lib.fp8bs_version() == 101
+    assert lib.fp8bs_version() == 102
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert fp.status_string(code) != "unknown status"
     assert fp.status_string(7) == "unknown status"
@@ -74,14 +74,20 @@ def test_quantize_transposed_rejects_bad_arguments(lib):
 
 def test_gemm_rejects_bad_arguments(lib):
     g = lib.fp8_block_gemm
-    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, None, 0, None) == -6
-    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 132, 256, FAKE, FAKE, 16384, None) == -1  # n % 8
-    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 0, 128, 256, FAKE, FAKE, 16384, None) == -1
-    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 192, FAKE, FAKE, 16384, None) == -1  # k % 128
-    assert g(FAKE, FAKE, 3, FAKE, FAKE, 1, None, None, 128, 128, 256, FAKE, FAKE, 16384, None) == -3  # mixed
-    assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, None, None, 128, 128, 256, FAKE, FAKE, 16384, None) == -1  # nvfp4 ts
-    assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, FAKE, 16384, None) == -1  # k % 256
-    assert g(MISALIGNED, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, FAKE, 16384, None) == -2
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, None, 0, None) == -6
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 132, 256, FAKE, 0, FAKE, 16384, None) == -1  # n % 8
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 0, 128, 256, FAKE, 0, FAKE, 16384, None) == -1
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 192, FAKE, 0, FAKE, 16384, None) == -1  # k % 128
+    assert g(FAKE, FAKE, 3, FAKE, FAKE, 1, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -3  # mixed
+    assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -1  # nvfp4 ts
+    assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, 0, FAKE, 16384, None) == -1  # k % 256
+    assert g(MISALIGNED, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -2
+
+
+def test_gemm_rejects_unknown_output_dtype(lib):
+    g = lib.fp8_block_gemm
+    for bad in (2, -1):
+        assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, bad, FAKE, 16384, None) == -1
 
 
 def test_grouped_gemm_rejects_bad_arguments(lib):
@@ -131,10 +137,10 @@ def test_dequantize_rejects_bad_arguments(lib):
 
 def test_gemm_row_scaled_nvfp4_arguments(lib):
     g = lib.fp8_block_gemm
-    assert g(FAKE, FAKE, 7, FAKE, FAKE, 7, FAKE, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -3  # B per row
-    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, None, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -1  # A S_g
-    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, ODD4, FAKE, 128, 128, 256, FAKE, FAKE, 16384, None) == -2
-    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, FAKE, 16384, None) == -1  # k % 256
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 7, FAKE, FAKE, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -3  # B per row
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, None, FAKE, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -1  # A S_g
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, ODD4, FAKE, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -2
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, 0, FAKE, 16384, None) == -1  # k % 256
 
 
 def test_gathered_quantize_rejects_bad_arguments(lib):
