@@ -182,6 +182,7 @@ struct RowSrc {
     int64_t tokens;       // gather: rows of x
     int64_t up;           // SwiGLU: column where up starts
     int* status;          // gather: sticky status word for an index out of range
+    bool keep_x;          // gather: load x with an L2 evict-last policy (x fits in L2)
 };
 
 // Float32 pair arithmetic, each half rounded on its own (round to nearest).
@@ -365,6 +366,16 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
                 const int64_t c = cb + j * 256 + lane * 8;
                 v[j] = (c < cols) ? ldg_v4(xr + c) : make_uint4(0, 0, 0, 0);
                 uv[j] = (c < cols) ? ldg_v4(xr + src.up + c) : make_uint4(0, 0, 0, 0);
+            }
+        } else if (SRC == kSrcGather && src.keep_x) {
+            // Each token is gathered once per expert it is routed to, rows
+            // apart; the evict-last mark keeps x in L2 between those copies
+            // while the codes stream out.
+            const uint64_t pol = l2_policy_evict_last();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t c = cb + j * 256 + lane * 8;
+                v[j] = (c < cols && valid) ? ldg_v4_policy(xr + c, pol) : make_uint4(0, 0, 0, 0);
             }
         } else {
 #pragma unroll
@@ -1413,7 +1424,7 @@ static int launch_rows_src(const QuantJob& j, const RowSrc& src, int nb, cudaStr
 int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int64_t tokens, int64_t up,
                              cudaStream_t st) {
     const int nb = rowwise_blocks(j.rows, j.cols, sm_count() * 8);
-    RowSrc src{token_index, tokens, up, j.status};
+    RowSrc src{token_index, tokens, up, j.status, token_index != nullptr && l2_keep_x(tokens, j.ldx)};
     if (token_index != nullptr) return launch_rows_src<kSrcGather>(j, src, nb, st);
     return launch_rows_src<kSrcSwiglu>(j, src, nb, st);
 }
