@@ -539,14 +539,23 @@ def nvfp4_bench(torch, fp, dev, pk, flush):
 
 # ---------------------------------------------------------------- CPU oracle
 def cpu_model() -> str:
-    """The host CPU's model name (Linux /proc/cpuinfo), else the platform's."""
+    """The host CPU's model name: /proc/cpuinfo's (x86), lscpu's (Arm, whose
+    /proc/cpuinfo has none), else the platform's."""
     import platform
+    import subprocess
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 if line.lower().startswith(("model name", "cpu model")):
                     return line.split(":", 1)[1].strip()
     except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
         pass
     return platform.processor() or platform.machine()
 

@@ -86,7 +86,6 @@ struct Params {
     int experts;
     uint64_t wait_ns;     // bound of every pipeline wait
     int stall_stage0;     // test hook: the producer withholds stage 0
-    int out_f32;          // D is float32 (tm_d then maps float32 32 x 16 boxes)
 };
 
 // Dense tile order: groups of row tiles, row tile fastest inside a group.
@@ -320,7 +319,10 @@ __device__ __forceinline__ void drain_scale_copies(uint32_t bar, int lane, uint6
     __syncwarp();
 }
 
-template <int KIND, int SA, int SB>
+// F32: D is float32 (tm_d then maps float32 32 x 16 boxes); a template
+// parameter rather than a run-time flag, since the extra epilogue branch
+// cost the short-K grouped GEMMs a few per cent.
+template <int KIND, int SA, int SB, bool F32>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_d, Params p) {
@@ -591,7 +593,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
             const int64_t col0 = ti.n0 + 128 * h;
-            if (p.out_f32) {
+            if constexpr (F32) {
                 // float32 output: 32 rows x 16 floats per box (64-byte rows,
                 // the same swizzle and staging buffer as the BF16 boxes)
 #pragma unroll
@@ -675,20 +677,27 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 }
 
-template <int KIND, int SA = 0, int SB = 0>
-int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
-                cudaStream_t st) {
+template <int KIND, int SA, int SB, bool F32>
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
+                 cudaStream_t st) {
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<KIND, SA, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_bytes<KIND>());
+        cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<KIND, SA, SB, F32>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<KIND>());
         if (e != cudaSuccess) return (int)e;
         attr_set[dev] = true;
     }
-    gemm_mx_kernel<KIND, SA, SB><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, td, p);
+    gemm_mx_kernel<KIND, SA, SB, F32><<<grid, NUM_THREADS, smem_bytes<KIND>(), st>>>(ta, tb, td, p);
     return (int)cudaGetLastError();
+}
+
+template <int KIND, int SA = 0, int SB = 0>
+int launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
+                bool f32, cudaStream_t st) {
+    return f32 ? launch_typed<KIND, SA, SB, true>(ta, tb, td, p, grid, st)
+               : launch_typed<KIND, SA, SB, false>(ta, tb, td, p, grid, st);
 }
 
 }  // namespace
@@ -718,18 +727,18 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     p.experts = j.experts;
     p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
     p.stall_stage0 = j.stall_stage0;
-    p.out_f32 = j.d_f32 ? 1 : 0;
+    const bool f32 = j.d_f32;
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) grid = (int)std::min<int64_t>(ceil_div(j.m, BM) * ceil_div(j.n, BN), sms);
-    if (nv) return launch_kind<kNv>(ta, tb, td, p, grid, st);
-    if (j.a_gran == 3) return launch_kind<kMx>(ta, tb, td, p, grid, st);
+    if (nv) return launch_kind<kNv>(ta, tb, td, p, grid, f32, st);
+    if (j.a_gran == 3) return launch_kind<kMx>(ta, tb, td, p, grid, f32, st);
     // power-of-two block-wise: 5 = one byte per row and 128 K, 6 = per 128x128 block
     const int sa = j.a_gran == 5 ? 1 : 2, sb = j.b_gran == 5 ? 1 : 2;
-    if (sa == 1 && sb == 2) return launch_kind<kP2, 1, 2>(ta, tb, td, p, grid, st);
-    if (sa == 1 && sb == 1) return launch_kind<kP2, 1, 1>(ta, tb, td, p, grid, st);
-    if (sa == 2 && sb == 2) return launch_kind<kP2, 2, 2>(ta, tb, td, p, grid, st);
-    return launch_kind<kP2, 2, 1>(ta, tb, td, p, grid, st);
+    if (sa == 1 && sb == 2) return launch_kind<kP2, 1, 2>(ta, tb, td, p, grid, f32, st);
+    if (sa == 1 && sb == 1) return launch_kind<kP2, 1, 1>(ta, tb, td, p, grid, f32, st);
+    if (sa == 2 && sb == 2) return launch_kind<kP2, 2, 2>(ta, tb, td, p, grid, f32, st);
+    return launch_kind<kP2, 2, 1>(ta, tb, td, p, grid, f32, st);
 }
 
 }  // namespace fp8bs
