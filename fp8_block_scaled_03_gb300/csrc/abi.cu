@@ -389,7 +389,7 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
 }
 
 int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream) {
-    if (counts == nullptr || nvfp4 < 0 || nvfp4 > 2) return FP8BS_EINVAL;
+    if (counts == nullptr || nvfp4 < 0 || nvfp4 > 3) return FP8BS_EINVAL;
     if (reinterpret_cast<uintptr_t>(counts) & 7u) return FP8BS_EALIGN;
     return cuda_status(launch_quotient_sweep(counts, nvfp4, reinterpret_cast<cudaStream_t>(stream)));
 }

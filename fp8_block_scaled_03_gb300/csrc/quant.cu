@@ -396,9 +396,9 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
             uint2 o;
             if constexpr (GRAN == kGranTok) {
                 const uint32_t m = warp_max_u32(absmax_v4(v[j]), 16);
-                const float s = fp32_scale_from_amax(amax_bits_to_f32(m));
-                o = cast8_div(f, scale_div(s, true));
-                if (ok && (lane & 15) == 0) static_cast<float*>(sout)[r * ng + (c >> 7)] = s;
+                const ScaleDiv sd = scale_div_from_amax(amax_bits_to_f32(m));
+                o = cast8_div(f, sd);
+                if (ok && (lane & 15) == 0) static_cast<float*>(sout)[r * ng + (c >> 7)] = sd.s;
             } else if constexpr (GRAN == kGranMx) {
                 const uint32_t m = warp_max_u32(SRC == kSrcPlain ? absmax_v4_pairs(v[j]) : absmax_v4(v[j]), 4);
                 const int e = mx_exponent_from_amax_bits(m << 16);
@@ -901,6 +901,7 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         uint32_t m0 = mm & 0xFFFFu, m1 = mm >> 16;
         float d0 = 1.0f, d1 = 1.0f;       // divisors (FP32 scales) or multipliers (power-of-two scales)
         int e0 = 0, e1 = 0;
+        ScaleDiv tok0{}, tok1{};          // 1x128: the scales with their reciprocals
         if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
             sh.red[rq][cp] = make_uint2(m0, m1);
             __syncthreads();
@@ -911,8 +912,10 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                 m1 = max(m1, o.y);
             }
             if constexpr (GRAN == kGranTok) {
-                d0 = fp32_scale_from_amax(amax_bits_to_f32(m0));
-                d1 = fp32_scale_from_amax(amax_bits_to_f32(m1));
+                tok0 = scale_div_from_amax(amax_bits_to_f32(m0));
+                tok1 = scale_div_from_amax(amax_bits_to_f32(m1));
+                d0 = tok0.s;
+                d1 = tok1.s;
             } else {
                 e0 = mx_exponent_from_amax_bits(m0 << 16);
                 e1 = mx_exponent_from_amax_bits(m1 << 16);
@@ -926,8 +929,8 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
             d1 = exp2_neg(e1);
         }
         // ---------------- column pass, sweep 2: codes of X^T into registers (4 rows per word)
-        const ScaleDiv sd0 = kPow2<GRAN> ? ScaleDiv{d0, 0.0f, false} : scale_div(d0, true);
-        const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : scale_div(d1, true);
+        const ScaleDiv sd0 = kPow2<GRAN> ? ScaleDiv{d0, 0.0f, false} : tok0;
+        const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : tok1;
         uint32_t c0w[8], c1w[8];
         auto col_codes = [&](auto fast) {
             [[maybe_unused]] constexpr bool F = decltype(fast)::value;
@@ -1002,20 +1005,22 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
                 const uint32_t a = absmax_v4(v);
                 float dd;
                 int ee = 0;
+                ScaleDiv tokd{};
                 if constexpr (GRAN == kGranMx) {
                     ee = mx_exponent_from_amax_bits(warp_max_u32(a, 4) << 16);
                     dd = exp2_neg(ee);
                 } else {
                     const uint32_t m = warp_max_u32(a, 16);
                     if constexpr (GRAN == kGranTok) {
-                        dd = fp32_scale_from_amax(amax_bits_to_f32(m));
+                        tokd = scale_div_from_amax(amax_bits_to_f32(m));
+                        dd = tokd.s;
                     } else {
                         ee = mx_exponent_from_amax_bits(m << 16);
                         dd = exp2_neg(ee);
                     }
                 }
                 const int64_t c = c0 + 8 * ch;
-                const ScaleDiv sdd = kPow2<GRAN> ? ScaleDiv{dd, 0.0f, false} : scale_div(dd, true);
+                const ScaleDiv sdd = kPow2<GRAN> ? ScaleDiv{dd, 0.0f, false} : tokd;
                 if (r < rows) {
                     if (c < cols) {
                         auto row_codes = [&](auto fast) {
@@ -1331,8 +1336,27 @@ __global__ void __launch_bounds__(256) quotient_sweep_block_code_kernel(unsigned
     atomicAdd(&counts[2], fast);
 }
 
+// FP32 scales without IEEE operations: for every finite BF16 amax (zero
+// and subnormals included), the S and RN(1/S) that scale_div_from_amax
+// gives against __fdiv_rn(amax, 448) and __frcp_rn(S), bit for bit.
+// counts[0] amax values, [1] mismatches, [2] values on the fast path.
+__global__ void __launch_bounds__(256) quotient_sweep_scale_kernel(unsigned long long* __restrict__ counts) {
+    const uint32_t ai = blockIdx.x * blockDim.x + threadIdx.x;
+    if (ai > 0x7F7Fu) return;
+    const float amax = __uint_as_float(ai << 16);
+    const ScaleDiv got = scale_div_from_amax(amax);
+    const ScaleDiv want = scale_div(fp32_scale_from_amax(amax), true);
+    const bool same = __float_as_uint(got.s) == __float_as_uint(want.s) && got.fast == want.fast &&
+                      (!want.fast || __float_as_uint(got.r) == __float_as_uint(want.r));
+    atomicAdd(&counts[0], 1ull);
+    if (!same) atomicAdd(&counts[1], 1ull);
+    if (amax >= kFastScaleMinAmax) atomicAdd(&counts[2], 1ull);
+}
+
 int launch_quotient_sweep(unsigned long long* counts, int nvfp4, cudaStream_t st) {
-    if (nvfp4 == 2)
+    if (nvfp4 == 3)
+        quotient_sweep_scale_kernel<<<(0x7F80u + 255u) / 256u, 256, 0, st>>>(counts);
+    else if (nvfp4 == 2)
         quotient_sweep_block_code_kernel<<<(0x7F80u + 255u) / 256u, 256, 0, st>>>(counts);
     else if (nvfp4)
         quotient_sweep_nvfp4_kernel<<<(0x7F80u * 252u + 255u) / 256u, 256, 0, st>>>(counts);

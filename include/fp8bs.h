@@ -414,13 +414,20 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
  *              the correction step with r = RN(1/S_g): every positive
  *              finite BF16 amax_T, both outer divisors, every BF16 block
  *              amax a <= amax_T (about 1.6e9 codes); also RN(a / 6) itself,
- *              bit for bit, for every finite BF16 a >= 0.
+ *              bit for bit, for every finite BF16 a >= 0;
+ *   nvfp4 = 3  FP32 scales of the casts: for every finite BF16 amax, the
+ *              scale S = RN(amax / 448) and its reciprocal RN(1/S), which
+ *              the quantisers take for amax >= 2^-79 by the correction step
+ *              (r = RN(1/448)) and by two Newton steps from the hardware's
+ *              approximate reciprocal, against IEEE division and
+ *              reciprocal, bit for bit ([0] amax values, [1] mismatches,
+ *              [2] values on that path).
  *   counts  DEVICE uint64[3], zero-filled by the caller, 8-byte aligned;
  *           receives [0] pairs checked, [1] pairs whose codes differ (0 is
  *           the contract; mode 2 also counts RN(a / 6) mismatches here),
  *           [2] scales on the fast path (S >= 2^-88; smaller ones divide
  *           exactly).
- * Runs for about a millisecond (nvfp4 = 0 and 2) or a second (nvfp4 = 1).
+ * Runs for about a millisecond (nvfp4 = 0, 2, 3) or a second (nvfp4 = 1).
  * No counterpart on the pages.
  */
 int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_stream_t stream);

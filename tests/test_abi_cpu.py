@@ -212,7 +212,7 @@ def test_stalled_gemm_nvfp4_rejects_bad_arguments(lib):
 
 def test_quotient_sweep_rejects_bad_arguments(lib):
     assert lib.fp8bs_test_quotient_sweep(None, 0, None) == -1
-    assert lib.fp8bs_test_quotient_sweep(FAKE, 3, None) == -1
+    assert lib.fp8bs_test_quotient_sweep(FAKE, 4, None) == -1
     assert lib.fp8bs_test_quotient_sweep(FAKE, -1, None) == -1
     assert lib.fp8bs_test_quotient_sweep(ODD4, 1, None) == -2
 

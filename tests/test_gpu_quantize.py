@@ -263,6 +263,16 @@ def test_fp32_scale_division_matches_ieee_codes_exhaustively():
 
 
 
+def test_fp32_scales_without_ieee_operations_match_exhaustively():
+    """The FP32-scale casts take S = RN(amax / 448) and RN(1/S) without
+    IEEE division or reciprocal for amax >= 2^-79; for every finite BF16
+    amax both must be bit-identical to the IEEE results."""
+    values, bad, fast = fp.test_quotient_sweep(nvfp4=3)
+    assert values == 0x7F80
+    assert bad == 0
+    assert fast > 26_000
+
+
 def test_nvfp4_block_scale_codes_match_ieee_exhaustively():
     """The NVFP4 block scale code E4M3(RN(RN(a / 6) / S_g)) (and the
     four-over-six a / 4 form) is taken without IEEE division on the fast
