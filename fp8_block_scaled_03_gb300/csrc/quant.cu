@@ -255,17 +255,29 @@ __device__ __forceinline__ uint32_t bf16_bits_rne_f64(double v) {
     return __float_as_uint(f) >> 16;
 }
 
-// Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up; the
-// exponential, the sum and the product on element pairs, in float32 (a few
-// float32 ulps from the exact value before the BF16 rounding).
+// Eight SwiGLU outputs as BF16: silu(g) = g / (1 + e^-g), times up, in
+// float32 on element pairs (a few float32 ulps from the exact value before
+// the BF16 rounding).  The quotient g / d, d = 1 + e^-g in [1, e^80 + 1],
+// takes the correction step of div_fast with r from the hardware's
+// approximate reciprocal refined by Newton steps (rcp_newton): within about
+// one float32 ulp of the IEEE quotient, at a quarter of its instructions.
+// As in neg_quotient2, the pair steps run negated: q' = -g/d, and the
+// product with -up gives y.
 __device__ __forceinline__ uint4 swiglu8_f32(const float* g, const uint4& uv) {
     float u[8], y[8];
     unpack8(uv, u);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
         float d0, d1;
-        unpair(fadd2(splat2(1.0f), exp_seq2(-g[i], -g[i + 1])), d0, d1);
-        unpair(fmul2(pair_f32(__fdiv_rn(g[i], d0), __fdiv_rn(g[i + 1], d1)), pair_f32(u[i], u[i + 1])), y[i], y[i + 1]);
+        const uint64_t d2 = fadd2(splat2(1.0f), exp_seq2(-g[i], -g[i + 1]));
+        unpair(d2, d0, d1);
+        const uint64_t n2 = pair_f32(-rcp_newton(d0), -rcp_newton(d1));
+        const uint64_t g2 = pair_f32(g[i], g[i + 1]);
+        uint64_t yq, t, q;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(yq) : "l"(g2), "l"(n2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(yq), "l"(d2), "l"(g2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(t), "l"(n2), "l"(yq));
+        unpair(fmul2(q, pair_f32(-u[i], -u[i + 1])), y[i], y[i + 1]);
     }
     uint4 o;
     uint32_t* ow = &o.x;

@@ -249,7 +249,8 @@ int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, i
  *           float32 ulps (or 2^-146) of a BF16 rounding boundary, where
  *           either neighbouring BF16 value may result.  (The kernel
  *           evaluates y in float32: e^t by Cody-Waite reduction with ln 2
- *           split in two and the Taylor series of e^r to r^7, within a few
+ *           split in two and the Taylor series of e^r to r^7, the quotient
+ *           by a refined reciprocal and one correction step, within a few
  *           float32 ulps; gates below -80, where e^-g leaves the float32
  *           range, in float64.)  y must be finite.
  *   gran    TOKEN_1x128, MXFP8_1x32 or TOKEN_1x128_POW2 (other valid
