@@ -625,7 +625,9 @@ def workload_config(args):
                         "intermediate 9728); X,dY 1x128 FP32 scales (dual row+transposed), W 128x128 FP32 scales",
             "tokens": M3, "hidden": H3, "intermediate": I3, "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs 250 MB and step working set ~630 MB, both > 129 MB L2; sub-benchmarks flush L2 "
-                  "before each timed call (512 MB written, then 256 MB of it read back, so L2 starts cold and clean)"}
+                  "before each timed call (512 MB written, then 256 MB of it read back, so L2 starts cold and "
+                  "clean); quantiser rows time 16 back-to-back calls over 4 rotating input/output sets "
+                  "(~400 MB) after such a flush"}
 
 
 # ---------------------------------------------------------------- main
