@@ -94,3 +94,43 @@ def test_f32_output_rejects_other_dtypes():
     s = torch.ones((128, 1), dtype=torch.float32, device="cuda")
     with pytest.raises(ValueError):
         fp.fp8_block_gemm(q, s, "1x128", q, s, "1x128", out_dtype=torch.float16)
+
+
+def test_f32_output_full_size_step_sampled():
+    """The dense linear layer's three GEMMs at full size (Qwen3-4B MLP shape,
+    tokens 8192, hidden 2560, intermediate 9728) with float32 output: the
+    whole output rounded to BF16 equals the BF16 output, and sampled rows and
+    128-column blocks meet the accumulation bound against the oracle."""
+    m3, h3, i3 = 8192, 2560, 9728
+    x = synth.activations((m3, h3), seed=0, outlier_frac=0.01, outlier_mult=50.0)
+    w = synth.weights((i3, h3), seed=1, std=0.02)
+    dy = synth.activations((m3, i3), seed=2, outlier_frac=0.01, outlier_mult=50.0)
+    qxt, sxt, qx, sx = fp.fp8_quantize_transposed(to_dev_bf16(x), "1x128", also_rowwise=True)
+    qwt, swt, qw, sw = fp.fp8_quantize_transposed(to_dev_bf16(w), "128x128", also_rowwise=True)
+    qdyt, sdyt, qdy, sdy = fp.fp8_quantize_transposed(to_dev_bf16(dy), "1x128", also_rowwise=True)
+    xf, wf, dyf = to_f32(x), to_f32(w), to_f32(dy)
+    g = np.random.Generator(np.random.PCG64(31))
+    cases = (
+        # (A codes, scales, gran, B codes, scales, gran, k, A rows source, B rows source)
+        ("fprop", (qx, sx, "1x128", qw, sw, "128x128"), h3, lambda r: xf[r], lambda c: wf[c]),
+        ("dgrad", (qdy, sdy, "1x128", qwt, swt, "128x128"), i3, lambda r: dyf[r],
+         lambda c: np.ascontiguousarray(wf[:, c].T)),
+        ("wgrad", (qdyt, sdyt, "1x128", qxt, sxt, "1x128"), m3, lambda r: np.ascontiguousarray(dyf[:, r].T),
+         lambda c: np.ascontiguousarray(xf[:, c].T)),
+    )
+    for name, args, k, a_src, b_src in cases:
+        d32 = fp.fp8_block_gemm(*args, out_dtype=torch.float32)
+        d16 = fp.fp8_block_gemm(*args)
+        assert torch.equal(d32.to(torch.bfloat16).view(torch.int16), d16.view(torch.int16)), name
+        m, n = d32.shape
+        rows = np.sort(g.choice(m, 32, replace=False))
+        rows[-1] = m - 1
+        nb = int(g.integers(0, n // 128))
+        cols = np.arange(nb * 128, (nb + 1) * 128)
+        a64 = deq(a_src(rows), args[2])
+        b64 = deq(b_src(cols), args[5])
+        ref = OG.gemm_f64(a64, b64)
+        bound = (k + 3 * k / 128 + 2) * 2.0 ** -23 * (np.abs(a64) @ np.abs(b64).T)
+        got = d32[torch.from_numpy(rows).cuda()][:, nb * 128:(nb + 1) * 128].double().cpu().numpy()
+        assert np.all(np.abs(got - ref) <= bound), name
+    assert fp.read_status() == 0
