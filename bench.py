@@ -726,7 +726,7 @@ def main():
         line["moe_mxfp8"] = moe_bench(torch, fp, dev, pk, flush)
         line["nvfp4"] = nvfp4_bench(torch, fp, dev, pk, flush)
         line["moe_nvfp4"] = moe_nvfp4_bench(torch, fp, dev, pk, flush)
-        line["e2e"] = e2e_bench(torch, fp, dev, step)
+        line["e2e"] = e2e_bench(torch, fp, dev, step, reps=max(8, args.steps))
         line["cpu_baseline"] = cpu_oracle_sample()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -888,7 +888,10 @@ def e2e_bench(torch, fp, dev, step, reps=8):
     in and Y, dX and dW out.  The copies run on streams of their own, two
     buffer sets deep, so step i's outputs go out and step i+1's inputs come in
     while step i computes (as a training loop overlaps its transfers).
-    Timed with CUDA events from the first input copy to the last output copy."""
+    Timed with CUDA events from the first input copy to the last output copy,
+    over `reps` steps (the bench's --steps, at least 8): the pipeline's fill
+    (the first input copy and compute) and drain (the last output copy) are
+    inside the timed region and spread over those steps."""
     sets = [step, DenseStep(torch, fp, dev, seed=3000)]
     hx, hw, hdy = (t.cpu().pin_memory() for t in (step.x, step.w, step.dy))
     hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (s_.y, s_.dx, s_.dw)] for s_ in sets]
@@ -952,7 +955,7 @@ def e2e_bench(torch, fp, dev, step, reps=8):
     d2h = sum(t.numel() * t.element_size() for t in hout[0])
     return {"value": round(STEP_FLOP / (ms * 1e-3) / 1e12, 1), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "pipeline": "2 buffer sets; H2D, compute and D2H on separate streams",
+            "pipeline": f"2 buffer sets; H2D, compute and D2H on separate streams; {reps} steps timed",
             "host_link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
