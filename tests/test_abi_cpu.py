@@ -223,3 +223,21 @@ def test_encoder_breakpoints_and_scratch_hook_reject_bad_arguments(lib):
     p = ctypes.c_void_p()
     assert lib.fp8bs_test_noalloc_scratch(None, ctypes.byref(p)) == -1
     assert lib.fp8bs_test_noalloc_scratch(ctypes.byref(p), None) == -1
+
+
+def test_header_compiles_as_c99_and_links(lib, tmp_path):
+    """A plain C99 program (no CUDA headers) includes include/fp8bs.h, links
+    libfp8bs.so and calls entry points that need no GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(fp.LIB_PATH)
+    exe = str(tmp_path / "abi_c99")
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_c99.c"), "-L", libdir, "-lfp8bs", f"-Wl,-rpath,{libdir}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "c99 abi ok" in r.stdout, r.stdout + r.stderr
