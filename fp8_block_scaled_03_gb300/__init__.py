@@ -431,9 +431,10 @@ def test_quotient_sweep(nvfp4=False, stream=None):
 
 def test_encoder_breakpoints(stream=None):
     """Run fp8bs_test_encoder_breakpoints; returns the 266 breakpoint bit
-    patterns as a list (E4M3 positive, E4M3 negative, E2M1 positive, E2M1
-    negative)."""
-    out = torch.zeros(266, dtype=torch.int32, device="cuda")
+    patterns (E4M3 positive, E4M3 negative, E2M1 positive, E2M1 negative)
+    followed by the count of monotonicity and symmetry violations over every
+    finite float32."""
+    out = torch.zeros(267, dtype=torch.int32, device="cuda")
     _check("fp8bs_test_encoder_breakpoints", load_library().fp8bs_test_encoder_breakpoints(_ptr(out), _stream(stream)))
     return [v & 0xFFFFFFFF for v in out.cpu().tolist()]
 

@@ -1308,8 +1308,34 @@ __global__ void __launch_bounds__(288) encoder_breakpoints_kernel(uint32_t* __re
     out[t] = ok ? hi : 0xFFFFFFFFu;
 }
 
+// Every finite positive float32 bit pattern b in [0, 0x7F7FFFFE]: the
+// packed E4M3 and E2M1 casts of b+1 give a code magnitude at least that of
+// b (monotone), and the cast of -b is the cast of b with its sign bit set
+// (symmetric).  Violations are counted into *bad.  With the breakpoints
+// above this fixes both casts on every finite float32.
+__global__ void __launch_bounds__(256) encoder_monotone_kernel(unsigned int* __restrict__ bad) {
+    const uint32_t stride = gridDim.x * blockDim.x;
+    unsigned int n = 0;
+    for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < 0x7F7FFFFFu; b += stride) {
+        const float x0 = __uint_as_float(b), x1 = __uint_as_float(b + 1);
+        const uint32_t e = e4m3x4_pairs(pair_f32(x0, x1), pair_f32(-x0, -x1));
+        const uint32_t c0 = e & 0xFFu, c1 = (e >> 8) & 0xFFu, n0 = (e >> 16) & 0xFFu, n1 = e >> 24;
+        n += (c1 < c0) ? 1u : 0u;
+        n += (n0 != (c0 | 0x80u) || n1 != (c1 | 0x80u)) ? 1u : 0u;
+        const float a[8] = {x0, x1, -x0, -x1, 0.f, 0.f, 0.f, 0.f};
+        const uint32_t f = e2m1x8(a);
+        const uint32_t d0 = f & 0xFu, d1 = (f >> 4) & 0xFu, m0 = (f >> 8) & 0xFu, m1 = (f >> 12) & 0xFu;
+        n += (d1 < d0) ? 1u : 0u;
+        n += (m0 != (d0 | 0x8u) || m1 != (d1 | 0x8u)) ? 1u : 0u;
+    }
+    if (n) atomicAdd(bad, n);
+}
+
 int launch_encoder_breakpoints(uint32_t* out, cudaStream_t st) {
     encoder_breakpoints_kernel<<<1, 288, 0, st>>>(out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    encoder_monotone_kernel<<<sm_count() * 8, 256, 0, st>>>(out + 266);
     return (int)cudaGetLastError();
 }
 

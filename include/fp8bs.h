@@ -442,11 +442,16 @@ int fp8bs_test_quotient_sweep(unsigned long long* counts, int nvfp4, fp8bs_strea
  * has magnitude >= c.  A one-CTA kernel finds them by binary search over
  * the float32 bit patterns, through the same packed casts the quantisers
  * use, for both signs.
- *   out  DEVICE uint32[266]: out[s*126 + c-1] (s = 0 positive, 1 negative,
+ *   out  DEVICE uint32[267]: out[s*126 + c-1] (s = 0 positive, 1 negative,
  *        c = 1..126) the E4M3 breakpoints' float32 bits (magnitude);
  *        out[252 + s*7 + c-1] (c = 1..7) the E2M1 ones.  An entry is
  *        0xFFFFFFFF if the lanes of a packed cast disagreed or a code had
- *        the wrong sign.
+ *        the wrong sign.  out[266], zero-filled by the caller, receives the
+ *        count of violations of monotonicity (the code magnitude of the
+ *        successor of every finite positive float32 bit pattern is at least
+ *        its own) and of symmetry (the code of -x is that of x with the sign
+ *        bit set), for both casts over all 2^31 patterns; with the
+ *        breakpoints this fixes the casts on every finite float32.
  * FP8BS_EINVAL for NULL, FP8BS_EALIGN if out is not 4-byte aligned.
  */
 int fp8bs_test_encoder_breakpoints(uint32_t* out, fp8bs_stream_t stream);

@@ -300,9 +300,13 @@ def test_encoder_breakpoints_match_the_oracle():
     code.  The device finds, through the quantisers' own packed casts and for
     both signs, the smallest float32 magnitude giving each nonzero code
     magnitude (E4M3: 126, E2M1: 7); the oracle's encoder must give exactly
-    that code there and the code below it one float32 step lower.  Together
-    that is the comparison over all float32 inputs, code by code."""
-    bp = fp.test_encoder_breakpoints()
+    that code there and the code below it one float32 step lower.  The
+    device also checks that both casts are monotone and sign-symmetric over
+    all 2^31 finite magnitudes; with equal breakpoints that makes them the
+    oracle's casts on every finite float32."""
+    out = fp.test_encoder_breakpoints()
+    bp, violations = out[:266], out[266]
+    assert violations == 0                       # monotone and sign-symmetric on every finite float32
     assert 0xFFFFFFFF not in bp                  # lanes agreed, signs right
     sections = ((0, 126, OF.e4m3_encode, 0x7F, 1.0), (126, 126, OF.e4m3_encode, 0x7F, -1.0),
                 (252, 7, OF.e2m1_encode, 0x7, 1.0), (259, 7, OF.e2m1_encode, 0x7, -1.0))
