@@ -60,7 +60,8 @@ def parse():
                     choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
                              "quant_per_tensor", "quant_nvfp4", "quant_nvfp4_row_4over6", "dequant_1x128",
                              "moe_gate_up", "moe_gather_quant",
-                             "moe_swiglu_quant", "moe_quant_then_gather", "moe_layer", "nvfp4"],
+                             "moe_swiglu_quant", "moe_quant_then_gather", "moe_layer", "nvfp4",
+                             "mma_peak_e4m3", "mma_peak_mxfp8", "mma_peak_nvfp4"],
                     help="run only this piece of the path W+K times (for profiler captures); prints its time")
     return ap.parse_args()
 
@@ -833,6 +834,15 @@ def single_kernel(args, torch, fp, dev):
         fn = lambda: fp.fp8_grouped_gemm(qa, sa, qb.view(128, 1536, 2048), sb.view(128, 1536, 64), off,  # noqa: E731
                                          "mxfp8", out=out, ws=ws)
         work = 2 * rows * 1536 * 2048
+    elif name.startswith("mma_peak"):
+        # the tensor-core throughput loop behind the measured FP8 / FP4 peaks
+        kind = {"mma_peak_e4m3": 0, "mma_peak_mxfp8": 1, "mma_peak_nvfp4": 2}[name]
+        flop = [0]
+
+        def fn():
+            flop[0] = fp.mma_peak(kind, 256, 8192)
+        fn()
+        work = flop[0]
     else:  # nvfp4
         m, n, k = 16384, 27648, 5120
         qx, sx, tx = fp.fp8_quantize(act((m, k), 0.0, 1.0), "nvfp4", ws=ws)
