@@ -806,33 +806,47 @@ quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols
 
 // ---------------------------------------------------------------- transposed (+ optional row-wise), TMA-fed
 // 1x128, 1x128 with power-of-two scales, and MXFP8: a scale per column of X
-// (per row of X^T) and another per row of X.
-// Persistent CTAs of 256 threads, three per SM.  A 2-stage ring of 128x128
-// BF16 tiles (32 KB each) per CTA is filled by TMA ahead of the compute, so the
-// loads of later tiles are in flight while a tile is quantised.  Per tile:
-//   column pass (codes of X^T): thread t owns columns 2(t%64), 2(t%64)+1 and
-//     rows 32(t/64) .. +31 -- 4-byte reads, a warp reads 128 contiguous bytes
-//     of a row; one sweep for the amax, one for the codes (kept in
-//     registers).  Column amaxes of the four row quarters meet in shared
-//     memory (1x128), a row quarter is one 1x32 group (MXFP8).
-//   row pass (row-wise codes of X, dual mode): a half-warp owns a row, 16
-//     lanes x 8 columns, so each 16-byte read and each 8-byte code store of a
-//     warp covers two whole rows; group amaxes are xor-shuffles.
-//   X^T out: once every thread has read the BF16 values, the column codes go
-//     into the consumed stage as a [column][row] byte tile (16-byte chunks
-//     XOR-swizzled by column/2, so a quarter-warp's stores hit 8 different
-//     bank groups) and leave as whole 128-byte rows of X^T.
-// A tile's stage is refilled once every thread has passed the CTA barrier
-// that ends the tile (generic-proxy accesses, then an async-proxy fence).
+// (per row of X^T) and, in dual mode, another per row of X.
+// Persistent CTAs of 256 threads, three per SM (two for the dual
+// power-of-two forms, kTileCtas).  A 2-stage ring of 128x128
+// BF16 tiles (32 KB each) per CTA is filled by TMA ahead of the compute, so
+// the load of the next tile is in flight while a tile is quantised.
+// Thread t holds an 8 x 8 block of the tile in registers, read as eight
+// 16-byte shared-memory loads: columns 8*(t%16) .. +7 of rows 8*(t/16) ..
+// +7, so a warp holds 16 whole rows and a half-warp 8.  From the registers:
+//   column pass (codes of X^T): column maxima over the thread's 8 rows,
+//     over the warp's 16 by one shuffle, then over the tile's 128 rows
+//     (1x128: the eight warps' maxima meet in shared memory and each
+//     column's scale is computed once) or over a 32-row group (MXFP8: two
+//     warps).  Codes of two rows of a column per float32-pair instruction;
+//     a column's 8 codes go into the consumed stage as 8 bytes of a
+//     [column][row] byte tile (16-byte chunks XOR-swizzled by column/8, so
+//     a warp's stores spread over all banks) and leave as whole 128-byte
+//     rows of X^T.
+//   row pass (row-wise codes of X, dual mode): a row's 128 columns lie in
+//     the 16 lanes of a half-warp.  A transposing butterfly of shuffles
+//     leaves each lane pair with the maximum of one of the half-warp's 8
+//     rows (1x128), or each lane with two rows of its 32-column group
+//     (MXFP8); the scales come back through shared memory (1x128) or
+//     shuffles (MXFP8).  Codes of two adjacent columns per float32-pair
+//     instruction; a half-warp stores whole 128-byte row segments.
+// Every thread fences its generic accesses to a stage at the end of the
+// tile; the stage is refilled once every thread has passed the barrier that
+// opens the next tile.
 constexpr int kTileThreads = 256;
 constexpr int kTileStages = 2;
+// CTAs per SM: three, except for the dual power-of-two forms (MXFP8, 1x128
+// power of two), which spill at three CTAs' register share (80) and run
+// faster at two (MXFP8 dual [8192, 4096]: 32.8 against 30.7 us).
+template <int GRAN, bool DUAL> constexpr int kTileCtas = (kPow2<GRAN> && DUAL) ? 2 : 3;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;
 
 struct TileShared {
     uint32_t tile[kTileStages][128 * 64];   // BF16 pairs, row pitch 64 words
-    uint2 red[4][64];                        // column-pair amax of each row quarter
+    uint4 red[8][16];          // per warp and 8-column group: |x| maxima (BF16 bit pairs) over the warp's 16 rows
+    float2 csr[128];           // per column of the tile: S (or 2^-e) and RN(1/S), 0 off the fast path
+    float2 rsr[8][16];         // per warp and row (1x128 rows, dual): the same
     uint64_t full[kTileStages];
-    int abort;
 };
 constexpr size_t kTileSmem = sizeof(TileShared) + 1024;
 
@@ -849,253 +863,308 @@ __device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, int* st
     }
 }
 
-// x / S (FP32 grans) or x * 2^-e (power-of-two grans) for two BF16 values
-// packed in `word`; d0, d1 carry S (and its reciprocal) or 2^-e in .s.
-// FAST: both divisors take the correction step (the caller tested .fast).
-template <int GRAN, bool FAST = false>
-__device__ __forceinline__ float2 tile_scaled2(uint32_t word, const ScaleDiv& d0, const ScaleDiv& d1) {
-    const float a = bf16_lo(word), b = bf16_hi(word);
-    if constexpr (kPow2<GRAN>) return make_float2(__fmul_rn(a, d0.s), __fmul_rn(b, d1.s));
-    if constexpr (FAST) return make_float2(div_fast(a, d0), div_fast(b, d1));
-    return make_float2(div_scale(a, d0), div_scale(b, d1));
+// Eight E4M3 codes of two float32 pairs each of two values: x / S by the
+// correction step (FP32 scale S, r = RN(1/S)) or x * m (power of two, m in s).
+template <bool P2>
+__device__ __forceinline__ uint2 codes8_fast(uint64_t x01, uint64_t x23, uint64_t x45, uint64_t x67, float s, float r) {
+    if constexpr (P2) {
+        const uint64_t m2 = pair_f32(s, s);
+        return make_uint2(e4m3x4_mul2(x01, x23, m2), e4m3x4_mul2(x45, x67, m2));
+    } else {
+        const ScaleDiv2 d = scale_div2(ScaleDiv{s, r, true});
+        return make_uint2(e4m3x4_div_fast2(x01, x23, d), e4m3x4_div_fast2(x45, x67, d));
+    }
+}
+
+// The same eight codes of x / S for a group off the fast path (r = 0: IEEE
+// division; an all-zero or tiny group), out of line: such groups are rare.
+__device__ __noinline__ uint2 codes8_slow(uint64_t x01, uint64_t x23, uint64_t x45, uint64_t x67, float s, float r) {
+    const ScaleDiv d{s, r, r != 0.0f};
+    float f[8];
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f[0]), "=f"(f[1]) : "l"(x01));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f[2]), "=f"(f[3]) : "l"(x23));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f[4]), "=f"(f[5]) : "l"(x45));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f[6]), "=f"(f[7]) : "l"(x67));
+    return make_uint2(e4m3x4(div_scale(f[0], d), div_scale(f[1], d), div_scale(f[2], d), div_scale(f[3], d)),
+                      e4m3x4(div_scale(f[4], d), div_scale(f[5], d), div_scale(f[6], d), div_scale(f[7], d)));
 }
 
 template <int GRAN, bool DUAL>
-__global__ void __launch_bounds__(kTileThreads, 3)
+__global__ void __launch_bounds__(kTileThreads, kTileCtas<GRAN, DUAL>)
 quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, int64_t cols,
                       uint8_t* __restrict__ qt, void* __restrict__ st,
                       uint8_t* __restrict__ q, void* __restrict__ s, int* status) {
     static_assert(GRAN == kGranTok || GRAN == kGranTokP2 || GRAN == kGranMx, "per-column scales only");
+    constexpr bool kMxG = GRAN == kGranMx;
+    constexpr bool kP2 = kPow2<GRAN>;     // MXFP8 and 1x128 power of two: codes by multiplication
+    constexpr uint32_t kFull = 0xFFFFFFFFu;
     extern __shared__ uint8_t tile_smem_raw[];
     TileShared& sh = *reinterpret_cast<TileShared*>((reinterpret_cast<uintptr_t>(tile_smem_raw) + 1023) &
                                                     ~uintptr_t(1023));
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int64_t tiles_c = ceil_div(cols, 128), tiles_r = ceil_div(rows, 128);
-    const int64_t ntiles = tiles_c * tiles_r;
+    const int cg = lane & 15, half = lane >> 4, rg = 2 * w + half;   // the thread's 8-column and 8-row groups
+    // rows < 2^23 (at most 65535 row tiles); column tiles < 2^31
+    const int tiles_c = (int)ceil_div(cols, 128), tiles_r = (int)ceil_div(rows, 128);
+    const int nrows = (int)rows;
+    const int64_t ntiles = (int64_t)tiles_c * tiles_r;
+    // The CTA's tiles are t = blockIdx.x + i * gridDim.x, walked as (row tile,
+    // column tile) cursors: one for the loads (thread 0), one for the compute.
+    const int step_r = (int)(gridDim.x / (unsigned)tiles_c), step_c = (int)(gridDim.x % (unsigned)tiles_c);
+    auto advance = [&](int& rt_, int& ct_) {
+        ct_ += step_c;
+        rt_ += step_r;
+        if (ct_ >= tiles_c) {
+            ct_ -= tiles_c;
+            ++rt_;
+        }
+    };
+    int rt = (int)(blockIdx.x / (unsigned)tiles_c), ct = (int)(blockIdx.x % (unsigned)tiles_c);
+    int lrt = rt, lct = ct;
 
     if (tid == 0) {
         for (int k = 0; k < kTileStages; ++k) mbar_init(smem_u32(&sh.full[k]), 1);
-        sh.abort = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
     }
     __syncthreads();
     int64_t issued = 0;     // tiles whose load thread 0 has issued
-    auto issue = [&](int64_t i) {  // i-th tile of this CTA into stage i % kTileStages
-        const int64_t t = blockIdx.x + i * (int64_t)gridDim.x;
-        const int64_t rt = t / tiles_c, ct = t - rt * tiles_c;
+    auto issue = [&](int64_t i) {  // the next tile of this CTA into stage i % kTileStages
         const uint32_t bar = smem_u32(&sh.full[i % kTileStages]);
         mbar_arrive_expect_tx(bar, kTileBytes);
-        tma_load_2d(smem_u32(sh.tile[i % kTileStages]), &tm_x, bar, (int32_t)(ct * 128), (int32_t)(rt * 128));
+        tma_load_2d(smem_u32(sh.tile[i % kTileStages]), &tm_x, bar, lct * 128, lrt * 128);
+        advance(lrt, lct);
     };
     const int64_t mine = (ntiles > blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     if (tid == 0) {
         for (; issued < mine && issued < kTileStages; ++issued) issue(issued);
     }
 
-    const int cp = tid & 63, rq = tid >> 6;        // column pass
     int64_t consumed = 0;   // tiles whose load has been waited for
     for (int64_t i = 0; i < mine; ++i) {
         const int stg = (int)(i % kTileStages);
         const bool got = tile_wait(smem_u32(&sh.full[stg]), (uint32_t)((i / kTileStages) & 1), status);
         if (!__syncthreads_and(got)) break;
         consumed = i + 1;
-        const int64_t t = blockIdx.x + i * (int64_t)gridDim.x;
-        const int64_t rt = t / tiles_c, ct = t - rt * tiles_c;
-        const int64_t r0 = rt * 128, c0 = ct * 128;
-        const uint32_t* tile = sh.tile[stg];
-
-        // ---------------- column pass, sweep 1: amax of columns 2cp, 2cp+1 over rows 32rq..+31
-        const uint32_t* colp = tile + (32 * rq) * 64 + cp;
-        uint32_t mm = 0;   // |x| bits of both columns, 16 bits each
-#pragma unroll
-        for (int k = 0; k < 32; ++k) mm = __vmaxu2(mm, colp[k * 64] & 0x7FFF7FFFu);
-        uint32_t m0 = mm & 0xFFFFu, m1 = mm >> 16;
-        float d0 = 1.0f, d1 = 1.0f;       // divisors (FP32 scales) or multipliers (power-of-two scales)
-        int e0 = 0, e1 = 0;
-        ScaleDiv tok0{}, tok1{};          // 1x128: the scales with their reciprocals
-        if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
-            sh.red[rq][cp] = make_uint2(m0, m1);
-            __syncthreads();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint2 o = sh.red[k][cp];
-                m0 = max(m0, o.x);
-                m1 = max(m1, o.y);
-            }
-            if constexpr (GRAN == kGranTok) {
-                tok0 = scale_div_from_amax(amax_bits_to_f32(m0));
-                tok1 = scale_div_from_amax(amax_bits_to_f32(m1));
-                d0 = tok0.s;
-                d1 = tok1.s;
-            } else {
-                e0 = mx_exponent_from_amax_bits(m0 << 16);
-                e1 = mx_exponent_from_amax_bits(m1 << 16);
-                d0 = exp2_neg(e0);
-                d1 = exp2_neg(e1);
-            }
-        } else {   // MXFP8: a row quarter is one 1x32 group of X^T
-            e0 = mx_exponent_from_amax_bits(m0 << 16);
-            e1 = mx_exponent_from_amax_bits(m1 << 16);
-            d0 = exp2_neg(e0);
-            d1 = exp2_neg(e1);
-        }
-        // ---------------- column pass, sweep 2: codes of X^T into registers (4 rows per word)
-        const ScaleDiv sd0 = kPow2<GRAN> ? ScaleDiv{d0, 0.0f, false} : tok0;
-        const ScaleDiv sd1 = kPow2<GRAN> ? ScaleDiv{d1, 0.0f, false} : tok1;
-        uint32_t c0w[8], c1w[8];
-        auto col_codes = [&](auto fast) {
-            [[maybe_unused]] constexpr bool F = decltype(fast)::value;
-            if constexpr (kPow2<GRAN>) {   // x * 2^-e, four rows of each column as two pairs
-                const uint64_t m0 = pair_f32(sd0.s, sd0.s), m1 = pair_f32(sd1.s, sd1.s);
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const uint32_t wa = colp[k * 64], wb = colp[(k + 1) * 64];
-                    const uint32_t wc = colp[(k + 2) * 64], wd = colp[(k + 3) * 64];
-                    c0w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), m0);
-                    c1w[k >> 2] = e4m3x4_mul2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), m1);
-                }
-            } else if constexpr (F) {   // four rows of each of the two columns as two pairs each
-                const ScaleDiv2 e0 = scale_div2(sd0), e1 = scale_div2(sd1);
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const uint32_t wa = colp[k * 64], wb = colp[(k + 1) * 64];
-                    const uint32_t wc = colp[(k + 2) * 64], wd = colp[(k + 3) * 64];
-                    c0w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_lo(wa), bf16_lo(wb)), pair_f32(bf16_lo(wc), bf16_lo(wd)), e0);
-                    c1w[k >> 2] = e4m3x4_div_fast2(pair_f32(bf16_hi(wa), bf16_hi(wb)), pair_f32(bf16_hi(wc), bf16_hi(wd)), e1);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const float2 a = tile_scaled2<GRAN, F>(colp[k * 64], sd0, sd1);
-                    const float2 b = tile_scaled2<GRAN, F>(colp[(k + 1) * 64], sd0, sd1);
-                    const float2 c = tile_scaled2<GRAN, F>(colp[(k + 2) * 64], sd0, sd1);
-                    const float2 d = tile_scaled2<GRAN, F>(colp[(k + 3) * 64], sd0, sd1);
-                    c0w[k >> 2] = e4m3x4(a.x, b.x, c.x, d.x);
-                    c1w[k >> 2] = e4m3x4(a.y, b.y, c.y, d.y);
-                }
-            }
-        };
-        if (!kPow2<GRAN> && sd0.fast && sd1.fast) col_codes(std::true_type{});
-        else col_codes(std::false_type{});
-        // scales of X^T ([cols, *] grid)
-        {
-            const int64_t rbase = r0 + 32 * rq;
-            if constexpr (GRAN == kGranTok || GRAN == kGranTokP2) {
-                if (rq == 0) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int64_t c = c0 + 2 * cp + j;
-                        if (c < cols) {
-                            if constexpr (GRAN == kGranTok) static_cast<float*>(st)[c * tiles_r + rt] = j ? d1 : d0;
-                            else static_cast<uint8_t*>(st)[c * tiles_r + rt] = (uint8_t)((j ? e1 : e0) + 127);
-                        }
-                    }
-                }
-            } else {
-                const int64_t nrb = ceil_div(rows, 32);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int64_t c = c0 + 2 * cp + j;
-                    if (c < cols && rbase < rows)
-                        static_cast<uint8_t*>(st)[c * nrb + (rbase >> 5)] = (uint8_t)((j ? e1 : e0) + 127);
-                }
-            }
-        }
-
-        // ---------------- row pass: row-wise codes of X.  A half-warp owns a
-        // row (16 lanes x 8 columns), so every 16-byte read and every 8-byte
-        // store of a warp covers two whole rows.
-        if constexpr (DUAL) {
-            const int ch = lane & 15;
-            const int64_t ncb = ceil_div(cols, GRAN == kGranMx ? 32 : 128);
-#pragma unroll 2
-            for (int it2 = 0; it2 < 8; ++it2) {
-                const int rloc = 16 * w + 2 * it2 + (lane >> 4);
-                const int64_t r = r0 + rloc;
-                const uint4 v = *reinterpret_cast<const uint4*>(tile + rloc * 64 + ch * 4);
-                const uint32_t a = absmax_v4(v);
-                float dd;
-                int ee = 0;
-                ScaleDiv tokd{};
-                if constexpr (GRAN == kGranMx) {
-                    ee = mx_exponent_from_amax_bits(warp_max_u32(a, 4) << 16);
-                    dd = exp2_neg(ee);
-                } else {
-                    const uint32_t m = warp_max_u32(a, 16);
-                    if constexpr (GRAN == kGranTok) {
-                        tokd = scale_div_from_amax(amax_bits_to_f32(m));
-                        dd = tokd.s;
-                    } else {
-                        ee = mx_exponent_from_amax_bits(m << 16);
-                        dd = exp2_neg(ee);
-                    }
-                }
-                const int64_t c = c0 + 8 * ch;
-                const ScaleDiv sdd = kPow2<GRAN> ? ScaleDiv{dd, 0.0f, false} : tokd;
-                if (r < rows) {
-                    if (c < cols) {
-                        auto row_codes = [&](auto fast) {
-                            constexpr bool F = decltype(fast)::value;
-                            if constexpr (kPow2<GRAN>) {
-                                const uint64_t m2 = pair_f32(sdd.s, sdd.s);
-                                return make_uint2(e4m3x4_mul2(pair_bf16(v.x), pair_bf16(v.y), m2),
-                                                  e4m3x4_mul2(pair_bf16(v.z), pair_bf16(v.w), m2));
-                            } else if constexpr (F) {
-                                const ScaleDiv2 e2 = scale_div2(sdd);
-                                return make_uint2(e4m3x4_div_fast2(pair_bf16(v.x), pair_bf16(v.y), e2),
-                                                  e4m3x4_div_fast2(pair_bf16(v.z), pair_bf16(v.w), e2));
-                            }
-                            const float2 x0 = tile_scaled2<GRAN, F>(v.x, sdd, sdd);
-                            const float2 x1 = tile_scaled2<GRAN, F>(v.y, sdd, sdd);
-                            const float2 x2 = tile_scaled2<GRAN, F>(v.z, sdd, sdd);
-                            const float2 x3 = tile_scaled2<GRAN, F>(v.w, sdd, sdd);
-                            return make_uint2(e4m3x4(x0.x, x0.y, x1.x, x1.y), e4m3x4(x2.x, x2.y, x3.x, x3.y));
-                        };
-                        *reinterpret_cast<uint2*>(q + r * cols + c) =
-                            (!kPow2<GRAN> && sdd.fast) ? row_codes(std::true_type{}) : row_codes(std::false_type{});
-                    }
-                    if constexpr (GRAN == kGranMx) {
-                        if ((ch & 3) == 0 && c < cols) static_cast<uint8_t*>(s)[r * ncb + (c >> 5)] = (uint8_t)(ee + 127);
-                    } else if constexpr (GRAN == kGranTok) {
-                        if (ch == 0) static_cast<float*>(s)[r * ncb + ct] = dd;
-                    } else if constexpr (GRAN == kGranTokP2) {
-                        if (ch == 0) static_cast<uint8_t*>(s)[r * ncb + ct] = (uint8_t)(ee + 127);
-                    }
-                }
-            }
-        }
-
-        // ---------------- X^T codes: through the consumed stage as a [column][row]
-        // byte tile (16-byte chunks XOR-swizzled by column/2), then out as
-        // whole 128-byte rows of X^T
-        __syncthreads();   // every read of the BF16 values is done
-        {
-            uint8_t* ct8 = reinterpret_cast<uint8_t*>(sh.tile[stg]);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = 2 * cp + j;
-                const uint32_t* cw = j ? c1w : c0w;
-                const int sw = (col >> 1) & 7;
-                *reinterpret_cast<uint4*>(ct8 + col * 128 + 16 * ((2 * rq) ^ sw)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                *reinterpret_cast<uint4*>(ct8 + col * 128 + 16 * ((2 * rq + 1) ^ sw)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-                const int xr = (tid >> 3) + 32 * pass, k = tid & 7;   // row of X^T within the tile, 16-byte chunk
-                const int64_t c = c0 + xr;
-                if (c < cols && r0 + 16 * k < rows)
-                    *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) =
-                        *reinterpret_cast<const uint4*>(ct8 + xr * 128 + 16 * (k ^ ((xr >> 1) & 7)));
-            }
-        }
-        __syncthreads();   // every read of this stage (and of red) is done
-        if (tid == 0 && issued < mine) {
-            fence_proxy_async_smem();
+        // every thread is done with the previous tile's stage: refill it
+        if (tid == 0 && i > 0 && issued < mine) {
             issue(issued);
             ++issued;
         }
+        const int r0 = rt * 128, rbase = r0 + 8 * rg;                           // the thread's first row
+        const int64_t c0 = (int64_t)ct * 128, cbase = c0 + 8 * cg;             // and first column
+        uint32_t* tile = sh.tile[stg];
+
+        // ---------------- the thread's 8 x 8 block: x[k][j] = columns 2j, 2j+1 of row k
+        uint32_t x[8][4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + (8 * rg + k) * 64 + 4 * cg);
+            x[k][0] = v.x;
+            x[k][1] = v.y;
+            x[k][2] = v.z;
+            x[k][3] = v.w;
+        }
+        // |x| maxima as BF16 bit pairs (non-negative patterns order like their
+        // values): per column pair over the 8 rows, per row over the 8 columns
+        uint32_t cm[4] = {0u, 0u, 0u, 0u}, rm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t a0 = x[k][0] & 0x7FFF7FFFu, a1 = x[k][1] & 0x7FFF7FFFu;
+            const uint32_t a2 = x[k][2] & 0x7FFF7FFFu, a3 = x[k][3] & 0x7FFF7FFFu;
+            cm[0] = __vmaxu2(cm[0], a0);
+            cm[1] = __vmaxu2(cm[1], a1);
+            cm[2] = __vmaxu2(cm[2], a2);
+            cm[3] = __vmaxu2(cm[3], a3);
+            rm[k] = __vmaxu2(__vmaxu2(a0, a1), __vmaxu2(a2, a3));
+        }
+        // column maxima over the warp's 16 rows (both halves end with them)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(kFull, cm[j], 16));
+        if (half == 0) sh.red[w][cg] = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+
+        // ---------------- row pass: row-wise codes of X
+        if constexpr (DUAL) {
+            // row k's 8 values as float32 pairs (columns 2j, 2j+1)
+            auto row_codes = [&](int k, float sv, float rv, bool fast) -> uint2 {
+                if (kP2 || fast) return codes8_fast<kP2>(pair_bf16(x[k][0]), pair_bf16(x[k][1]), pair_bf16(x[k][2]),
+                                                          pair_bf16(x[k][3]), sv, rv);
+                return codes8_slow(pair_bf16(x[k][0]), pair_bf16(x[k][1]), pair_bf16(x[k][2]), pair_bf16(x[k][3]), sv, rv);
+            };
+            const bool cols_in = cbase < cols;
+            if constexpr (!kMxG) {
+                // Transposing butterfly over the half-warp: each step halves the
+                // rows a lane keeps and doubles the lanes they are reduced over.
+                // At the end lanes 2p and 2p + 1 hold row p, p = 4 b3 + 2 b2 + b1.
+                const bool b3 = (lane & 8) != 0, b2 = (lane & 4) != 0, b1 = (lane & 2) != 0;
+                uint32_t m4[4], m2[2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t send = b3 ? rm[k] : rm[4 + k], keep = b3 ? rm[4 + k] : rm[k];
+                    m4[k] = __vmaxu2(keep, __shfl_xor_sync(kFull, send, 8));
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t send = b2 ? m4[k] : m4[2 + k], keep = b2 ? m4[2 + k] : m4[k];
+                    m2[k] = __vmaxu2(keep, __shfl_xor_sync(kFull, send, 4));
+                }
+                uint32_t m1 = __vmaxu2(b1 ? m2[1] : m2[0], __shfl_xor_sync(kFull, b1 ? m2[0] : m2[1], 2));
+                m1 = __vmaxu2(m1, __shfl_xor_sync(kFull, m1, 1));
+                const uint32_t m = max(m1 & 0xFFFFu, m1 >> 16);
+                const int p = (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0);
+                const int r = rbase + p;
+                float sv, rv = 0.0f;
+                if constexpr (GRAN == kGranTok) {
+                    const ScaleDiv sd = scale_div_from_amax(amax_bits_to_f32(m));
+                    sv = sd.s;
+                    rv = sd.fast ? sd.r : 0.0f;
+                    if ((lane & 1) == 0 && r < nrows) static_cast<float*>(s)[(int64_t)r * tiles_c + ct] = sv;
+                } else {
+                    const int e = mx_exponent_from_amax_bits(m << 16);
+                    sv = exp2_neg(e);
+                    if ((lane & 1) == 0 && r < nrows) static_cast<uint8_t*>(s)[(int64_t)r * tiles_c + ct] = (uint8_t)(e + 127);
+                }
+                if ((lane & 1) == 0) sh.rsr[w][8 * half + p] = make_float2(sv, rv);
+                const bool warp_fast = __all_sync(kFull, kP2 || rv != 0.0f);   // the warp's 16 rows
+                __syncwarp();
+                auto rows_out = [&](auto fast) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float2 sr = sh.rsr[w][8 * half + k];
+                        const int r = rbase + k;
+                        const uint2 o = row_codes(k, sr.x, sr.y, decltype(fast)::value || sr.y != 0.0f);
+                        if (r < nrows && cols_in) *reinterpret_cast<uint2*>(q + (int64_t)r * cols + cbase) = o;
+                    }
+                };
+                if (warp_fast) rows_out(std::true_type{});
+                else rows_out(std::false_type{});
+            } else {
+                // MXFP8: a 32-column group is 4 lanes (lane bits 0 and 1).  After
+                // the butterfly lane j of the group holds rows 2j and 2j + 1.
+                const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+                uint32_t m4[4], m2[2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t send = b1 ? rm[k] : rm[4 + k], keep = b1 ? rm[4 + k] : rm[k];
+                    m4[k] = __vmaxu2(keep, __shfl_xor_sync(kFull, send, 2));
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t send = b0 ? m4[k] : m4[2 + k], keep = b0 ? m4[2 + k] : m4[k];
+                    m2[k] = __vmaxu2(keep, __shfl_xor_sync(kFull, send, 1));
+                }
+                const int p0 = (b1 ? 4 : 0) + (b0 ? 2 : 0);
+                const int64_t ncb = ceil_div(cols, 32);
+                const int64_t gcol = c0 + 32 * (cg >> 2);   // the group's first column
+                uint32_t packed = 0;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = mx_exponent_from_amax_bits(max(m2[k] & 0xFFFFu, m2[k] >> 16) << 16);
+                    packed |= (uint32_t)(e + 127) << (8 * k);
+                    const int r = rbase + p0 + k;
+                    if (r < nrows && gcol < cols) static_cast<uint8_t*>(s)[(int64_t)r * ncb + (gcol >> 5)] = (uint8_t)(e + 127);
+                }
+                uint32_t pk[4];   // biased exponents of rows 2j (bits 0..7) and 2j + 1 (bits 8..15)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) pk[j] = __shfl_sync(kFull, packed, (lane & ~3) | j);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = rbase + k;
+                    const float mk = exp2_neg((int)((pk[k >> 1] >> (8 * (k & 1))) & 0xFFu) - 127);
+                    const uint2 o = row_codes(k, mk, 0.0f, true);
+                    if (r < nrows && cols_in) *reinterpret_cast<uint2*>(q + (int64_t)r * cols + cbase) = o;
+                }
+            }
+        }
+
+        // ---------------- column scales
+        __syncthreads();   // red is complete, and every thread holds its block: the stage's BF16 data is dead
+        // MXFP8: column j's exponent from the group's maxima in cm
+        auto mx_col_exp = [&](int j) {
+            return mx_exponent_from_amax_bits(((j & 1) ? (cm[j >> 1] >> 16) : (cm[j >> 1] & 0xFFFFu)) << 16);
+        };
+        bool tile_fast = true;
+        if constexpr (kMxG) {
+            // this warp's and the other warp's maxima of the 32-row group (read
+            // back rather than kept in registers through the row pass)
+            const uint4 o0 = sh.red[w][cg], o1 = sh.red[w ^ 1][cg];
+            cm[0] = __vmaxu2(o0.x, o1.x);
+            cm[1] = __vmaxu2(o0.y, o1.y);
+            cm[2] = __vmaxu2(o0.z, o1.z);
+            cm[3] = __vmaxu2(o0.w, o1.w);
+            // X^T scales: one byte per column and 32-row group, from the group's first warp
+            if ((w & 1) == 0 && half == 0 && r0 + 16 * w < nrows) {
+                const int64_t nrb = ceil_div(rows, 32), rb = (r0 >> 5) + (w >> 1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (cbase + j < cols) static_cast<uint8_t*>(st)[(cbase + j) * nrb + rb] = (uint8_t)(mx_col_exp(j) + 127);
+            }
+        } else {
+            bool mine_fast = true;
+            if (tid < 64) {
+                // columns 2 tid and 2 tid + 1: word tid % 4 of 8-column group tid / 4
+                uint32_t mm = 0;
+#pragma unroll
+                for (int ww = 0; ww < 8; ++ww) mm = __vmaxu2(mm, reinterpret_cast<const uint32_t*>(&sh.red[ww][tid >> 2])[tid & 3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t mb = h ? (mm >> 16) : (mm & 0xFFFFu);
+                    const int cl = 2 * tid + h;
+                    const int64_t c = c0 + cl;
+                    if constexpr (GRAN == kGranTok) {
+                        const ScaleDiv sd = scale_div_from_amax(amax_bits_to_f32(mb));
+                        sh.csr[cl] = make_float2(sd.s, sd.fast ? sd.r : 0.0f);
+                        mine_fast = mine_fast && sd.fast;
+                        if (c < cols) static_cast<float*>(st)[c * tiles_r + rt] = sd.s;
+                    } else {
+                        const int e = mx_exponent_from_amax_bits(mb << 16);
+                        sh.csr[cl] = make_float2(exp2_neg(e), 0.0f);
+                        if (c < cols) static_cast<uint8_t*>(st)[c * tiles_r + rt] = (uint8_t)(e + 127);
+                    }
+                }
+            }
+            tile_fast = __syncthreads_and(mine_fast);   // the tile's column scales are in csr
+        }
+
+        // ---------------- X^T codes: the thread's 8 rows of each of its 8 columns,
+        // as 8 bytes of the [column][row] byte tile in the consumed stage
+        uint8_t* ct8 = reinterpret_cast<uint8_t*>(tile);
+        const int sw = cg & 7;   // = (column / 8) % 8 for all 8 columns
+        auto cols_out = [&](auto fast) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int jw = j >> 1;
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = (j & 1) ? bf16_hi(x[k][jw]) : bf16_lo(x[k][jw]);
+                float sv, rv = 0.0f;
+                if constexpr (kMxG) {
+                    sv = exp2_neg(mx_col_exp(j));
+                } else {
+                    const float2 sr = sh.csr[8 * cg + j];
+                    sv = sr.x;
+                    rv = sr.y;
+                }
+                const uint64_t p01 = pair_f32(v[0], v[1]), p23 = pair_f32(v[2], v[3]);
+                const uint64_t p45 = pair_f32(v[4], v[5]), p67 = pair_f32(v[6], v[7]);
+                uint2 o;
+                if (kP2 || decltype(fast)::value || rv != 0.0f) o = codes8_fast<kP2>(p01, p23, p45, p67, sv, rv);
+                else o = codes8_slow(p01, p23, p45, p67, sv, rv);
+                *reinterpret_cast<uint2*>(ct8 + (8 * cg + j) * 128 + 16 * (w ^ sw) + 8 * half) = o;
+            }
+        };
+        if (kP2 || tile_fast) cols_out(std::true_type{});
+        else cols_out(std::false_type{});
+        __syncthreads();   // the byte tile is complete
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int xr = (tid >> 3) + 32 * pass, k = tid & 7;   // row of X^T within the tile, 16-byte chunk
+            const int64_t c = c0 + xr;
+            if (c < cols && r0 + 16 * k < nrows)
+                *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) =
+                    *reinterpret_cast<const uint4*>(ct8 + xr * 128 + 16 * (k ^ ((xr >> 3) & 7)));
+        }
+        fence_proxy_async_smem();   // this thread's generic accesses to the stage come before its refill
+        advance(rt, ct);
     }
     // After an abort, copies issued but not yet waited for must land before
     // the CTA exits (each stage has at most one such copy).
@@ -1492,7 +1561,8 @@ int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int6
 }
 
 template <int GRAN, bool DUAL>
-static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int grid, cudaStream_t st) {
+static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int64_t tiles, cudaStream_t st) {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, kTileCtas<GRAN, DUAL> * (int64_t)sm_count()));
     static bool attr_set[64] = {false};   // one flag per kernel instantiation and device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1513,9 +1583,8 @@ static int launch_tile(const QuantJob& j, cudaStream_t st) {
     if (!make_tmap_b16(&tm, j.x, (uint64_t)j.cols, (uint64_t)j.rows, (uint64_t)j.ldx, 128, 128))
         return (int)cudaErrorInvalidValue;
     const int64_t tiles = ceil_div(j.cols, 128) * ceil_div(j.rows, 128);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, 3 * (int64_t)sm_count()));
-    if (j.q != nullptr) return launch_tile_k<GRAN, true>(tm, j, grid, st);
-    return launch_tile_k<GRAN, false>(tm, j, grid, st);
+    if (j.q != nullptr) return launch_tile_k<GRAN, true>(tm, j, tiles, st);
+    return launch_tile_k<GRAN, false>(tm, j, tiles, st);
 }
 
 template <int GRAN>
