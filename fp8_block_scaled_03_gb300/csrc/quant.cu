@@ -675,138 +675,12 @@ quant_block_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, i
     }
 }
 
-// ---------------------------------------------------------------- transposed, one scale per tile
-// Per-tensor, 128x128 and 128x128 with power-of-two scales: one scale covers
-// the whole 128x128 tile, so the codes of X and of X^T are the same numbers.
-// CTA tile: 128 rows x 128 columns of X, 512 threads, two CTAs per SM, the
-// tile held in registers.  Warp w owns rows 8w..8w+7, lane l owns columns
-// 4l..4l+3 (8-byte loads, 256 bytes per warp and row).  The codes of X^T are
-// staged in shared memory as a [column][row] byte tile (row pitch 136 bytes,
-// so the 8-byte stores of one warp spread over all banks) and leave as whole
-// 128-byte rows of X^T; the row-wise codes of X (dual mode) are computed
-// again from the registers and leave as 4-byte runs (128 bytes per warp and
-// row).  On GB300 this
-// kernel is faster than the TMA-fed one below for these granularities.
-constexpr int kRegTileThreads = 512;
-constexpr int kTPitch = 136;
-
-template <int GRAN, bool DUAL>
-__global__ void __launch_bounds__(kRegTileThreads, 2)
-quant_tile_reg_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
-                      uint8_t* __restrict__ qt, void* __restrict__ st,
-                      uint8_t* __restrict__ q, void* __restrict__ s,
-                      const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
-    static_assert(GRAN == kGranPT || GRAN == kGranBlk || GRAN == kGranBlkP2, "one scale per tile only");
-    __shared__ __align__(16) uint8_t tq[128 * kTPitch];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t rt = blockIdx.y, ct = blockIdx.x;
-    const int64_t r0 = rt * 128, c0 = ct * 128;
-    const int64_t cc = c0 + lane * 4;
-    const bool cok = cc < cols;
-    const int64_t rw = r0 + 8 * w;           // first row of this warp
-    const bool wok = rw < rows;              // rows % 16 == 0: 8 rows all valid or all not
-
-    float sc = 1.0f;                         // divisor (FP32 scales) or multiplier (power of two)
-    int e_blk = 0;
-    if constexpr (GRAN == kGranPT) {
-        if (given != nullptr) {
-            sc = *given;
-        } else {
-            sc = fp32_scale_from_amax(tensor_amax(partials, nparts));
-            if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-                static_cast<float*>(st)[0] = sc;
-                if (DUAL) static_cast<float*>(s)[0] = sc;
-            }
-        }
-    }
-
-    uint2 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v[i] = (cok && wok) ? ldg_v2(x + (rw + i) * ldx + cc) : make_uint2(0, 0);
-
-    if constexpr (GRAN == kGranBlk || GRAN == kGranBlkP2) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m = max(m, max(bf16x2_absmax_bits(v[i].x), bf16x2_absmax_bits(v[i].y)));
-        const uint32_t bm = block_max_u32(m);
-        if constexpr (GRAN == kGranBlk) {
-            sc = fp32_scale_from_amax(amax_bits_to_f32(bm));
-        } else {
-            e_blk = mx_exponent_from_amax_bits(bm << 16);
-            sc = exp2_neg(e_blk);
-        }
-    }
-
-    // Four codes of x / S (FP32 scales: the packed correction-step quotient
-    // when S came from an amax, the test taken once per thread; IEEE division
-    // for a supplied per-tensor S) or of x * 2^-e.
-    const ScaleDiv sd = kPow2<GRAN> ? ScaleDiv{sc, 0.0f, false} : scale_div(sc, given == nullptr);
-    const ScaleDiv2 sd2 = scale_div2(sd);
-    auto codes4 = [&](float a0, float a1, float a2, float a3, auto fast) -> uint32_t {
-        if constexpr (kPow2<GRAN>) return e4m3x4_mul2(pair_f32(a0, a1), pair_f32(a2, a3), pair_f32(sc, sc));
-        else if constexpr (decltype(fast)::value) return e4m3x4_div_fast2(pair_f32(a0, a1), pair_f32(a2, a3), sd2);
-        else return e4m3x4(__fdiv_rn(a0, sc), __fdiv_rn(a1, sc), __fdiv_rn(a2, sc), __fdiv_rn(a3, sc));
-    };
-
-    // ---- codes of column cc + j, rows rw .. rw+7 -> shared [column][row] tile
-    auto col_pass = [&](auto fast) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t word = (j < 2) ? v[i].x : v[i].y;
-                f[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
-            }
-            const uint2 o = make_uint2(codes4(f[0], f[1], f[2], f[3], fast), codes4(f[4], f[5], f[6], f[7], fast));
-            *reinterpret_cast<uint2*>(tq + (lane * 4 + j) * kTPitch + 8 * w) = o;
-        }
-    };
-    if (sd.fast) col_pass(std::true_type{});
-    else col_pass(std::false_type{});
-    __syncthreads();
-    // ---- whole rows of X^T: 128 columns x 128 bytes, 16 bytes per thread and pass
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-        const int t = threadIdx.x + pass * kRegTileThreads;
-        const int qc = t >> 3, k = t & 7;    // column of X (row of X^T), 16-byte chunk
-        const int64_t c = c0 + qc;
-        if (c < cols && r0 + 16 * k < rows) {
-            const uint8_t* src = tq + qc * kTPitch + 16 * k;
-            const uint2 lo = *reinterpret_cast<const uint2*>(src);
-            const uint2 hi = *reinterpret_cast<const uint2*>(src + 8);
-            *reinterpret_cast<uint4*>(qt + c * rows + r0 + 16 * k) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        }
-    }
-    if constexpr (GRAN == kGranBlk) {
-        if (threadIdx.x == 0) static_cast<float*>(st)[ct * gridDim.y + rt] = sc;
-    } else if constexpr (GRAN == kGranBlkP2) {
-        if (threadIdx.x == 0) static_cast<uint8_t*>(st)[ct * gridDim.y + rt] = (uint8_t)(e_blk + 127);
-    }
-
-    // ---- row-wise codes of X from the same registers
-    if constexpr (DUAL) {
-        auto row_pass = [&](auto fast) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t o = codes4(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y), fast);
-                if (cok && wok) *reinterpret_cast<uint32_t*>(q + (rw + i) * cols + cc) = o;
-            }
-        };
-        if (sd.fast) row_pass(std::true_type{});
-        else row_pass(std::false_type{});
-        if constexpr (GRAN == kGranBlk) {
-            if (threadIdx.x == 0) static_cast<float*>(s)[rt * gridDim.x + ct] = sc;
-        } else if constexpr (GRAN == kGranBlkP2) {
-            if (threadIdx.x == 0) static_cast<uint8_t*>(s)[rt * gridDim.x + ct] = (uint8_t)(e_blk + 127);
-        }
-    }
-}
-
 // ---------------------------------------------------------------- transposed (+ optional row-wise), TMA-fed
 // 1x128, 1x128 with power-of-two scales, and MXFP8: a scale per column of X
-// (per row of X^T) and, in dual mode, another per row of X.
+// (per row of X^T) and, in dual mode, another per row of X.  Per-tensor,
+// 128x128 and 128x128 with power-of-two scales: one scale covers the whole
+// 128x128 tile, so the codes of X and of X^T are the same bytes; each thread
+// casts its block once (by rows) and transposes the 8 x 8 bytes in registers.
 // Persistent CTAs of 256 threads, three per SM (two for the dual
 // power-of-two forms, kTileCtas).  A 2-stage ring of 128x128
 // BF16 tiles (32 KB each) per CTA is filled by TMA ahead of the compute, so
@@ -846,6 +720,7 @@ struct TileShared {
     uint4 red[8][16];          // per warp and 8-column group: |x| maxima (BF16 bit pairs) over the warp's 16 rows
     float2 csr[128];           // per column of the tile: S (or 2^-e) and RN(1/S), 0 off the fast path
     float2 rsr[8][16];         // per warp and row (1x128 rows, dual): the same
+    uint32_t tmax[8];          // one scale per tile: each warp's |x| maximum (BF16 bits)
     uint64_t full[kTileStages];
 };
 constexpr size_t kTileSmem = sizeof(TileShared) + 1024;
@@ -861,6 +736,17 @@ __device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, int* st
             return false;
         }
     }
+}
+
+// 4 x 4 byte transpose: a_k holds bytes (k, 0..3), c_j receives bytes (0..3, j).
+__device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t& c0,
+                                             uint32_t& c1, uint32_t& c2, uint32_t& c3) {
+    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);   // (0,0) (1,0) (0,1) (1,1); (0,2) ..
+    const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+    c0 = __byte_perm(t0, t2, 0x5410);
+    c1 = __byte_perm(t0, t2, 0x7632);
+    c2 = __byte_perm(t1, t3, 0x5410);
+    c3 = __byte_perm(t1, t3, 0x7632);
 }
 
 // Eight E4M3 codes of two float32 pairs each of two values: x / S by the
@@ -893,8 +779,10 @@ template <int GRAN, bool DUAL>
 __global__ void __launch_bounds__(kTileThreads, kTileCtas<GRAN, DUAL>)
 quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, int64_t cols,
                       uint8_t* __restrict__ qt, void* __restrict__ st,
-                      uint8_t* __restrict__ q, void* __restrict__ s, int* status) {
-    static_assert(GRAN == kGranTok || GRAN == kGranTokP2 || GRAN == kGranMx, "per-column scales only");
+                      uint8_t* __restrict__ q, void* __restrict__ s, int* status,
+                      const uint32_t* __restrict__ partials, int nparts, const float* __restrict__ given) {
+    constexpr bool kOne = GRAN == kGranPT || GRAN == kGranBlk || GRAN == kGranBlkP2;   // one scale per tile
+    static_assert(kOne || GRAN == kGranTok || GRAN == kGranTokP2 || GRAN == kGranMx, "transposed granularities");
     constexpr bool kMxG = GRAN == kGranMx;
     constexpr bool kP2 = kPow2<GRAN>;     // MXFP8 and 1x128 power of two: codes by multiplication
     constexpr uint32_t kFull = 0xFFFFFFFFu;
@@ -939,6 +827,24 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         for (; issued < mine && issued < kTileStages; ++issued) issue(issued);
     }
 
+    // Per-tensor: S from the amax partials (written out by one thread), or
+    // supplied (then divided by exactly, IEEE).
+    float pt_s = 1.0f, pt_r = 0.0f;
+    if constexpr (GRAN == kGranPT) {
+        ScaleDiv sd;
+        if (given != nullptr) {
+            sd = scale_div(*given, false);
+        } else {
+            sd = scale_div(fp32_scale_from_amax(tensor_amax(partials, nparts)), true);
+            if (blockIdx.x == 0 && tid == 0) {
+                static_cast<float*>(st)[0] = sd.s;
+                if constexpr (DUAL) static_cast<float*>(s)[0] = sd.s;
+            }
+        }
+        pt_s = sd.s;
+        pt_r = sd.fast ? sd.r : 0.0f;
+    }
+
     int64_t consumed = 0;   // tiles whose load has been waited for
     for (int64_t i = 0; i < mine; ++i) {
         const int stg = (int)(i % kTileStages);
@@ -964,6 +870,72 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
             x[k][2] = v.z;
             x[k][3] = v.w;
         }
+        uint8_t* ct8 = reinterpret_cast<uint8_t*>(tile);   // the consumed stage, later the [column][row] byte tile
+        const int sw = cg & 7;   // its 16-byte chunk swizzle: (column / 8) % 8, the same for the thread's 8 columns
+        if constexpr (kOne) {
+            // ---------------- one scale for the tile: the codes of X and of X^T are the same bytes
+            float sv = pt_s, rv = pt_r;
+            if constexpr (GRAN != kGranPT) {
+                uint32_t m2 = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) m2 = __vmaxu2(m2, x[k][j] & 0x7FFF7FFFu);
+                const uint32_t m = warp_max_u32(max(m2 & 0xFFFFu, m2 >> 16), 32);
+                if (lane == 0) sh.tmax[w] = m;
+            }
+            __syncthreads();   // every thread holds its block (the stage's BF16 data is dead); tmax is complete
+            if constexpr (GRAN != kGranPT) {
+                const uint4 t0 = *reinterpret_cast<const uint4*>(&sh.tmax[0]);
+                const uint4 t1 = *reinterpret_cast<const uint4*>(&sh.tmax[4]);
+                const uint32_t m = max(max(max(t0.x, t0.y), max(t0.z, t0.w)), max(max(t1.x, t1.y), max(t1.z, t1.w)));
+                if constexpr (GRAN == kGranBlk) {
+                    const ScaleDiv sd = scale_div_from_amax(amax_bits_to_f32(m));
+                    sv = sd.s;
+                    rv = sd.fast ? sd.r : 0.0f;
+                    if (tid == 0) {
+                        static_cast<float*>(st)[(int64_t)ct * tiles_r + rt] = sv;
+                        if constexpr (DUAL) static_cast<float*>(s)[(int64_t)rt * tiles_c + ct] = sv;
+                    }
+                } else {
+                    const int e = mx_exponent_from_amax_bits(m << 16);
+                    sv = exp2_neg(e);
+                    if (tid == 0) {
+                        static_cast<uint8_t*>(st)[(int64_t)ct * tiles_r + rt] = (uint8_t)(e + 127);
+                        if constexpr (DUAL) static_cast<uint8_t*>(s)[(int64_t)rt * tiles_c + ct] = (uint8_t)(e + 127);
+                    }
+                }
+            }
+            // codes of the thread's 8 rows (bytes 0..7 = its 8 columns)
+            uint2 rc[8];
+            auto rows_cast = [&](auto fast) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t p0 = pair_bf16(x[k][0]), p1 = pair_bf16(x[k][1]);
+                    const uint64_t p2 = pair_bf16(x[k][2]), p3 = pair_bf16(x[k][3]);
+                    if constexpr (kP2 || decltype(fast)::value) rc[k] = codes8_fast<kP2>(p0, p1, p2, p3, sv, rv);
+                    else rc[k] = codes8_slow(p0, p1, p2, p3, sv, rv);
+                }
+            };
+            if (kP2 || rv != 0.0f) rows_cast(std::true_type{});
+            else rows_cast(std::false_type{});
+            if constexpr (DUAL) {
+                if (cbase < cols) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (rbase + k < nrows) *reinterpret_cast<uint2*>(q + (int64_t)(rbase + k) * cols + cbase) = rc[k];
+                }
+            }
+            // the same bytes as 8 columns of 8 rows: an 8 x 8 byte transpose in four 4 x 4 blocks
+            uint32_t cl[8], chh[8];   // column j: rows 0..3, rows 4..7
+            transpose4x4(rc[0].x, rc[1].x, rc[2].x, rc[3].x, cl[0], cl[1], cl[2], cl[3]);
+            transpose4x4(rc[4].x, rc[5].x, rc[6].x, rc[7].x, chh[0], chh[1], chh[2], chh[3]);
+            transpose4x4(rc[0].y, rc[1].y, rc[2].y, rc[3].y, cl[4], cl[5], cl[6], cl[7]);
+            transpose4x4(rc[4].y, rc[5].y, rc[6].y, rc[7].y, chh[4], chh[5], chh[6], chh[7]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint2*>(ct8 + (8 * cg + j) * 128 + 16 * (w ^ sw) + 8 * half) = make_uint2(cl[j], chh[j]);
+        } else {
         // |x| maxima as BF16 bit pairs (non-negative patterns order like their
         // values): per column pair over the 8 rows, per row over the 8 columns
         uint32_t cm[4] = {0u, 0u, 0u, 0u}, rm[8];
@@ -1127,8 +1099,6 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
 
         // ---------------- X^T codes: the thread's 8 rows of each of its 8 columns,
         // as 8 bytes of the [column][row] byte tile in the consumed stage
-        uint8_t* ct8 = reinterpret_cast<uint8_t*>(tile);
-        const int sw = cg & 7;   // = (column / 8) % 8 for all 8 columns
         auto cols_out = [&](auto fast) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1154,6 +1124,7 @@ quant_tile_tma_kernel(const __grid_constant__ CUtensorMap tm_x, int64_t rows, in
         };
         if (kP2 || tile_fast) cols_out(std::true_type{});
         else cols_out(std::false_type{});
+        }
         __syncthreads();   // the byte tile is complete
 #pragma unroll
         for (int pass = 0; pass < 4; ++pass) {
@@ -1561,7 +1532,8 @@ int launch_quantize_rows_src(const QuantJob& j, const int64_t* token_index, int6
 }
 
 template <int GRAN, bool DUAL>
-static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int64_t tiles, cudaStream_t st) {
+static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int64_t tiles, cudaStream_t st,
+                         const uint32_t* partials, int nparts, const float* given) {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, kTileCtas<GRAN, DUAL> * (int64_t)sm_count()));
     static bool attr_set[64] = {false};   // one flag per kernel instantiation and device
     int dev = 0;
@@ -1573,31 +1545,21 @@ static int launch_tile_k(const CUtensorMap& tm, const QuantJob& j, int64_t tiles
         attr_set[dev] = true;
     }
     quant_tile_tma_kernel<GRAN, DUAL><<<grid, kTileThreads, kTileSmem, st>>>(
-        tm, j.rows, j.cols, j.qt, j.st, DUAL ? j.q : nullptr, DUAL ? j.s : nullptr, j.status);
+        tm, j.rows, j.cols, j.qt, j.st, DUAL ? j.q : nullptr, DUAL ? j.s : nullptr, j.status, partials, nparts, given);
     return (int)cudaGetLastError();
 }
 
 template <int GRAN>
-static int launch_tile(const QuantJob& j, cudaStream_t st) {
+static int launch_tile(const QuantJob& j, cudaStream_t st, const uint32_t* partials = nullptr, int nparts = 0,
+                       const float* given = nullptr) {
     CUtensorMap tm;
     if (!make_tmap_b16(&tm, j.x, (uint64_t)j.cols, (uint64_t)j.rows, (uint64_t)j.ldx, 128, 128))
         return (int)cudaErrorInvalidValue;
     const int64_t tiles = ceil_div(j.cols, 128) * ceil_div(j.rows, 128);
-    if (j.q != nullptr) return launch_tile_k<GRAN, true>(tm, j, tiles, st);
-    return launch_tile_k<GRAN, false>(tm, j, tiles, st);
+    if (j.q != nullptr) return launch_tile_k<GRAN, true>(tm, j, tiles, st, partials, nparts, given);
+    return launch_tile_k<GRAN, false>(tm, j, tiles, st, partials, nparts, given);
 }
 
-template <int GRAN>
-static int launch_tile_reg(const QuantJob& j, cudaStream_t st, int nparts, const float* given) {
-    const dim3 grid((unsigned)ceil_div(j.cols, 128), (unsigned)ceil_div(j.rows, 128));
-    if (j.q != nullptr)
-        quant_tile_reg_kernel<GRAN, true><<<grid, kRegTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st, j.q,
-                                                                          j.s, j.partials, nparts, given);
-    else
-        quant_tile_reg_kernel<GRAN, false><<<grid, kRegTileThreads, 0, st>>>(j.x, j.rows, j.cols, j.ldx, j.qt, j.st,
-                                                                           nullptr, nullptr, j.partials, nparts, given);
-    return (int)cudaGetLastError();
-}
 
 // Granularities with a scale per column of X (1x128, 1x32 groups of X^T's
 // rows) take the TMA-fed kernel; those with one scale per tile the
@@ -1608,14 +1570,14 @@ int launch_quantize_transposed(const QuantJob& j, cudaStream_t st) {
     case kGranTok: return launch_tile<kGranTok>(j, st);
     case kGranMx: return launch_tile<kGranMx>(j, st);
     case kGranTokP2: return launch_tile<kGranTokP2>(j, st);
-    case kGranBlk: return launch_tile_reg<kGranBlk>(j, st, 0, nullptr);
-    case kGranBlkP2: return launch_tile_reg<kGranBlkP2>(j, st, 0, nullptr);
+    case kGranBlk: return launch_tile<kGranBlk>(j, st);
+    case kGranBlkP2: return launch_tile<kGranBlkP2>(j, st);
     case kGranPT: {
         if (!j.given_scale) {
             const int e = launch_amax(j, st, &nparts);
             if (e) return e;
         }
-        return launch_tile_reg<kGranPT>(j, st, nparts, j.given_scale ? static_cast<const float*>(j.st) : nullptr);
+        return launch_tile<kGranPT>(j, st, j.partials, nparts, j.given_scale ? static_cast<const float*>(j.st) : nullptr);
     }
     default:
         return (int)cudaErrorInvalidValue;
