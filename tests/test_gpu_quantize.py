@@ -156,6 +156,56 @@ def test_zero_and_extreme_tensors(gran):
     check_rowwise(tiny, gran)
 
 
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("dual", [False, True])
+def test_zero_and_extreme_tensors_transposed(gran, dual):
+    """The transposed (and dual) path on all-zero tiles with a negative zero,
+    on values near float32's top and bottom, and on BF16 subnormals: the
+    tiles and columns whose scale leaves the reciprocal fast path."""
+    zeros = np.zeros((64, 256), dtype=np.uint16)
+    zeros[3, 7] = 0x8000
+    check_transposed(zeros, gran, dual)
+    g = np.random.Generator(np.random.PCG64(19))
+    extreme = np.where(g.random((64, 256)) < 0.5,
+                       synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(3e37)),
+                       synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(1e-38)))
+    check_transposed(extreme.astype(np.uint16), gran, dual)
+    tiny = synth.f32_to_bf16_bits(g.standard_normal((64, 256)).astype(np.float32) * np.float32(1e-39))
+    check_transposed(tiny, gran, dual)
+    # one tile of ordinary values beside a tile of subnormals, in the same rows and columns
+    mixed = synth.activations((128, 256), seed=20).copy()
+    mixed[:, 128:] = tiny[:64].repeat(2, axis=0)[:, :128]
+    check_transposed(mixed, gran, dual)
+
+
+def test_every_bf16_pattern_transposed():
+    """All finite BF16 patterns through the transposed and dual path (rows a
+    multiple of 16, as the transposed entry point requires)."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = allbits[(allbits & 0x7F80) != 0x7F80]
+    g = np.random.Generator(np.random.PCG64(21))
+    perm = finite[g.permutation(finite.size)]
+    n = (perm.size // (16 * 256)) * 16 * 256
+    parts = [perm[:n].reshape(-1, 256), np.resize(perm[n:], (16, 256))]
+    for bits in parts:
+        for gran in GRANS:
+            check_transposed(bits, gran, dual=True)
+
+
+def test_given_tensor_scale_transposed():
+    """A supplied per-tensor scale divides exactly (IEEE) on the transposed
+    path too, for X^T and X."""
+    bits = synth.activations((64, 256), seed=22)
+    x = to_f32(bits)
+    xd = to_dev_bf16(bits)
+    qt, st, q, s = fp.fp8_quantize_transposed(xd, "per_tensor", True,
+                                              scales_t=torch.tensor([0.125], dtype=torch.float32, device="cuda"),
+                                              flags=fp.FLAG_GIVEN_TENSOR_SCALE)
+    assert np.array_equal(np_u8(qt), OQ.cast_e4m3(np.ascontiguousarray(x.T), np.float32(0.125)))
+    assert np.array_equal(np_u8(q), OQ.cast_e4m3(x, np.float32(0.125)))
+    assert fp.read_status() == 0
+
+
 def test_every_bf16_pattern():
     """All 65536 BF16 bit patterns except inf/NaN, in several group contexts."""
     allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
