@@ -437,15 +437,15 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, in
 // ---------------------------------------------------------------- NVFP4 1x16 (row-wise)
 // "4. NVFP4 (Blackwell)": E2M1 codes in 1x16 blocks, an E4M3 block scale
 // s_b = E4M3((amax_b / 6) / S_g) and an outer float32 S_g (per tensor, or per
-// row for per-token activation scaling).  A lane owns 8 elements, so a block
-// is a lane pair (2j, 2j+1).
+// row for per-token activation scaling).  A lane owns whole blocks (two
+// 16-byte loads each), so a block's scale is computed once, with no
+// shuffle.
 //
 // Four-over-six ("Advanced: four-over-six"): each block is also quantised
 // with its amax mapped to 4 (s_b from amax_b / 4) and keeps that result only
-// when its squared error is strictly smaller.  The error of 8 elements is
-// summed in order in float32 (no fused multiply-add); the two lanes' half
-// sums are then added, which is the same sum on both lanes (IEEE addition
-// commutes).  S_g is amax / (256 * 6) in that mode.
+// when its squared error is strictly smaller.  The error of each half block
+// (8 elements) is summed in order in float32 (no fused multiply-add), and
+// the two half sums are then added.  S_g is amax / (256 * 6) in that mode.
 
 // tab[c] = RN(1/S_b) for S_b = RN(E4M3value(c) * S_g), c = 0..127 (entries
 // for c = 0 and the NaN code 127 are never read), written by `n` threads
@@ -516,26 +516,26 @@ __device__ __forceinline__ uint32_t nvfp4_block_code(float amax_b, float s_g, co
     return e4m3_byte(__fdiv_rn(__fdiv_rn(amax_b, four ? 4.0f : kE2M1Max), s_g));
 }
 
-// One lane's half block: packed E2M1 codes and the block's scale byte.  Every
-// lane of the warp must call this (shuffles).
+// One lane's whole block of 16 elements (v0: elements 0..7, v1: 8..15):
+// packed E2M1 codes (element i in bits 4i..4i+3 of the 64-bit result) and
+// the block's scale byte.  With four-over-six the squared error of each half
+// of the block is summed in element order and the two halves are then added.
 template <bool FOS>
-__device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, const ScaleDiv& dg, const float* rcp,
-                                                 bool from_amax, uint32_t& packed, uint32_t& code) {
-    const uint32_t m = warp_max_u32(absmax_v4(v), 2);
-    const float amax_b = amax_bits_to_f32(m);
-    float f[8];
-    unpack8(v, f);
+__device__ __forceinline__ void nvfp4_block(const uint4& v0, const uint4& v1, float s_g, const ScaleDiv& dg,
+                                            const float* rcp, bool from_amax, uint2& packed, uint32_t& code) {
+    const float amax_b = amax_bits_to_f32(max(absmax_v4(v0), absmax_v4(v1)));
+    float f[16];
+    unpack8(v0, f);
+    unpack8(v1, f + 8);
     code = nvfp4_block_code(amax_b, s_g, dg, false);
-    const float s6 = __fmul_rn(e4m3_value(code), s_g);
-    packed = e2m1_quant8(f, s6, rcp[code], from_amax);
+    const float s6 = __fmul_rn(e4m3_value(code), s_g), r6 = rcp[code];
+    packed = make_uint2(e2m1_quant8(f, s6, r6, from_amax), e2m1_quant8(f + 8, s6, r6, from_amax));
     if constexpr (FOS) {
         const uint32_t code4 = nvfp4_block_code(amax_b, s_g, dg, true);
-        const float s4 = __fmul_rn(e4m3_value(code4), s_g);
-        const uint32_t p4 = e2m1_quant8(f, s4, rcp[code4], from_amax);
-        float e6 = half_sq_err(f, packed, s6);
-        float e4 = half_sq_err(f, p4, s4);
-        e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, 1));
-        e4 = __fadd_rn(e4, __shfl_xor_sync(0xFFFFFFFFu, e4, 1));
+        const float s4 = __fmul_rn(e4m3_value(code4), s_g), r4 = rcp[code4];
+        const uint2 p4 = make_uint2(e2m1_quant8(f, s4, r4, from_amax), e2m1_quant8(f + 8, s4, r4, from_amax));
+        const float e6 = __fadd_rn(half_sq_err(f, packed.x, s6), half_sq_err(f + 8, packed.y, s6));
+        const float e4 = __fadd_rn(half_sq_err(f, p4.x, s4), half_sq_err(f + 8, p4.y, s4));
         if (e4 < e6) {
             packed = p4;
             code = code4;
@@ -543,27 +543,41 @@ __device__ __forceinline__ void nvfp4_half_block(const uint4& v, float s_g, cons
     }
 }
 
-// Quantise columns [cb, cb + 1024) of row r with outer scale s_g.
+// 16 bytes of BF16 through L1 (the lane's block is one 32-byte sector read
+// by two such loads: the second finds it in L1).
+__device__ __forceinline__ uint4 ldg_v4_l1(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Quantise columns [cb, cb + 1024) of row r with outer scale s_g: lane l owns
+// the blocks at columns cb + 16 l and cb + 512 + 16 l (cols % 16 == 0, so a
+// block lies wholly inside the row or wholly past its end).
 template <bool FOS>
 __device__ __forceinline__ void nvfp4_segment(const uint16_t* __restrict__ x, int64_t r, int64_t cb, int64_t cols,
                                               int64_t ldx, uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
                                               float s_g, const ScaleDiv& dg, const float* rcp, bool from_amax,
                                               int lane) {
     const int64_t nb = cols >> 4;
+    const uint16_t* xr = x + r * ldx;
     uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t c = cb + j * 256 + lane * 8;
-        v[j] = (c < cols) ? ldg_v4(x + r * ldx + c) : make_uint4(0, 0, 0, 0);
+    for (int h = 0; h < 2; ++h) {
+        const int64_t c = cb + 512 * h + 16 * lane;
+        const bool in = c < cols;
+        v[2 * h] = in ? ldg_v4_l1(xr + c) : make_uint4(0, 0, 0, 0);
+        v[2 * h + 1] = in ? ldg_v4_l1(xr + c + 8) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t c = cb + j * 256 + lane * 8;
-        uint32_t packed, code;
-        nvfp4_half_block<FOS>(v[j], s_g, dg, rcp, from_amax, packed, code);
+    for (int h = 0; h < 2; ++h) {
+        const int64_t c = cb + 512 * h + 16 * lane;
+        uint2 packed;
+        uint32_t code;
+        nvfp4_block<FOS>(v[2 * h], v[2 * h + 1], s_g, dg, rcp, from_amax, packed, code);
         if (c < cols) {
-            *reinterpret_cast<uint32_t*>(q + r * (cols >> 1) + (c >> 1)) = packed;
-            if ((lane & 1) == 0) sb[r * nb + (c >> 4)] = (uint8_t)code;
+            *reinterpret_cast<uint2*>(q + r * (cols >> 1) + (c >> 1)) = packed;
+            sb[r * nb + (c >> 4)] = (uint8_t)code;
         }
     }
 }
