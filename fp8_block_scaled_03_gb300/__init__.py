@@ -141,6 +141,13 @@ def workspace(device=None) -> torch.Tensor:
     return ws
 
 
+def new_workspace(device=None) -> torch.Tensor:
+    """A fresh zero-initialised workspace: calls that run concurrently (on
+    different streams) need one each."""
+    dev = torch.device(device if device is not None else torch.cuda.current_device())
+    return torch.zeros(load_library().fp8bs_workspace_size(), dtype=torch.uint8, device=dev)
+
+
 def read_status(ws: Optional[torch.Tensor] = None, stream=None) -> int:
     ws = ws if ws is not None else workspace()
     return load_library().fp8bs_read_status(_ptr(ws), _stream(stream))

@@ -103,6 +103,7 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gr
     if (!aligned16(q)) return FP8BS_EALIGN;
     if (needs_partials(gran, flags) && (workspace == nullptr || workspace_bytes < kWorkspaceBytes))
         return FP8BS_EWORKSPACE;
+    if (workspace != nullptr && !aligned16(workspace)) return FP8BS_EALIGN;
     QuantJob j{};
     j.x = static_cast<const uint16_t*>(x);
     j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
@@ -129,6 +130,7 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
     if (!aligned16(q_t) || (q != nullptr && !aligned16(q))) return FP8BS_EALIGN;
     if (needs_partials(gran, flags) && (workspace == nullptr || workspace_bytes < kWorkspaceBytes))
         return FP8BS_EWORKSPACE;
+    if (workspace != nullptr && !aligned16(workspace)) return FP8BS_EALIGN;
     QuantJob j{};
     j.x = static_cast<const uint16_t*>(x);
     j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
@@ -170,6 +172,7 @@ int fp8_quantize_gathered(const void* x, int64_t tokens, int64_t cols, int64_t l
         (reinterpret_cast<uintptr_t>(token_index) & 7u))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     QuantJob j{};
     j.x = static_cast<const uint16_t*>(x);
     j.rows = rows; j.cols = cols; j.ldx = ld_x; j.gran = gran;
@@ -194,6 +197,7 @@ int fp8_gather_rows(const void* q_src, const void* scales_src, int64_t tokens, i
         (reinterpret_cast<uintptr_t>(token_index) & 7u))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     GatherJob j{};
     j.q_src = static_cast<const uint8_t*>(q_src);
     j.s_src = scales_src;
@@ -235,6 +239,7 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
     if (!scales_aligned(a_scales, a_gran) || !scales_aligned(b_scales, b_gran)) return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     const bool fp32_a = a_gran <= FP8BS_BLOCK_128x128, fp32_b = b_gran <= FP8BS_BLOCK_128x128;
     GemmJob j{};
     j.a = a; j.sa = a_scales; j.a_gran = a_gran;
@@ -289,6 +294,7 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
                !aligned4(b_tensor_scale)))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     if (total_rows == 0) return FP8BS_OK;
     GemmJob j{};
     j.a = a; j.sa = a_scales; j.b = b; j.sb = b_scales;
@@ -327,6 +333,7 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned4(a_scales) || !aligned4(b_scales))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     GemmJob j{};
     j.a = a; j.sa = a_scales; j.a_gran = FP8BS_MXFP8_1x32;
     j.b = b; j.sb = b_scales; j.b_gran = FP8BS_MXFP8_1x32;
@@ -352,6 +359,7 @@ int fp8bs_test_stalled_gemm_blockwise(const void* a, const void* a_scales, int a
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned4(a_scales) || !aligned4(b_scales))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     GemmJob j{};
     j.a = a; j.sa = a_scales; j.a_gran = a_gran;
     j.b = b; j.sb = b_scales; j.b_gran = b_gran;
@@ -376,6 +384,7 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
         !aligned4(a_tensor_scale) || !aligned4(b_tensor_scale))
         return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     GemmJob j{};
     j.a = a; j.sa = a_scales; j.a_gran = FP8BS_NVFP4_1x16;
     j.b = b; j.sb = b_scales; j.b_gran = FP8BS_NVFP4_1x16;
@@ -408,6 +417,7 @@ int fp8bs_mma_peak(int kind, int n, int iters, int pattern, float* out, void* wo
         return FP8BS_EINVAL;
     if (out != nullptr && !aligned4(out)) return FP8BS_EALIGN;
     if (workspace == nullptr || workspace_bytes < kWorkspaceBytes) return FP8BS_EWORKSPACE;
+    if (!aligned16(workspace)) return FP8BS_EALIGN;
     return cuda_status(launch_mma_peak(kind, sm_count(), iters, n, pattern, out, static_cast<int*>(workspace),
                                        reinterpret_cast<cudaStream_t>(stream)));
 }

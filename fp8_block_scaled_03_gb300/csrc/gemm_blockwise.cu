@@ -29,7 +29,13 @@
 //               shared-memory ring.  The per-column B scales of the 1x128
 //               mode would otherwise cost every epilogue warp one scattered
 //               load per column per K block.
-//   warp 3      idle (completes the producer warpgroup)
+//   warp 3      tile fetcher (one lane): the CTA's first tile is blockIdx.x,
+//               each later one the next index of a tile counter in the
+//               workspace (atomicAdd), published to the other roles through
+//               a shared-memory ring.  Tiles go in index order to whichever
+//               CTA is free, so a launch that starts on SMs as an earlier
+//               kernel leaves them evens out its own tail.  The last CTA to
+//               finish puts the counter back to 0 for the next launch.
 //   warps 4..11 epilogue: warp w reads TMEM lanes 32*(w%4).. (one D row per
 //               thread) and columns 128*((w-4)/4).. (one 128-column half);
 //               acc += partial * sa * sb with both scales read from the
@@ -58,6 +64,19 @@ constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BY
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(BM, BN);
+// Tile indices in flight.  One: a CTA claims its next tile when its
+// epilogue starts the current one, so claims keep pace with the work (a
+// deeper ring let every CTA claim several tiles at launch, in arbitrary
+// order: the tiles spread unevenly over the CTAs and wgrad took 0.38 ms
+// instead of 0.29).
+constexpr int TQ = 1;
+constexpr int TQ_READERS = 11; // producer, MMA thread, scale loader, 8 epilogue warps
+// Dynamic tile order for B with one scale per 128 x 128 block (or per
+// tensor).  The per-column-scale form (the weight gradient's 1 x 128 B)
+// keeps the static order: a tile index that arrives at run time stays live
+// through its epilogue's K loop, and that form is already at the register
+// limit there (its spills grew and it ran 6 % slower).
+template <int SB> constexpr bool kDynamicTiles = SB != 1;
 
 struct Params {
     int64_t m, n, k;
@@ -70,12 +89,16 @@ struct Params {
     uint64_t wait_ns;     // bound of every pipeline wait
     int stall_stage0;     // test hook: the producer withholds stage 0
     int out_f32;          // D is float32 (tm_d then maps float32 32 x 32 boxes)
+    unsigned long long* tile_next;   // tiles handed out past the first wave (nullptr: static order)
+    unsigned int* tile_done;         // CTAs finished
 };
 
 struct alignas(16) Shared {
     float sa[SRING][SG][BM];   // A scale of each tile row, per K block of the group
     float sb[SRING][SG][BN];   // B scale of each tile column (modes 0 / 2: entries 0 and 128 only)
     uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], sfull[SRING], sempty[SRING], drain;
+    uint64_t tq_full[TQ], tq_empty[TQ];
+    int64_t tq[TQ];            // tile index ring (an index >= total ends the CTA's work)
     uint32_t tmem_base;
     int abort;
     SchedShared sched;
@@ -135,6 +158,10 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             mbar_init(smem_u32(&sh->sempty[g]), 8);    // every epilogue warp arrives
         }
         mbar_init(smem_u32(&sh->drain), 1);
+        for (int i = 0; i < TQ; ++i) {
+            mbar_init(smem_u32(&sh->tq_full[i]), 1);
+            mbar_init(smem_u32(&sh->tq_empty[i]), TQ_READERS);
+        }
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -152,6 +179,22 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
+    // The i-th tile of this CTA: from the ring (dynamic order), or
+    // blockIdx.x + i * gridDim.x.  `t` >= total ends the work.  The caller
+    // releases the ring slot once it has read it.
+    auto next_tile = [&](uint32_t i, int64_t& t) -> bool {
+        if constexpr (!kDynamicTiles<SB_MODE>) {
+            t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+            return true;
+        }
+        const uint32_t slot = i % TQ;
+        if (!mbar_wait(smem_u32(&sh->tq_full[slot]), (i / TQ) & 1, abort, p.status, p.wait_ns)) return false;
+        t = sh->tq[slot];
+        return true;
+    };
+    auto release_tile = [&](uint32_t i) {
+        if constexpr (kDynamicTiles<SB_MODE>) mbar_arrive(smem_u32(&sh->tq_empty[i % TQ]));
+    };
 
     if (warp < 4) {
     setmaxnreg_dec<72>();
@@ -160,7 +203,11 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (uint32_t ti_i = 0; ok; ++ti_i) {
+                int64_t t;
+                if (!next_tile(ti_i, t)) { ok = false; break; }
+                release_tile(ti_i);
+                if (t >= total) break;
                 const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
@@ -186,7 +233,11 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         if (lane == 0) {
             uint32_t it = 0, kbg = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (uint32_t ti_i = 0; ok; ++ti_i) {
+                int64_t t;
+                if (!next_tile(ti_i, t)) { ok = false; break; }
+                release_tile(ti_i);
+                if (t >= total) break;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
@@ -215,7 +266,8 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         const float sa0 = (SA_MODE == 0) ? __ldg(p.sa) : 0.0f;
         uint32_t gg = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        // one tile's scale groups
+        auto loader_tile = [&](int64_t t) {
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const float* sb_e = p.sb;
             if (p.experts) {
@@ -266,6 +318,37 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 }
                 mbar_arrive(smem_u32(&sh->sfull[g]));
             }
+        };
+        if constexpr (kDynamicTiles<SB_MODE>) {
+            for (uint32_t ti_i = 0; ok; ++ti_i) {
+                int64_t t = 0;
+                bool got = true;
+                if (lane == 0) {
+                    got = next_tile(ti_i, t);
+                    if (got) release_tile(ti_i);
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
+                t = __shfl_sync(0xFFFFFFFFu, t, 0);
+                if (t >= total) break;
+                loader_tile(t);
+            }
+        } else {
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) loader_tile(t);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ tile fetcher
+        if (kDynamicTiles<SB_MODE> && lane == 0) {
+            for (uint32_t i = 0;; ++i) {
+                const uint32_t slot = i % TQ;
+                if (!mbar_wait(smem_u32(&sh->tq_empty[slot]), ((i / TQ) & 1) ^ 1, abort, p.status, p.wait_ns)) break;
+                int64_t t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;   // static order
+                if (p.tile_next != nullptr && i > 0)
+                    t = (int64_t)gridDim.x + (int64_t)atomicAdd(p.tile_next, 1ull);
+                sh->tq[slot] = t < total ? t : total;
+                mbar_arrive(smem_u32(&sh->tq_full[slot]));   // release: the index is visible to the waiters
+                if (t >= total) break;
+            }
         }
         __syncwarp();
     }
@@ -278,7 +361,8 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint32_t kbg = 0, gg = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        // one tile: promote every K block, then store D
+        auto epilogue_tile = [&](int64_t t) {
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
@@ -347,7 +431,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     ++gg;
                 }
             }
-            if (!ok) break;
+            if (!ok) return;
             // This warp's 32 rows leave by TMA when they all belong to the
             // tile's row group (always for a dense GEMM; an expert's last,
             // partial row block may end inside them, and the rows after it
@@ -437,6 +521,23 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     }
                 }
             }
+        };
+        if constexpr (kDynamicTiles<SB_MODE>) {
+            // lane 0 takes the tile index from the ring and hands it to the warp
+            for (uint32_t ti_i = 0; ok; ++ti_i) {
+                int64_t t = 0;
+                bool got = true;
+                if (lane == 0) {
+                    got = next_tile(ti_i, t);
+                    if (got) release_tile(ti_i);
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
+                t = __shfl_sync(0xFFFFFFFFu, t, 0);
+                if (t >= total) break;
+                epilogue_tile(t);
+            }
+        } else {
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) epilogue_tile(t);
         }
         if (lane == 0) bulk_wait0();   // this warp's output stores are complete
     }
@@ -446,6 +547,15 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+    // Every fetch of this CTA has returned (the fetcher used its value before
+    // the barrier above); the last CTA to get here puts the counter back to 0.
+    if (kDynamicTiles<SB_MODE> && p.tile_next != nullptr && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.tile_done, 1u) == gridDim.x - 1) {
+            atomicExch(p.tile_next, 0ull);
+            atomicExch(p.tile_done, 0u);
+        }
     }
 }
 
@@ -492,6 +602,11 @@ int launch_gemm_blockwise(const GemmJob& j, cudaStream_t st) {
     p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
     p.stall_stage0 = j.stall_stage0;
     p.out_f32 = j.d_f32 ? 1 : 0;
+    if (j.status != nullptr) {   // the workspace: its tile counter
+        char* ws = reinterpret_cast<char*>(j.status);
+        p.tile_next = reinterpret_cast<unsigned long long*>(ws + kTileCounterOffset);
+        p.tile_done = reinterpret_cast<unsigned int*>(ws + kTileCounterOffset + 8);
+    }
     const int sms = sm_count();
     int grid = sms;
     if (j.experts == 0) {

@@ -10,6 +10,10 @@ namespace fp8bs {
 // Workspace layout: [0, 4) sticky status word; [256, ...) amax partials.
 constexpr size_t kWorkspaceBytes = 16384;
 constexpr size_t kPartialsOffset = 256;
+// Blockwise GEMM tile counter in the workspace: bytes [64, 72) the next tile
+// past the first wave, [72, 76) the CTAs finished; the kernel's last CTA
+// puts both back to 0, so they are 0 between calls.
+constexpr size_t kTileCounterOffset = 64;
 constexpr int kMaxPartials = (int)((kWorkspaceBytes - kPartialsOffset) / 4);
 
 int sm_count();  // of the current device, cached per device

@@ -33,14 +33,18 @@
  *     elements.  Outputs are densely packed (pitch = their column count).
  *   - Arguments are checked on the host before any launch; a failed check
  *     returns a negative fp8bs_status and enqueues nothing.
- *   - `workspace` is a caller-owned device buffer of at least
- *     FP8BS_WORKSPACE_BYTES bytes, zero-filled once by the caller before its
+ *   - `workspace` is a caller-owned, 16-byte aligned device buffer of at
+ *     least FP8BS_WORKSPACE_BYTES bytes, zero-filled once by the caller before its
  *     first use.  Its first 4 bytes are a sticky device status word that
  *     kernels set (never clear) when a bounded wait gives up, a gathered
  *     token index is out of range or expert offsets are malformed; read it with
- *     fp8bs_read_status and clear it with fp8bs_clear_status.  The rest is
+ *     fp8bs_read_status and clear it with fp8bs_clear_status.  Bytes
+ *     [64, 80) hold the blockwise GEMM's tile counter (its CTAs take tiles
+ *     in index order as they become free; the kernel's last CTA puts the
+ *     counter back to 0, so it is 0 between calls).  From byte 256 on it is
  *     scratch for the per-tensor / NVFP4 amax reduction.  Calls that share a
- *     workspace must be ordered on the GPU (same stream or events).
+ *     workspace must be ordered on the GPU (same stream or events); calls
+ *     that run concurrently need a workspace each.
  *   - Launch failures return FP8BS_ECUDA (cudaGetLastError is consumed).
  */
 #ifndef FP8BS_H

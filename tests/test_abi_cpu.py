@@ -62,6 +62,7 @@ def test_quantize_rejects_bad_arguments(lib):
     assert q(FAKE, 4, 128, 128, 4, FAKE, FAKE, None, 0, FAKE, 16384, None) == -1  # nvfp4 needs S_g ptr
     assert q(FAKE, 4, 120, 120, 4, FAKE, FAKE, FAKE, 0, FAKE, 16384, None) == -1  # nvfp4 cols % 16
     assert q(FAKE, 4, 128, 128, 4, FAKE, FAKE, FAKE, 0, FAKE, 1024, None) == -6   # ws too small
+    assert q(FAKE, 4, 128, 128, 0, FAKE, FAKE, None, 0, MISALIGNED, 16384, None) == -2   # ws misaligned
 
 
 def test_quantize_transposed_rejects_bad_arguments(lib):
@@ -82,6 +83,8 @@ def test_gemm_rejects_bad_arguments(lib):
     assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -1  # nvfp4 ts
     assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, 0, FAKE, 16384, None) == -1  # k % 256
     assert g(MISALIGNED, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -2
+    # the workspace holds 8-byte tile counters and the status word: 16-byte aligned
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, MISALIGNED, 16384, None) == -2
 
 
 def test_gemm_rejects_unknown_output_dtype(lib):
