@@ -266,8 +266,19 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         const float sa0 = (SA_MODE == 0) ? __ldg(p.sa) : 0.0f;
         uint32_t gg = 0;
         bool ok = true;
-        // one tile's scale groups
-        auto loader_tile = [&](int64_t t) {
+        // one tile's scale groups, under the dynamic or the static loop (the
+        // body written out in each, as in the epilogue)
+        if constexpr (kDynamicTiles<SB_MODE>) {
+        for (uint32_t ti_i = 0; ok; ++ti_i) {
+            int64_t t = 0;
+            bool got = true;
+            if (lane == 0) {
+                got = next_tile(ti_i, t);
+                if (got) release_tile(ti_i);
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
+            t = __shfl_sync(0xFFFFFFFFu, t, 0);
+            if (t >= total) break;
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const float* sb_e = p.sb;
             if (p.experts) {
@@ -318,22 +329,60 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 }
                 mbar_arrive(smem_u32(&sh->sfull[g]));
             }
-        };
-        if constexpr (kDynamicTiles<SB_MODE>) {
-            for (uint32_t ti_i = 0; ok; ++ti_i) {
-                int64_t t = 0;
-                bool got = true;
-                if (lane == 0) {
-                    got = next_tile(ti_i, t);
-                    if (got) release_tile(ti_i);
-                }
-                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
-                t = __shfl_sync(0xFFFFFFFFu, t, 0);
-                if (t >= total) break;
-                loader_tile(t);
-            }
+        }
         } else {
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) loader_tile(t);
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
+            const float* sb_e = p.sb;
+            if (p.experts) {
+                const int64_t per = (SB_MODE == 2) ? ((p.n + 127) / 128) * nkb : p.n * nkb;
+                sb_e = p.sb + (int64_t)ti.expert * per;
+            }
+            for (int64_t kb0 = 0; kb0 < nkb; kb0 += SG, ++gg) {
+                const uint32_t g = gg % SRING, ph = (gg / SRING) & 1;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&sh->sempty[g]), ph ^ 1, abort, p.status, p.wait_ns))) {
+                    ok = false;
+                    break;
+                }
+                float4 va[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t row = ti.row0 + lane + 32 * i;
+                    if (SA_MODE == 0) va[i] = make_float4(sa0, sa0, sa0, sa0);
+                    else if (row >= ti.row_end) va[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    else if (SA_MODE == 1) va[i] = scales4(p.sa + row * nkb, kb0, nkb, vec_a);
+                    else va[i] = scales4(p.sa + (row >> 7) * nkb, kb0, nkb, false);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) put4a(sh->sa[g], lane + 32 * i, va[i]);
+                if (SB_MODE == 1) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float4 vb[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t col = ti.n0 + lane + 32 * (4 * half + i);
+                            vb[i] = (col < p.n) ? scales4(sb_e + col * nkb, kb0, nkb, vec_b) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) put4(sh->sb[g], lane + 32 * (4 * half + i), vb[i]);
+                    }
+                } else if (lane < 2) {
+                    const int64_t col = ti.n0 + 128 * lane;
+                    float4 vb = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (col < p.n) {
+                        if (SB_MODE == 0) {
+                            const float s0 = __ldg(sb_e);
+                            vb = make_float4(s0, s0, s0, s0);
+                        } else {
+                            vb = scales4(sb_e + (col >> 7) * nkb, kb0, nkb, false);
+                        }
+                    }
+                    put4(sh->sb[g], 128 * lane, vb);
+                }
+                mbar_arrive(smem_u32(&sh->sfull[g]));
+            }
+        }
         }
         __syncwarp();
     } else if (warp == 3) {
@@ -361,8 +410,21 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint32_t kbg = 0, gg = 0;
         bool ok = true;
-        // one tile: promote every K block, then store D
-        auto epilogue_tile = [&](int64_t t) {
+        // The same tile body under two loops (written out twice: wrapped in a
+        // lambda, the body compiled to code 2-3 % slower): the dynamic order
+        // takes each index from the ring (lane 0, then a shuffle), the static
+        // one computes it.
+        if constexpr (kDynamicTiles<SB_MODE>) {
+        for (uint32_t ti_i = 0; ok; ++ti_i) {
+            int64_t t = 0;
+            bool got = true;
+            if (lane == 0) {
+                got = next_tile(ti_i, t);
+                if (got) release_tile(ti_i);
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
+            t = __shfl_sync(0xFFFFFFFFu, t, 0);
+            if (t >= total) break;
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
@@ -431,7 +493,7 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     ++gg;
                 }
             }
-            if (!ok) return;
+            if (!ok) break;
             // This warp's 32 rows leave by TMA when they all belong to the
             // tile's row group (always for a dense GEMM; an expert's last,
             // partial row block may end inside them, and the rows after it
@@ -521,23 +583,168 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     }
                 }
             }
-        };
-        if constexpr (kDynamicTiles<SB_MODE>) {
-            // lane 0 takes the tile index from the ring and hands it to the warp
-            for (uint32_t ti_i = 0; ok; ++ti_i) {
-                int64_t t = 0;
-                bool got = true;
-                if (lane == 0) {
-                    got = next_tile(ti_i, t);
-                    if (got) release_tile(ti_i);
-                }
-                if (!__shfl_sync(0xFFFFFFFFu, got, 0)) { ok = false; break; }
-                t = __shfl_sync(0xFFFFFFFFu, t, 0);
-                if (t >= total) break;
-                epilogue_tile(t);
-            }
+        }
         } else {
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) epilogue_tile(t);
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
+            const int64_t row = ti.row0 + 32 * q + lane;
+            const int64_t col0 = ti.n0 + 128 * h;
+            uint64_t acc[64];   // FP32 pairs: columns (2j, 2j+1) of this thread's 128-column half
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+
+            for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
+                const uint32_t g = gg % SRING, kk = (uint32_t)(kb & (SG - 1));
+                if (kk == 0) {
+                    const bool got_s = mbar_wait(smem_u32(&sh->sfull[g]), (gg / SRING) & 1, abort, p.status, p.wait_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got_s)) { ok = false; break; }
+                }
+                const float fa = sh->sa[g][kk][32 * q + lane];
+                const float* sbk = &sh->sb[g][kk][128 * h];
+                const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
+                const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
+                if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }   // tcgen05.ld is .sync.aligned
+                tc_fence_after();
+                const float fb = (SB_MODE == 1) ? 0.0f : sbk[0];
+                const uint64_t f2 = f2_pack(fa * fb, fa * fb);
+                const uint64_t fa2 = f2_pack(fa, fa);
+                const float4* buf4 = reinterpret_cast<const float4*>(sbk);
+                const uint32_t taddr = tmem + lane_base + b * BN + 128 * h;
+                // Promote one 16-column chunk held in r: acc += partial * scale.
+                auto promote = [&](const uint32_t* r, int c) {
+                    if (SB_MODE == 1) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 s4 = buf4[(16 * c + j) >> 2];
+                            f2_fma(acc[(16 * c + j) / 2], f2_pack_bits(r[j], r[j + 1]), f2_mul(fa2, f2_pack(s4.x, s4.y)));
+                            f2_fma(acc[(16 * c + j) / 2 + 1], f2_pack_bits(r[j + 2], r[j + 3]),
+                                   f2_mul(fa2, f2_pack(s4.z, s4.w)));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) f2_fma(acc[8 * c + j], f2_pack_bits(r[2 * j], r[2 * j + 1]), f2);
+                    }
+                };
+                // Two 16-register staging buffers: the TMEM load of chunk c+1 is
+                // in flight while chunk c is promoted.
+                uint32_t ra[16], rb[16];
+                tmem_ld_32x32b_x16(taddr, ra);
+                tmem_ld_wait16(ra);
+#pragma unroll
+                for (int c = 0; c < 8; c += 2) {
+                    tmem_ld_32x32b_x16(taddr + 16 * (c + 1), rb);
+                    promote(ra, c);
+                    tmem_ld_wait16(rb);
+                    if (c + 2 < 8) {
+                        tmem_ld_32x32b_x16(taddr + 16 * (c + 2), ra);
+                        promote(rb, c + 1);
+                        tmem_ld_wait16(ra);
+                    } else {
+                        // every read of this partial buffer is complete: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+                        promote(rb, c + 1);
+                    }
+                }
+                if (kk == SG - 1 || kb + 1 == nkb) {
+                    // this warp's last read of the scale group: hand the slot back to the loader
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh->sempty[g]));
+                    ++gg;
+                }
+            }
+            if (!ok) break;
+            // This warp's 32 rows leave by TMA when they all belong to the
+            // tile's row group (always for a dense GEMM; an expert's last,
+            // partial row block may end inside them, and the rows after it
+            // belong to the next expert).
+            if ((p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) && p.out_f32) {
+                // float32 output: the same staging buffer holds 32 rows x 32
+                // floats (128-byte rows, same swizzle); four boxes per warp
+                uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float a0, a1, a2, a3;
+                        f2_unpack(acc[16 * qq + 2 * c], a0, a1);
+                        f2_unpack(acc[16 * qq + 2 * c + 1], a2, a3);
+                        *reinterpret_cast<float4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_float4(a0, a1, a2, a3);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 32 * qq), (int32_t)(ti.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            } else if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
+                // BF16 tile rows through this warp's staging buffer (128-byte
+                // swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)), then a
+                // TMA store of the 32 x 64 box; the TMA clips rows and columns
+                // past the matrix
+                uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float lo, hi;
+                            f2_unpack(acc[32 * half + 4 * c + u], lo, hi);
+                            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+                            o[u] = *reinterpret_cast<uint32_t*>(&v);
+                        }
+                        *reinterpret_cast<uint4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, smem_u32(ob), (int32_t)(col0 + 64 * half), (int32_t)(ti.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            } else if (row < ti.row_end && p.out_f32) {
+                float* drow = reinterpret_cast<float*>(p.d) + row * p.n + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4) {
+                    if (col0 + j < p.n) {
+                        float a0, a1, a2, a3;
+                        f2_unpack(acc[j / 2], a0, a1);
+                        f2_unpack(acc[j / 2 + 1], a2, a3);
+                        *reinterpret_cast<float4*>(drow + j) = make_float4(a0, a1, a2, a3);
+                    }
+                }
+            } else if (row < ti.row_end) {
+                __nv_bfloat16* drow = p.d + row * p.n + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 8) {
+                    if (col0 + j < p.n) {
+                        uint4 o;
+                        float a0, a1, a2, a3, a4, a5, a6, a7;
+                        f2_unpack(acc[j / 2 + 0], a0, a1);
+                        f2_unpack(acc[j / 2 + 1], a2, a3);
+                        f2_unpack(acc[j / 2 + 2], a4, a5);
+                        f2_unpack(acc[j / 2 + 3], a6, a7);
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(a0, a1);
+                        __nv_bfloat162 v1 = __floats2bfloat162_rn(a2, a3);
+                        __nv_bfloat162 v2 = __floats2bfloat162_rn(a4, a5);
+                        __nv_bfloat162 v3 = __floats2bfloat162_rn(a6, a7);
+                        o.x = *reinterpret_cast<uint32_t*>(&v0);
+                        o.y = *reinterpret_cast<uint32_t*>(&v1);
+                        o.z = *reinterpret_cast<uint32_t*>(&v2);
+                        o.w = *reinterpret_cast<uint32_t*>(&v3);
+                        *reinterpret_cast<uint4*>(drow + j) = o;
+                    }
+                }
+            }
+        }
         }
         if (lane == 0) bulk_wait0();   // this warp's output stores are complete
     }
