@@ -585,11 +585,21 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             }
         }
         } else {
+        // Static order: the per-column-scale form only (kDynamicTiles).  Its B
+        // carries one scale per column and K block, so TMEM is read in the
+        // .16x256b shape: thread t holds rows rq, rq + 8, rq + 16, rq + 24 of
+        // the warp's 32 (rq = t / 4) and, in each 8-column group of its half,
+        // columns cq and cq + 1 (cq = 2 (t % 4)).  It then needs 32 column
+        // scales a K block instead of the 128 of a whole row: with one row
+        // per thread, the shared loads of the column scales (16 bytes to all
+        // 32 lanes per 4 columns) kept the LSU write-back 61 % busy and
+        // bounded the K block.
+        static_assert(SB_MODE == 1, "the static loop serves the per-column-scale form");
+        const int rq = lane >> 2, cq = 2 * (lane & 3);
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TileInfo ti = sched_tile<BM, BN>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
-            const int64_t row = ti.row0 + 32 * q + lane;
             const int64_t col0 = ti.n0 + 128 * h;
-            uint64_t acc[64];   // FP32 pairs: columns (2j, 2j+1) of this thread's 128-column half
+            uint64_t acc[64];   // FP32 pairs: acc[16 ri + g] = row rq + 8 ri, columns 8g + cq, 8g + cq + 1
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0ull;
 
@@ -599,52 +609,57 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     const bool got_s = mbar_wait(smem_u32(&sh->sfull[g]), (gg / SRING) & 1, abort, p.status, p.wait_ns);
                     if (!__all_sync(0xFFFFFFFFu, got_s)) { ok = false; break; }
                 }
-                const float fa = sh->sa[g][kk][32 * q + lane];
-                const float* sbk = &sh->sb[g][kk][128 * h];
+                uint64_t fa2[4];   // the four rows' A scales, as pairs
+#pragma unroll
+                for (int ri = 0; ri < 4; ++ri) {
+                    const float fa = sh->sa[g][kk][32 * q + rq + 8 * ri];
+                    fa2[ri] = f2_pack(fa, fa);
+                }
+                const float* sbk = &sh->sb[g][kk][128 * h + cq];
                 const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
                 const bool got = mbar_wait(smem_u32(&sh->tfull[b]), tph, abort, p.status);
                 if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }   // tcgen05.ld is .sync.aligned
                 tc_fence_after();
-                const float fb = (SB_MODE == 1) ? 0.0f : sbk[0];
-                const uint64_t f2 = f2_pack(fa * fb, fa * fb);
-                const uint64_t fa2 = f2_pack(fa, fa);
-                const float4* buf4 = reinterpret_cast<const float4*>(sbk);
                 const uint32_t taddr = tmem + lane_base + b * BN + 128 * h;
-                // Promote one 16-column chunk held in r: acc += partial * scale.
-                auto promote = [&](const uint32_t* r, int c) {
-                    if (SB_MODE == 1) {
+                // chunk k: column groups 4(k/2) .. +3 of lanes 16 (k%2) .. +15 of the quarter
+                auto load_chunk = [&](int k, uint32_t* r) {
+                    tmem_ld_16x256b_x4(taddr + ((uint32_t)(16 * (k & 1)) << 16) + 32 * (k >> 1), r);
+                };
+                float2 sc[4];      // column scales of the chunk's four groups
+                // acc += partial * s_a * s_b for one chunk held in r
+                auto promote = [&](const uint32_t* r, int k) {
+                    const int c = k >> 1, hb = k & 1;
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 s4 = buf4[(16 * c + j) >> 2];
-                            f2_fma(acc[(16 * c + j) / 2], f2_pack_bits(r[j], r[j + 1]), f2_mul(fa2, f2_pack(s4.x, s4.y)));
-                            f2_fma(acc[(16 * c + j) / 2 + 1], f2_pack_bits(r[j + 2], r[j + 3]),
-                                   f2_mul(fa2, f2_pack(s4.z, s4.w)));
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t sb2 = f2_pack(sc[j].x, sc[j].y);
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int ri = 2 * hb + rr;
+                            f2_fma(acc[16 * ri + 4 * c + j], f2_pack_bits(r[4 * j + 2 * rr], r[4 * j + 2 * rr + 1]),
+                                   f2_mul(fa2[ri], sb2));
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) f2_fma(acc[8 * c + j], f2_pack_bits(r[2 * j], r[2 * j + 1]), f2);
                     }
                 };
-                // Two 16-register staging buffers: the TMEM load of chunk c+1 is
-                // in flight while chunk c is promoted.
                 uint32_t ra[16], rb[16];
-                tmem_ld_32x32b_x16(taddr, ra);
+                load_chunk(0, ra);
                 tmem_ld_wait16(ra);
 #pragma unroll
-                for (int c = 0; c < 8; c += 2) {
-                    tmem_ld_32x32b_x16(taddr + 16 * (c + 1), rb);
-                    promote(ra, c);
+                for (int k = 0; k < 8; k += 2) {
+                    load_chunk(k + 1, rb);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sc[j] = *reinterpret_cast<const float2*>(sbk + 8 * (2 * k + j));
+                    promote(ra, k);
                     tmem_ld_wait16(rb);
-                    if (c + 2 < 8) {
-                        tmem_ld_32x32b_x16(taddr + 16 * (c + 2), ra);
-                        promote(rb, c + 1);
+                    if (k + 2 < 8) {
+                        load_chunk(k + 2, ra);
+                        promote(rb, k + 1);
                         tmem_ld_wait16(ra);
                     } else {
                         // every read of this partial buffer is complete: hand it back to the MMA warp
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
-                        promote(rb, c + 1);
+                        promote(rb, k + 1);
                     }
                 }
                 if (kk == SG - 1 || kb + 1 == nkb) {
@@ -655,24 +670,23 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 }
             }
             if (!ok) break;
-            // This warp's 32 rows leave by TMA when they all belong to the
-            // tile's row group (always for a dense GEMM; an expert's last,
-            // partial row block may end inside them, and the rows after it
-            // belong to the next expert).
             if ((p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) && p.out_f32) {
-                // float32 output: the same staging buffer holds 32 rows x 32
-                // floats (128-byte rows, same swizzle); four boxes per warp
+                // float32 boxes of 32 rows x 32 columns (128-byte rows, 128-byte swizzle)
                 uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     if (lane == 0) bulk_wait_read0();
                     __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        float a0, a1, a2, a3;
-                        f2_unpack(acc[16 * qq + 2 * c], a0, a1);
-                        f2_unpack(acc[16 * qq + 2 * c + 1], a2, a3);
-                        *reinterpret_cast<float4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_float4(a0, a1, a2, a3);
+                    for (int ri = 0; ri < 4; ++ri) {
+                        const int lr = rq + 8 * ri;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {   // group 4 qq + j: bytes 32 j + 4 cq of the row
+                            float lo, hi;
+                            f2_unpack(acc[16 * ri + 4 * qq + j], lo, hi);
+                            *reinterpret_cast<float2*>(ob + lr * 128 + 16 * ((2 * j + (cq >> 2)) ^ (lr & 7)) +
+                                                       ((4 * cq) & 15)) = make_float2(lo, hi);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -682,26 +696,23 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     }
                 }
             } else if (p.experts == 0 || ti.row0 + 32 * q + 32 <= ti.row_end) {
-                // BF16 tile rows through this warp's staging buffer (128-byte
-                // swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)), then a
-                // TMA store of the 32 x 64 box; the TMA clips rows and columns
-                // past the matrix
+                // BF16 boxes of 32 rows x 64 columns (16-byte chunk j of row r at j ^ (r % 8))
                 uint8_t* ob = ostage + (size_t)ew * OSTAGE_BYTES;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     if (lane == 0) bulk_wait_read0();
                     __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t o[4];
+                    for (int ri = 0; ri < 4; ++ri) {
+                        const int lr = rq + 8 * ri;
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
+                        for (int j = 0; j < 8; ++j) {   // group 8 half + j: bytes 16 j + 2 cq of the row
                             float lo, hi;
-                            f2_unpack(acc[32 * half + 4 * c + u], lo, hi);
+                            f2_unpack(acc[16 * ri + 8 * half + j], lo, hi);
                             __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-                            o[u] = *reinterpret_cast<uint32_t*>(&v);
+                            *reinterpret_cast<uint32_t*>(ob + lr * 128 + 16 * (j ^ (lr & 7)) + 2 * cq) =
+                                *reinterpret_cast<uint32_t*>(&v);
                         }
-                        *reinterpret_cast<uint4*>(ob + lane * 128 + 16 * (c ^ (lane & 7))) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -710,37 +721,24 @@ gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                         bulk_commit();
                     }
                 }
-            } else if (row < ti.row_end && p.out_f32) {
-                float* drow = reinterpret_cast<float*>(p.d) + row * p.n + col0;
+            } else {
+                // rows of an expert's last, partial row block: direct stores, row by row
 #pragma unroll
-                for (int j = 0; j < 128; j += 4) {
-                    if (col0 + j < p.n) {
-                        float a0, a1, a2, a3;
-                        f2_unpack(acc[j / 2], a0, a1);
-                        f2_unpack(acc[j / 2 + 1], a2, a3);
-                        *reinterpret_cast<float4*>(drow + j) = make_float4(a0, a1, a2, a3);
-                    }
-                }
-            } else if (row < ti.row_end) {
-                __nv_bfloat16* drow = p.d + row * p.n + col0;
+                for (int ri = 0; ri < 4; ++ri) {
+                    const int64_t row = ti.row0 + 32 * q + rq + 8 * ri;
+                    if (row >= ti.row_end) continue;
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
-                    if (col0 + j < p.n) {
-                        uint4 o;
-                        float a0, a1, a2, a3, a4, a5, a6, a7;
-                        f2_unpack(acc[j / 2 + 0], a0, a1);
-                        f2_unpack(acc[j / 2 + 1], a2, a3);
-                        f2_unpack(acc[j / 2 + 2], a4, a5);
-                        f2_unpack(acc[j / 2 + 3], a6, a7);
-                        __nv_bfloat162 v0 = __floats2bfloat162_rn(a0, a1);
-                        __nv_bfloat162 v1 = __floats2bfloat162_rn(a2, a3);
-                        __nv_bfloat162 v2 = __floats2bfloat162_rn(a4, a5);
-                        __nv_bfloat162 v3 = __floats2bfloat162_rn(a6, a7);
-                        o.x = *reinterpret_cast<uint32_t*>(&v0);
-                        o.y = *reinterpret_cast<uint32_t*>(&v1);
-                        o.z = *reinterpret_cast<uint32_t*>(&v2);
-                        o.w = *reinterpret_cast<uint32_t*>(&v3);
-                        *reinterpret_cast<uint4*>(drow + j) = o;
+                    for (int gq = 0; gq < 16; ++gq) {
+                        const int64_t col = col0 + 8 * gq + cq;
+                        if (col >= p.n) continue;
+                        float lo, hi;
+                        f2_unpack(acc[16 * ri + gq], lo, hi);
+                        if (p.out_f32) {
+                            *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.d) + row * p.n + col) = make_float2(lo, hi);
+                        } else {
+                            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+                            *reinterpret_cast<__nv_bfloat162*>(p.d + row * p.n + col) = v;
+                        }
                     }
                 }
             }
