@@ -934,18 +934,18 @@ def pow2_step_bench(torch, fp, dev, args, pk):
     for _ in range(max(3, args.warmup)):
         step.run()
     torch.cuda.synchronize()
-    gev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(1, args.steps)
-    gms = [0.0, 0.0, 0.0]
+    # events for every GEMM of every step, read after the loop (no host
+    # synchronisation inside the timed steps)
+    gev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
+           for _ in range(n)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record()
-    for _ in range(n):
-        step.run(gev)
-        torch.cuda.synchronize()
-        for j in range(3):
-            gms[j] += gev[j][0].elapsed_time(gev[j][1])
+    for i in range(n):
+        step.run(gev[i])
     s1.record()
     s1.synchronize()
+    gms = [sum(g[j][0].elapsed_time(g[j][1]) for g in gev) for j in range(3)]
     per_step = s0.elapsed_time(s1) / n
     peak = pk["bf16_tflops"] * FP8_PER_BF16
     avg = statistics.mean(g / n for g in gms)
