@@ -180,6 +180,7 @@ class DenseStep:
         # free up.
         self.concurrent = recipe == "fp32"
         self.ws_g = [fp.new_workspace(dev) for _ in range(3)]
+        self.ws_q = [fp.new_workspace(dev) for _ in range(3)]
         lo, hi = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
         # torch reports (lowest, highest) priority; a smaller number is a higher priority
         prio = [min(lo, hi) if i == 2 else (max(lo, hi) if i == 0 else (lo + hi) // 2) for i in range(3)]
@@ -188,13 +189,32 @@ class DenseStep:
     launches_per_step = 6
 
     def quantize(self):
-        fp = self.fp
-        fp.fp8_quantize_transposed(self.x, self.g_tok, True, q_t=self.qxt, scales_t=self.sxt, q=self.qx,
-                                   scales=self.sx, ws=self.ws)
-        fp.fp8_quantize_transposed(self.w, self.g_blk, True, q_t=self.qwt, scales_t=self.swt, q=self.qw,
-                                   scales=self.sw, ws=self.ws)
-        fp.fp8_quantize_transposed(self.dy, self.g_tok, True, q_t=self.qdyt, scales_t=self.sdyt, q=self.qdy,
-                                   scales=self.sdy, ws=self.ws)
+        """X, W and dY, dual (row-wise and transposed).  With concurrent
+        GEMMs the three quantisers also run concurrently, dY (the largest)
+        on the highest-priority stream, each with a workspace of its own,
+        joined back into the current stream before the GEMMs."""
+        fp, torch = self.fp, self.torch
+        jobs = ((self.dy, self.g_tok, self.qdyt, self.sdyt, self.qdy, self.sdy),
+                (self.x, self.g_tok, self.qxt, self.sxt, self.qx, self.sx),
+                (self.w, self.g_blk, self.qwt, self.swt, self.qw, self.sw))
+        if not self.concurrent:
+            for src, g, qt, st, q, s in jobs:
+                fp.fp8_quantize_transposed(src, g, True, q_t=qt, scales_t=st, q=q, scales=s, ws=self.ws)
+            return
+        cur = torch.cuda.current_stream()
+        ready = torch.cuda.Event()
+        ready.record(cur)
+        done = []
+        for i, (src, g, qt, st, q, s) in enumerate(jobs):
+            s_ = self.side[2 - i]            # dY on wgrad's (highest-priority) stream
+            s_.wait_event(ready)
+            with torch.cuda.stream(s_):
+                fp.fp8_quantize_transposed(src, g, True, q_t=qt, scales_t=st, q=q, scales=s, ws=self.ws_q[i])
+                e_ = torch.cuda.Event()
+                e_.record(s_)
+            done.append(e_)
+        for e_ in done:
+            cur.wait_event(e_)
 
     def ops(self):
         t, b = self.g_tok, self.g_blk
@@ -249,7 +269,7 @@ class DenseStep:
                 phase[1].record()
 
     def status(self):
-        return max(abs(self.fp.read_status(w)) for w in [self.ws] + self.ws_g)
+        return max(abs(self.fp.read_status(w)) for w in [self.ws] + self.ws_g + self.ws_q)
 
 
 def max_over_ranks(torch, dist, value: float, device) -> float:
@@ -676,8 +696,8 @@ def gemm_source_sha16() -> str:
 def workload_config(args):
     return {"workload": "dense blockwise FP8 linear fwd+bwd, Qwen3-4B MLP shape (tokens 8192, hidden 2560, "
                         "intermediate 9728); X,dY 1x128 FP32 scales (dual row+transposed), W 128x128 FP32 scales; "
-                        "the three quantisers on the step's stream, then the three independent GEMMs concurrently "
-                        "(wgrad, dgrad, fprop on streams of their own, dynamic tile order)",
+                        "the three quantisers concurrently, then the three independent GEMMs concurrently "
+                        "(wgrad, dgrad, fprop on streams of their own by priority, dynamic tile order)",
             "tokens": M3, "hidden": H3, "intermediate": I3, "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs 250 MB and step working set ~630 MB, both > 129 MB L2; sub-benchmarks flush L2 "
                   "before each timed call (512 MB written, then 256 MB of it read back, so L2 starts cold and "
