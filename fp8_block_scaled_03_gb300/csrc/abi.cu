@@ -71,6 +71,13 @@ int check_quant_common(const void* x, int64_t rows, int64_t cols, int64_t ld_x, 
     return FP8BS_OK;
 }
 
+// Sizes that TMA addresses: tensor-map coordinates are 32-bit signed, so a
+// dimension a kernel walks by TMA stays below 2^31 (less one 256-wide box).
+constexpr int64_t kMaxTmaDim = 0x7FFFFF00;
+inline bool tma_dims_ok(int64_t a, int64_t b = 0, int64_t c = 0) {
+    return a <= kMaxTmaDim && b <= kMaxTmaDim && c <= kMaxTmaDim;
+}
+
 // Unknown flag bits, or four-over-six on a non-NVFP4 granularity.
 bool bad_flags(int gran, unsigned flags) {
     if (flags & ~(FP8BS_FLAG_GIVEN_TENSOR_SCALE | FP8BS_FLAG_NVFP4_4OVER6)) return true;
@@ -123,6 +130,7 @@ int fp8_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t l
     if (is_nvfp4(gran)) return FP8BS_EUNSUPPORTED;
     if (bad_flags(gran, flags)) return FP8BS_EINVAL;
     if (rows % 16 != 0) return FP8BS_EINVAL;
+    if (!tma_dims_ok(rows, cols, ld_x)) return FP8BS_EINVAL;
     int rc = check_quant_common(x, rows, cols, ld_x, gran);
     if (rc) return rc > 0 ? FP8BS_OK : rc;
     if (q_t == nullptr || scales_t == nullptr) return FP8BS_EINVAL;
@@ -233,6 +241,7 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0) return FP8BS_EINVAL;
+    if (!tma_dims_ok(m, n, k)) return FP8BS_EINVAL;
     if (d_dtype != FP8BS_OUT_BF16 && d_dtype != FP8BS_OUT_F32) return FP8BS_EINVAL;
     if (a_gran < 0 || a_gran > FP8BS_NVFP4_ROW_1x16 || b_gran < 0 || b_gran > FP8BS_NVFP4_ROW_1x16)
         return FP8BS_EINVAL;
@@ -287,6 +296,7 @@ int fp8_grouped_gemm(const void* a, const void* a_scales,
     if (experts <= 0 || experts > 1024 || total_rows < 0 || n <= 0 || k <= 0 || n % 8 != 0 ||
         k % (nv ? 256 : 128) != 0)
         return FP8BS_EINVAL;
+    if (!tma_dims_ok(total_rows, n * experts, k)) return FP8BS_EINVAL;
     if (nv && (a_tensor_scale == nullptr || b_tensor_scale == nullptr)) return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_EALIGN;
     if (!aligned4(a_scales) || !aligned4(b_scales) || (reinterpret_cast<uintptr_t>(offsets) & 7u)) return FP8BS_EALIGN;
@@ -329,6 +339,7 @@ int fp8bs_test_stalled_gemm(const void* a, const void* a_scales, const void* b, 
     if (a == nullptr || b == nullptr || d == nullptr || a_scales == nullptr || b_scales == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 128 != 0) return FP8BS_EINVAL;
+    if (!tma_dims_ok(m, n, k)) return FP8BS_EINVAL;
     if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned4(a_scales) || !aligned4(b_scales))
         return FP8BS_EALIGN;
@@ -355,6 +366,7 @@ int fp8bs_test_stalled_gemm_blockwise(const void* a, const void* a_scales, int a
         b_gran > FP8BS_BLOCK_128x128)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 128 != 0) return FP8BS_EINVAL;
+    if (!tma_dims_ok(m, n, k)) return FP8BS_EINVAL;
     if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned4(a_scales) || !aligned4(b_scales))
         return FP8BS_EALIGN;
@@ -379,6 +391,7 @@ int fp8bs_test_stalled_gemm_nvfp4(const void* a, const void* a_scales, const voi
         a_tensor_scale == nullptr || b_tensor_scale == nullptr)
         return FP8BS_EINVAL;
     if (m <= 0 || n <= 0 || k <= 0 || n % 8 != 0 || k % 256 != 0) return FP8BS_EINVAL;
+    if (!tma_dims_ok(m, n, k)) return FP8BS_EINVAL;
     if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return FP8BS_EINVAL;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(a_scales) || !aligned16(b_scales) ||
         !aligned4(a_tensor_scale) || !aligned4(b_tensor_scale))

@@ -153,7 +153,7 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int gr
  * transpose of the row-wise codes and the scales the transposed scale grid.
  *
  * gran: PER_TENSOR, TOKEN_1x128, BLOCK_128x128, MXFP8_1x32 or the two
- * _POW2 granularities (both NVFP4 granularities return FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0.
+ * _POW2 granularities (both NVFP4 granularities return FP8BS_EUNSUPPORTED).  Requirements as fp8_quantize plus rows % 16 == 0 and cols, ld_x below 2^31 - 256 (X is read by TMA).
  *   q_t      uint8 [cols, rows]           codes of X^T
  *   scales_t layout of the table above for a [cols, rows] matrix
  *   q, scales  optional (both NULL or both set): the row-wise result of
@@ -300,7 +300,8 @@ typedef enum {
  *       a_tensor_scale[i] * *b_tensor_scale (per-token activation scale)
  * Other pairs return FP8BS_EUNSUPPORTED.  Scale layouts are those written
  * by fp8_quantize for the operand's own [rows, k] shape.  m, n > 0,
- * n % 8 == 0; a, b, d 16-byte aligned.  a_tensor_scale / b_tensor_scale:
+ * n % 8 == 0, and m, n, k below 2^31 - 256 (TMA coordinates are 32-bit);
+ * a, b, d 16-byte aligned.  a_tensor_scale / b_tensor_scale:
  * device float32[1], NVFP4 only (else ignored, may be NULL);
  * a_tensor_scale is float32[m] for NVFP4_ROW_1x16.
  * workspace: required (status word for the bounded pipeline waits).
@@ -345,7 +346,8 @@ int fp8_block_gemm(const void* a, const void* a_scales, int a_gran,
  * float32[experts], the outer scale S_g of each expert's weight; row r of
  * expert e is multiplied by a_tensor_scale[0 or r] * b_tensor_scale[e].  Both
  * are ignored (may be NULL) for the other granularities.  NVFP4 block scales
- * 16-byte aligned.  D: BF16 [total_rows, n].  n % 8 == 0.  workspace
+ * 16-byte aligned.  D: BF16 [total_rows, n].  n % 8 == 0; total_rows,
+ * experts * n and k below 2^31 - 256 (TMA coordinates).  workspace
  * required.
  */
 int fp8_grouped_gemm(const void* a, const void* a_scales,

@@ -71,6 +71,7 @@ def test_quantize_transposed_rejects_bad_arguments(lib):
     assert t(FAKE, 32, 128, 128, 4, FAKE, FAKE, None, None, None, 0, None, 0, None) == -3  # nvfp4
     assert t(FAKE, 32, 128, 128, 1, FAKE, FAKE, FAKE, None, None, 0, None, 0, None) == -1  # q w/o scales
     assert t(FAKE, 32, 128, 128, 1, MISALIGNED, FAKE, None, None, None, 0, None, 0, None) == -2
+    assert t(FAKE, 32, 2 ** 31, 2 ** 31, 1, FAKE, FAKE, None, None, None, 0, None, 0, None) == -1  # TMA range
 
 
 def test_gemm_rejects_bad_arguments(lib):
@@ -83,6 +84,9 @@ def test_gemm_rejects_bad_arguments(lib):
     assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -1  # nvfp4 ts
     assert g(FAKE, FAKE, 4, FAKE, FAKE, 4, FAKE, FAKE, 128, 128, 128, FAKE, 0, FAKE, 16384, None) == -1  # k % 256
     assert g(MISALIGNED, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, FAKE, 16384, None) == -2
+    # TMA coordinates are 32-bit: dimensions of 2^31 and more are refused before any launch
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 2 ** 31, 128, 256, FAKE, 0, FAKE, 16384, None) == -1
+    assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 2 ** 31, FAKE, 0, FAKE, 16384, None) == -1
     # the workspace holds 8-byte tile counters and the status word: 16-byte aligned
     assert g(FAKE, FAKE, 1, FAKE, FAKE, 2, None, None, 128, 128, 256, FAKE, 0, MISALIGNED, 16384, None) == -2
 
@@ -100,6 +104,9 @@ def test_grouped_gemm_rejects_bad_arguments(lib):
     assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 64, 128, 200, 3, FAKE, FAKE, 16384, None) == -1  # k
     assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 64, 128, 256, 3, FAKE, None, 0, None) == -6
     assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 0, 128, 256, 3, FAKE, FAKE, 16384, None) == 0  # empty
+    # TMA coordinates are 32-bit: rows, and the stacked B rows (experts * n), stay below 2^31
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 8, 2 ** 31, 128, 256, 3, FAKE, FAKE, 16384, None) == -1
+    assert g(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1024, 64, 2 ** 21, 256, 3, FAKE, FAKE, 16384, None) == -1
     # NVFP4: both tensor scales required, k % 256, 16-byte block scales
     assert g(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 8, 64, 128, 256, 4, FAKE, FAKE, 16384, None) == -1
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 384, 7, FAKE, FAKE, 16384, None) == -1
