@@ -485,6 +485,6 @@ const char* fp8bs_status_string(int status) {
     }
 }
 
-int fp8bs_version(void) { return 102; }
+int fp8bs_version(void) { return 103; }
 
 }  // extern "C"

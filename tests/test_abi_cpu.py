@@ -40,7 +40,7 @@ def test_status_strings_and_sizes(lib):
     assert ws(2, 4, 128, 1, 0) == 0 and ws(7, 4, 128, 3, 0) == 0               # dequantise, SwiGLU: none
     assert all(ws(op, 4, 128, 3, 0) == 16384 for op in (3, 4, 5, 6))          # GEMMs, gathers: status word
     assert ws(8, 4, 128, 1, 0) == 2 ** 64 - 1 and ws(0, -1, 128, 1, 0) == 2 ** 64 - 1
-    assert lib.fp8bs_version() == 102
+    assert lib.fp8bs_version() == 103
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert fp.status_string(code) != "unknown status"
     assert fp.status_string(7) == "unknown status"
