@@ -173,12 +173,12 @@ class DenseStep:
         self.y, self.dx, self.dw = e(M3, I3, dt=bf), e(M3, H3, dt=bf), e(I3, H3, dt=bf)
         self.ws = fp.workspace(dev)
         # The three GEMMs are independent once X, W and dY are quantised: with
-        # the blockwise kernel's dynamic tile order they run concurrently, each
-        # on a stream (and workspace) of its own, wgrad (longest tiles) first
-        # and fprop (shortest) last, so fprop's tiles fill the SMs that dgrad's
+        # the GEMM kernels' dynamic tile order they run concurrently, each on a
+        # stream (and workspace) of its own, wgrad (longest tiles) first and
+        # fprop (shortest) last, so fprop's tiles fill the SMs that dgrad's
         # last wave leaves idle.  Stream priorities keep that order when SMs
         # free up.
-        self.concurrent = recipe == "fp32"
+        self.concurrent = True
         self.ws_g = [fp.new_workspace(dev) for _ in range(3)]
         self.ws_q = [fp.new_workspace(dev) for _ in range(3)]
         lo, hi = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
@@ -951,31 +951,39 @@ def pow2_step_bench(torch, fp, dev, args, pk):
     """The same fwd+bwd step with power-of-two block scales (tensor-core
     block-scale path instead of FP32 promotion)."""
     step = DenseStep(torch, fp, dev, seed=2000, recipe="pow2")
+    step.concurrent = not args.sequential_gemms
     for _ in range(max(3, args.warmup)):
         step.run()
     torch.cuda.synchronize()
     n = max(1, args.steps)
-    # events for every GEMM of every step, read after the loop (no host
-    # synchronisation inside the timed steps)
-    gev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
-           for _ in range(n)]
+    # the GEMM phase of every step bracketed by events, read after the loop
+    # (no host synchronisation inside the timed steps)
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record()
     for i in range(n):
-        step.run(gev[i])
+        step.run(phase=pev[i])
     s1.record()
     s1.synchronize()
-    gms = [sum(g[j][0].elapsed_time(g[j][1]) for g in gev) for j in range(3)]
     per_step = s0.elapsed_time(s1) / n
+    avg = statistics.mean(a.elapsed_time(b) for a, b in pev) / 3
+    # each GEMM alone, one after another, after the timed steps
+    gev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(3)]
+           for _ in range(max(3, n // 2))]
+    for g in gev:
+        step.gemms(g)
+    torch.cuda.synchronize()
+    gms = [statistics.mean(g[j][0].elapsed_time(g[j][1]) for g in gev) for j in range(3)]
+    assert step.status() == 0, "a device wait timed out during the power-of-two step"
     peak = pk["bf16_tflops"] * FP8_PER_BF16
-    avg = statistics.mean(g / n for g in gms)
     t = GEMM_FLOP / avg / 1e9
     lp = pk.get("loop", {}).get("mxfp8")
     return {"tflops_step": round(STEP_FLOP / per_step / 1e9, 1), "ms_per_step": round(per_step, 4),
             "gemm_tflops": round(t, 1), "gemm_frac": round(t / peak, 3),
             "gemm_frac_of_mxfp8_loop_peak": round(t / lp, 3) if lp else None,
             "peak_note": "measured bf16 burst x nominal fp8/bf16 ratio 2",
-            "per_gemm_ms": [round(g / n, 4) for g in gms]}
+            "gemm_phase_ms": round(3 * avg, 4),
+            "per_gemm_ms": [round(g, 4) for g in gms]}
 
 
 def e2e_bench(torch, fp, dev, step, reps=8):

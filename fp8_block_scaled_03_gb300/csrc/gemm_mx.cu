@@ -73,6 +73,17 @@ template <> struct Cfg<kNv> {
     static constexpr int SF_BYTES_PER_ROW = 16;
 };
 
+// Tile order.  The power-of-two form (the block-wise recipe's fast path,
+// whose dense GEMMs the step runs concurrently) takes its tiles dynamically:
+// the producer claims each next tile from a counter in the workspace
+// (atomicAdd, one tile ahead) and publishes the indices through a small
+// shared-memory ring that the MMA thread, the scale loaders and the
+// epilogue read; the last CTA to finish puts the counter back to 0.  The
+// MXFP8 and NVFP4 forms keep the static order blockIdx.x + i * gridDim.x.
+template <int KIND> constexpr bool kDynMx = KIND == kP2;
+constexpr int MX_TQ = 4;           // tile indices in flight (how far the producer may run ahead)
+constexpr int MX_TQ_READERS = 11;  // MMA thread, two scale loaders, eight epilogue warps
+
 struct Params {
     int64_t m, n, k;
     const uint8_t* sa;   // row-major scale bytes [m, k / vec]
@@ -86,6 +97,8 @@ struct Params {
     int experts;
     uint64_t wait_ns;     // bound of every pipeline wait
     int stall_stage0;     // test hook: the producer withholds stage 0
+    unsigned long long* tile_next;   // tiles handed out past the first wave (dynamic order)
+    unsigned int* tile_done;         // CTAs finished
 };
 
 // Dense tile order: groups of row tiles, row tile fastest inside a group.
@@ -98,6 +111,8 @@ template <int STAGES>
 struct alignas(16) Shared {
     uint64_t full[STAGES], empty[STAGES], tfull, tempty, drain;
     uint64_t ldrain[2];    // per scale loader: its scale copies have landed (exit path)
+    uint64_t tq_full[MX_TQ], tq_empty[MX_TQ];
+    int64_t tq[MX_TQ];     // tile index ring (dynamic order; an index >= total ends the work)
     uint32_t tmem_base;
     int abort;
     SchedShared sched;
@@ -351,6 +366,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         mbar_init(smem_u32(&sh->drain), 1);
         mbar_init(smem_u32(&sh->ldrain[0]), 1);
         mbar_init(smem_u32(&sh->ldrain[1]), 1);
+        for (int i = 0; i < MX_TQ; ++i) {
+            mbar_init(smem_u32(&sh->tq_full[i]), 1);
+            mbar_init(smem_u32(&sh->tq_empty[i]), MX_TQ_READERS);
+        }
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -368,13 +387,59 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
+    // The i-th tile of this CTA: the static order, or the ring's i-th index,
+    // read and released by the calling thread (tile_one) or by lane 0 and
+    // handed to the whole warp (tile_of).  false: a wait gave up.
+    auto tile_one = [&](uint32_t i, int64_t& t) -> bool {
+        if constexpr (!kDynMx<KIND>) {
+            t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+            return true;
+        }
+        const uint32_t slot = i % MX_TQ;
+        if (!mbar_wait(smem_u32(&sh->tq_full[slot]), (i / MX_TQ) & 1, abort, p.status, p.wait_ns)) return false;
+        t = sh->tq[slot];
+        mbar_arrive(smem_u32(&sh->tq_empty[slot]));
+        return true;
+    };
+    auto tile_of = [&](uint32_t i, int64_t& t) -> bool {
+        if constexpr (!kDynMx<KIND>) {
+            t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+            return true;
+        }
+        bool got = true;
+        int64_t v = 0;
+        if (lane == 0) got = tile_one(i, v);
+        t = __shfl_sync(0xFFFFFFFFu, v, 0);
+        return __shfl_sync(0xFFFFFFFFu, got, 0);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            // Dynamic order: round i's index is published while round i-1's
+            // tile is being loaded, right after it was claimed, so every reader
+            // finds it there before it needs it.  The index past the last tile
+            // (total) is published once and ends every role's loop.
+            auto publish = [&](uint32_t i, int64_t v) -> bool {
+                const uint32_t slot = i % MX_TQ;
+                if (!mbar_wait(smem_u32(&sh->tq_empty[slot]), ((i / MX_TQ) & 1) ^ 1, abort, p.status, p.wait_ns))
+                    return false;
+                sh->tq[slot] = v < total ? v : total;
+                mbar_arrive(smem_u32(&sh->tq_full[slot]));
+                return true;
+            };
+            int64_t cur = blockIdx.x;
+            if constexpr (kDynMx<KIND>) ok = publish(0, cur);
+            for (uint32_t ti_i = 0; ok; ++ti_i) {
+                const int64_t t = cur;
+                if (t >= total) break;
+                cur = t + gridDim.x;
+                if constexpr (kDynMx<KIND>) {
+                    if (p.tile_next != nullptr) cur = (int64_t)gridDim.x + (int64_t)atomicAdd(p.tile_next, 1ull);
+                    if (!publish(ti_i + 1, cur)) { ok = false; break; }
+                }
                 const TileInfo ti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
                 const int32_t brow = (int32_t)(ti.expert * p.n + ti.n0);
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
@@ -400,7 +465,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (lane == 0) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+            for (uint32_t ti_i = 0; ok; ++ti_i, ++tcount) {
+                int64_t t;
+                if (!tile_one(ti_i, t)) { ok = false; break; }
+                if (t >= total) break;
                 if (!mbar_wait(smem_u32(&sh->tempty), (tcount & 1) ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
@@ -443,18 +511,28 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // buffers, the loop unrolled by two so both names are constants).
         const int part = warp - 2;
         const bool vec = (sf_pitch & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.sa) | reinterpret_cast<uintptr_t>(p.sb)) & 3u) == 0;
-        int64_t lt = blockIdx.x, lkb0 = 0;                // load cursor (tile, first stage of the group)
+        // Load cursor: the tile's round, index and layout, and the first
+        // stage of the group.  A tile's index is read when its first group is
+        // loaded, not when the previous tile's last one is (the groups of that
+        // tile still to be written out must not wait on the next index).
+        uint32_t lt_i = 0;
+        int64_t lt = 0, lkb0 = 0;
+        bool lneed = true;
         TileInfo lti{};
-        if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
         auto load_next = [&](WideRegs& w, int64_t& kb0_out) -> bool {
+            if (lneed) {
+                lneed = false;
+                if (!tile_of(lt_i, lt)) lt = total;       // a wait gave up: the abort flag ends the rest
+                if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+            }
             if (lt >= total) return false;
             load_scales_group<SA, SB>(w, p, lti, lkb0, nkb, lane, sf_pitch, vec, part);
             kb0_out = lkb0;
             lkb0 += kSfGroup;
             if (lkb0 >= nkb) {
                 lkb0 = 0;
-                lt += gridDim.x;
-                if (lt < total) lti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, lt);
+                ++lt_i;
+                lneed = true;
             }
             return true;
         };
@@ -568,7 +646,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // S_g(B) per expert (one value for a dense GEMM)
         float g = 1.0f;
         uint32_t tcount = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+        for (uint32_t ti_i = 0;; ++ti_i, ++tcount) {
+            int64_t t;
+            if (!tile_of(ti_i, t)) break;
+            if (t >= total) break;
             const TileInfo ti = sched_tile<BM, BN, kTileGroupM<KIND>>(&sh->sched, p.offsets, p.experts, p.m, n_tiles, t);
             const int64_t row = ti.row0 + 32 * q + lane;
             if (KIND == kNv) {
@@ -675,6 +756,15 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    // Every claim of this CTA has returned (the producer used its value
+    // before the barrier above); the last CTA to get here resets the counter.
+    if (kDynMx<KIND> && p.tile_next != nullptr && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.tile_done, 1u) == gridDim.x - 1) {
+            atomicExch(p.tile_next, 0ull);
+            atomicExch(p.tile_done, 0u);
+        }
+    }
 }
 
 template <int KIND, int SA, int SB, bool F32>
@@ -727,6 +817,10 @@ int launch_gemm_mx(const GemmJob& j, cudaStream_t st) {
     p.experts = j.experts;
     p.wait_ns = j.wait_ns ? j.wait_ns : kWaitLimitNs;
     p.stall_stage0 = j.stall_stage0;
+    if (j.status != nullptr) {
+        p.tile_next = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(j.status) + kTileCounterOffset);
+        p.tile_done = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(j.status) + kTileCounterOffset + 8);
+    }
     const bool f32 = j.d_f32;
     const int sms = sm_count();
     int grid = sms;

@@ -1,7 +1,8 @@
-"""The blockwise GEMM's dynamic tile order.
+"""The GEMM kernels' dynamic tile order.
 
-CTAs of the 128x128-weight-scale forms take tiles from a counter in the
-workspace as they become free.  A tile's arithmetic does not depend on which
+CTAs of the blockwise kernel's 128x128-weight-scale forms, and of the
+block-scaled kernel's power-of-two (UE8M0) block forms, take tiles from a
+counter in the workspace as they become free.  A tile's arithmetic does not depend on which
 CTA computes it, so the three GEMMs of the dense step run concurrently on
 three streams (a workspace each) must give the same bits as the same calls
 one after another; the counter must be back to zero after every call (the
@@ -31,21 +32,26 @@ def counter_bytes(ws):
     return ws[64:80].cpu().numpy()
 
 
-def step_operands(m, h, i, seed):
+RECIPES = {"fp32": ("1x128", "128x128"), "pow2": ("1x128_pow2", "128x128_pow2")}
+
+
+def step_operands(m, h, i, seed, recipe="fp32"):
+    t, b = RECIPES[recipe]
     x = synth.activations((m, h), seed=seed, outlier_frac=0.01, outlier_mult=50.0)
     w = synth.weights((i, h), seed=seed + 1, std=0.02)
     dy = synth.activations((m, i), seed=seed + 2, outlier_frac=0.01, outlier_mult=50.0)
-    qxt, sxt, qx, sx = fp.fp8_quantize_transposed(to_dev_bf16(x), "1x128", also_rowwise=True)
-    qwt, swt, qw, sw = fp.fp8_quantize_transposed(to_dev_bf16(w), "128x128", also_rowwise=True)
-    qdyt, sdyt, qdy, sdy = fp.fp8_quantize_transposed(to_dev_bf16(dy), "1x128", also_rowwise=True)
-    return ((qx, sx, "1x128", qw, sw, "128x128"),        # fprop  [m, i]
-            (qdy, sdy, "1x128", qwt, swt, "128x128"),    # dgrad  [m, h]
-            (qdyt, sdyt, "1x128", qxt, sxt, "1x128"))    # wgrad  [i, h]
+    qxt, sxt, qx, sx = fp.fp8_quantize_transposed(to_dev_bf16(x), t, also_rowwise=True)
+    qwt, swt, qw, sw = fp.fp8_quantize_transposed(to_dev_bf16(w), b, also_rowwise=True)
+    qdyt, sdyt, qdy, sdy = fp.fp8_quantize_transposed(to_dev_bf16(dy), t, also_rowwise=True)
+    return ((qx, sx, t, qw, sw, b),          # fprop  [m, i]
+            (qdy, sdy, t, qwt, swt, b),      # dgrad  [m, h]
+            (qdyt, sdyt, t, qxt, sxt, t))    # wgrad  [i, h]
 
 
+@pytest.mark.parametrize("recipe", ["fp32", "pow2"])
 @pytest.mark.parametrize("m,h,i", [(1024, 640, 1152), (8192, 2560, 9728)])
-def test_concurrent_step_gemms_match_sequential(m, h, i):
-    ops = step_operands(m, h, i, seed=m + h)
+def test_concurrent_step_gemms_match_sequential(m, h, i, recipe):
+    ops = step_operands(m, h, i, seed=m + h, recipe=recipe)
     wss = [fp.new_workspace() for _ in range(3)]
     seq = [fp.fp8_block_gemm(*o, ws=wss[j]) for j, o in enumerate(ops)]
     torch.cuda.synchronize()
@@ -68,28 +74,30 @@ def test_concurrent_step_gemms_match_sequential(m, h, i):
         assert not counter_bytes(ws).any()
 
 
-def test_counter_reset_after_every_call_and_grouped():
-    """Dense and grouped (FP32 scale) calls back to back on one workspace:
-    every call computes all its tiles, and the counter ends at zero."""
+@pytest.mark.parametrize("recipe", ["fp32", "pow2"])
+def test_counter_reset_after_every_call_and_grouped(recipe):
+    """Dense and grouped calls back to back on one workspace: every call
+    computes all its tiles, and the counter ends at zero."""
+    t, bg = RECIPES[recipe]
     ws = fp.new_workspace()
     a = synth.activations((520, 384), seed=3, outlier_frac=0.01, outlier_mult=20.0)
     b = synth.weights((4 * 256, 384), seed=4)
-    qa, sa, _ = fp.fp8_quantize(to_dev_bf16(a), "1x128")
-    qb, sb, _ = fp.fp8_quantize(to_dev_bf16(b), "128x128")
-    ref = fp.fp8_block_gemm(qa, sa, "1x128", qb, sb, "128x128", ws=ws)
+    qa, sa, _ = fp.fp8_quantize(to_dev_bf16(a), t)
+    qb, sb, _ = fp.fp8_quantize(to_dev_bf16(b), bg)
+    ref = fp.fp8_block_gemm(qa, sa, t, qb, sb, bg, ws=ws)
     # grouped: 4 experts of 256 rows of B, ragged row counts (one empty)
     counts = [0, 130, 7, 383]
     offsets = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)).cuda()
     qbs, sbs = [], []
     for e in range(4):
-        q_, s_, _ = fp.fp8_quantize(to_dev_bf16(b[e * 256:(e + 1) * 256]), "128x128")
+        q_, s_, _ = fp.fp8_quantize(to_dev_bf16(b[e * 256:(e + 1) * 256]), bg)
         qbs.append(q_)
         sbs.append(s_)
     qbg, sbg = torch.stack(qbs), torch.stack(sbs)
-    gref = fp.fp8_grouped_gemm(qa, sa, qbg, sbg, offsets, "1x128", ws=fp.new_workspace())
+    gref = fp.fp8_grouped_gemm(qa, sa, qbg, sbg, offsets, t, ws=fp.new_workspace())
     for _ in range(4):
-        d = fp.fp8_block_gemm(qa, sa, "1x128", qb, sb, "128x128", ws=ws)
-        g = fp.fp8_grouped_gemm(qa, sa, qbg, sbg, offsets, "1x128", ws=ws)
+        d = fp.fp8_block_gemm(qa, sa, t, qb, sb, bg, ws=ws)
+        g = fp.fp8_grouped_gemm(qa, sa, qbg, sbg, offsets, t, ws=ws)
         torch.cuda.synchronize()
         assert torch.equal(d.view(torch.int16), ref.view(torch.int16))
         assert torch.equal(g.view(torch.int16), gref.view(torch.int16))
