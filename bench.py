@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--sequential-gemms", action="store_true",
                     help="run the step's three GEMMs one after another on the step's stream")
     ap.add_argument("--kernel", default=None,
-                    choices=["fprop", "dgrad", "wgrad", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
+                    choices=["fprop", "dgrad", "wgrad", "fprop_pow2", "dgrad_pow2", "wgrad_pow2", "quant_1x128", "quant_dual_1x128", "quant_mxfp8",
                              "quant_per_tensor", "quant_nvfp4", "quant_nvfp4_row_4over6", "dequant_1x128",
                              "moe_gate_up", "moe_gather_quant",
                              "moe_swiglu_quant", "moe_quant_then_gather", "moe_layer", "nvfp4",
@@ -827,15 +827,18 @@ def single_kernel(args, torch, fp, dev):
     act, wt = device_inputs(torch, 7, dev)
     ws = fp.workspace(dev)
     name = args.kernel
-    if name in ("fprop", "dgrad", "wgrad"):
-        m, n, k = {"fprop": (M3, I3, H3), "dgrad": (M3, H3, I3), "wgrad": (I3, H3, M3)}[name]
+    if name in ("fprop", "dgrad", "wgrad", "fprop_pow2", "dgrad_pow2", "wgrad_pow2"):
+        g = name.split("_")[0]
+        sfx = "_pow2" if name.endswith("_pow2") else ""
+        m, n, k = {"fprop": (M3, I3, H3), "dgrad": (M3, H3, I3), "wgrad": (I3, H3, M3)}[g]
         a = act((m, k), 0.01, 50.0)
-        b = act((n, k), 0.01, 50.0) if name == "wgrad" else wt((n, k))
-        gb = "1x128" if name == "wgrad" else "128x128"
-        qa, sa, _ = fp.fp8_quantize(a, "1x128", ws=ws)
+        b = act((n, k), 0.01, 50.0) if g == "wgrad" else wt((n, k))
+        ga = "1x128" + sfx
+        gb = ("1x128" if g == "wgrad" else "128x128") + sfx
+        qa, sa, _ = fp.fp8_quantize(a, ga, ws=ws)
         qb, sb, _ = fp.fp8_quantize(b, gb, ws=ws)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        fn = lambda: fp.fp8_block_gemm(qa, sa, "1x128", qb, sb, gb, out=out, ws=ws)  # noqa: E731
+        fn = lambda: fp.fp8_block_gemm(qa, sa, ga, qb, sb, gb, out=out, ws=ws)  # noqa: E731
         work = 2 * m * n * k
     elif name.startswith("quant") or name.startswith("dequant"):
         x = act((8192, 4096), 0.001, 100.0)

@@ -220,8 +220,21 @@ __device__ __forceinline__ void load_row_group(uint32_t* w, const uint8_t* __res
         return;
     }
     const uint8_t* p = src + kb0;
-    if (vec && kb0 + kSfGroup <= nkb) {
-        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
+    if (kb0 + kSfGroup <= nkb) {
+        uint32_t v;
+        if (vec) {
+            v = __ldg(reinterpret_cast<const uint32_t*>(p));
+        } else {
+            // row pitch not a multiple of 4: the aligned word holding p, and
+            // the next one only when p is not aligned (it then holds p[3], a
+            // byte of this group, so the read stays inside the words that
+            // hold the tensor)
+            const uintptr_t ap = reinterpret_cast<uintptr_t>(p);
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(ap & ~static_cast<uintptr_t>(3));
+            const uint32_t sh = 8u * static_cast<uint32_t>(ap & 3u);
+            const uint32_t w0 = __ldg(q);
+            v = sh != 0u ? __funnelshift_r(w0, __ldg(q + 1), sh) : w0;
+        }
 #pragma unroll
         for (int g = 0; g < kSfGroup; ++g) w[g] = ((v >> (8 * g)) & 0xFFu) * 0x01010101u;
     } else {

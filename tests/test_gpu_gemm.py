@@ -459,7 +459,10 @@ def p2_deq(x_f32, gran):
 
 @pytest.mark.parametrize("a_gran,b_gran", [("1x128_pow2", "128x128_pow2"), ("1x128_pow2", "1x128_pow2"),
                                            ("128x128_pow2", "128x128_pow2"), ("128x128_pow2", "1x128_pow2")])
-@pytest.mark.parametrize("m,n,k", [(300, 520, 384), (128, 256, 128), (1, 8, 256), (1000, 1536, 2048)])
+# k = 1152 and 896: 9 and 7 K blocks, so the scale rows' pitch is not a multiple
+# of 4 bytes and the rows start at every byte offset of a word
+@pytest.mark.parametrize("m,n,k", [(300, 520, 384), (128, 256, 128), (1, 8, 256), (1000, 1536, 2048),
+                                   (300, 520, 1152), (130, 264, 896)])
 def test_pow2_blockwise(a_gran, b_gran, m, n, k):
     ab = synth.activations((m, k), seed=m + k + 9, outlier_frac=0.01, outlier_mult=50.0)
     bb = synth.weights((n, k), seed=n + k + 10, std=0.02)
