@@ -271,38 +271,57 @@ __device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, 
             for (int g = 0; g < kSfGroup; ++g) w.b[4 * c][g] = 0u;
         }
     };
-    if (part == 0) {
-#pragma unroll
-        for (int r1 = 0; r1 < 4; ++r1) {
-            const int64_t row = ti.row0 + lane + 32 * r1;
-            const int64_t srow = (SA == 2) ? (row >> 7) : row;
-            load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
-        }
-        if constexpr (SB == 2) {
+    auto arow = [&](int r1) {
+        const int64_t row = ti.row0 + lane + 32 * r1;
+        const int64_t srow = (SA == 2) ? (row >> 7) : row;
+        load_row_group(w.a[r1], p.sa + srow * sf_pitch, kb0, nkb, row < p.m, vec);
+    };
+    // The two loaders take six row words each (per-row B scales) or two A
+    // rows and one B block each (128x128 B blocks): see store_scales_p2.
+    // (every register index a constant: a run-time index would put the
+    // register buffers in local memory)
+    if constexpr (SB == 2) {
+        if (part == 0) {
+            arow(0);
+            arow(1);
             bblock(0);
         } else {
-#pragma unroll
-            for (int r1 = 0; r1 < 4; ++r1) brow(r1);
-        }
-    } else {
-        if constexpr (SB == 2) {
+            arow(2);
+            arow(3);
             bblock(1);
-        } else {
-#pragma unroll
-            for (int r1 = 4; r1 < 8; ++r1) brow(r1);
         }
+    } else if (part == 0) {
+#pragma unroll
+        for (int r1 = 0; r1 < 4; ++r1) arow(r1);
+        brow(0);
+        brow(1);
+    } else {
+#pragma unroll
+        for (int r1 = 2; r1 < 8; ++r1) brow(r1);
     }
 }
 
-// One loader's share of a stage's atoms: part 0 the A atoms and B rows
-// 0..127, part 1 B rows 128..255 (power-of-two scales: one word per row).
-template <int KIND>
-__device__ __forceinline__ void store_scales_part(const ScaleRegs<KIND>& r, uint8_t* sf, int lane, int part) {
+// One loader's share of a stage's atoms (power-of-two scales: one word per
+// row; lane l's 16 bytes of an atom hold rows l, l+32, l+64, l+96).  With
+// per-row B scales part 0 writes the A atom and rows l, l+32 of the first B
+// atom, part 1 the rest of the B atoms; with 128x128 B blocks each part
+// writes half of the A atom and one B atom.  Six loads or three a lane each.
+template <int KIND, int SB>
+__device__ __forceinline__ void store_scales_p2(const ScaleRegs<KIND>& r, uint8_t* sf, int lane, int part) {
     uint8_t* sfb = sf + Cfg<KIND>::A_ATOMS * 512;
-    if (part == 0) {
+    if constexpr (SB == 2) {
+        if (part == 0) {
+            *reinterpret_cast<uint2*>(sf + lane * 16) = make_uint2(r.a[0][0], r.a[1][0]);
+            *reinterpret_cast<uint4*>(sfb + lane * 16) = make_uint4(r.b[0][0], r.b[1][0], r.b[2][0], r.b[3][0]);
+        } else {
+            *reinterpret_cast<uint2*>(sf + lane * 16 + 8) = make_uint2(r.a[2][0], r.a[3][0]);
+            *reinterpret_cast<uint4*>(sfb + 512 + lane * 16) = make_uint4(r.b[4][0], r.b[5][0], r.b[6][0], r.b[7][0]);
+        }
+    } else if (part == 0) {
         *reinterpret_cast<uint4*>(sf + lane * 16) = make_uint4(r.a[0][0], r.a[1][0], r.a[2][0], r.a[3][0]);
-        *reinterpret_cast<uint4*>(sfb + lane * 16) = make_uint4(r.b[0][0], r.b[1][0], r.b[2][0], r.b[3][0]);
+        *reinterpret_cast<uint2*>(sfb + lane * 16) = make_uint2(r.b[0][0], r.b[1][0]);
     } else {
+        *reinterpret_cast<uint2*>(sfb + lane * 16 + 8) = make_uint2(r.b[2][0], r.b[3][0]);
         *reinterpret_cast<uint4*>(sfb + 512 + lane * 16) = make_uint4(r.b[4][0], r.b[5][0], r.b[6][0], r.b[7][0]);
     }
 }
@@ -517,9 +536,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         __syncwarp();
     } else if ((warp == 2 || warp == 3) && KIND == kP2) {
         // ------------------------------------------------------------ scale loaders (power of two)
-        // Both warps walk every stage in order and split the rows: warp 2
-        // writes the A atom and B rows 0..127, warp 3 B rows 128..255 (the
-        // stage's full barrier counts both).  Groups of four stages are
+        // Both warps walk every stage in order and split the rows evenly
+        // (store_scales_p2; the stage's full barrier counts both).  Groups of four stages are
         // loaded one group ahead of the one being written out (two register
         // buffers, the loop unrolled by two so both names are constants).
         const int part = warp - 2;
@@ -559,7 +577,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1, abort, p.status, p.wait_ns)) { ok = false; break; }
                 ScaleRegs<KIND> r;
                 group_stage<KIND>(r, w, g);
-                store_scales_part<KIND>(r, stages + s * STAGE_B + A_BYTES + B_BYTES, lane, part);
+                store_scales_p2<KIND, SB>(r, stages + s * STAGE_B + A_BYTES + B_BYTES, lane, part);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
