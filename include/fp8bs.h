@@ -39,9 +39,10 @@
  *     kernels set (never clear) when a bounded wait gives up, a gathered
  *     token index is out of range or expert offsets are malformed; read it with
  *     fp8bs_read_status and clear it with fp8bs_clear_status.  Bytes
- *     [64, 80) hold the blockwise GEMM's tile counter (its CTAs take tiles
- *     in index order as they become free; the kernel's last CTA puts the
- *     counter back to 0, so it is 0 between calls).  From byte 256 on it is
+ *     [64, 80) hold the GEMMs' tile counter (the FP32-scale forms with
+ *     128x128 or per-tensor B scales and the power-of-two forms: their CTAs
+ *     take tiles in index order as they become free; the kernel's last CTA
+ *     puts the counter back to 0, so it is 0 between calls).  From byte 256 on it is
  *     scratch for the per-tensor / NVFP4 amax reduction.  Calls that share a
  *     workspace must be ordered on the GPU (same stream or events); calls
  *     that run concurrently need a workspace each.
