@@ -14,7 +14,7 @@ against the roofline, plus the CPU oracle on a bounded sample of the step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-For N > 1 the driver launches one rank per GPU with torchrun; every rank
+For N > 1, launch one rank per GPU with torchrun; every rank
 runs its own batch (weak scaling, no collective on the data path) and rank 0
 prints one JSON line.
 """
