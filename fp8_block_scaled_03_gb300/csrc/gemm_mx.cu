@@ -244,7 +244,7 @@ __device__ __forceinline__ void load_row_group(uint32_t* w, const uint8_t* __res
 }
 
 // SA / SB: 1 = one byte per row, 2 = one byte per 128-row block.
-// part 0: A rows and B rows 0..127; part 1: B rows 128..255.
+// part: which of the two loaders (the split of the rows is store_scales_p2's).
 template <int SA, int SB>
 __device__ __forceinline__ void load_scales_group(WideRegs& w, const Params& p, const TileInfo& ti, int64_t kb0,
                                                   int64_t nkb, int lane, int64_t sf_pitch, bool vec, int part) {
