@@ -472,9 +472,10 @@ def test_pow2_blockwise(a_gran, b_gran, m, n, k):
     assert fp.read_status() == 0
 
 
+@pytest.mark.parametrize("k", [384, 1152])   # 1152: 9 K blocks, scale rows at every byte offset of a word
 @pytest.mark.parametrize("counts", [[0, 1, 127, 129, 0, 3, 256, 64], [300], [128] * 12])
-def test_pow2_grouped_ragged(counts):
-    n, k = 264, 384
+def test_pow2_grouped_ragged(counts, k):
+    n = 264
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     rows, e = int(offsets[-1]), len(counts)
     ab = synth.activations((rows, k), seed=rows + 1, outlier_frac=0.01, outlier_mult=50.0)
